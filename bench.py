@@ -1,0 +1,453 @@
+#!/usr/bin/env python
+"""Benchmark of one speculative-decoding selection step on GB300.
+
+A step is one round: the exact top-k over the draft columns plus the fused
+greedy verify over the target columns, issued as ONE spec_round launch.  The
+default workload is 8 lanes x 7 drafts = 56 draft columns x V = 248,046 bf16
+logits with k = 8, and a verify over 8 lanes x 8 target columns.
+
+Prints one JSON line (rank 0).  ``value`` is logit GB/s (bytes of logits read
+per round x rounds / time, all GPUs), ``us_per_round`` the time per round,
+``roofline.frac`` the fraction of the measured HBM copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C2] [--impl ours|reference]
+
+Timing: W untimed warm-up rounds, then exactly K rounds replayed as CUDA
+graphs, bracketed by a barrier and a device synchronisation, timed with CUDA
+events on the launching stream; max over ranks.  Every round reads a
+different copy of the inputs from a ring larger than 4x the L2 cache, so
+the logits come from HBM.  ``e2e`` repeats the metric through the host-buffer
+entry point (spec_round_host): pinned host inputs copied in, outputs copied
+back, every step.  ``cpu_baseline`` times the CPU oracle on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "µs per round and logit GB/s (% of GB300 HBM peak), top-k + greedy verify"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_draft_column_gb300", "csrc", "specsel.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+WORKLOADS = {
+    "C1": "1 lane x 7 drafts: 7 draft columns x V=248,046 bf16 ~N(0,3) + 3 planted peaks, k=8; "
+          "verify 1 lane x 8 target columns",
+    "C2": "8 lanes x 7 drafts = 56 draft columns x V=248,046 bf16 ~N(0,3), k=8; verify 8 lanes x 8 target "
+          "columns (planted argmax), accepted length per lane uniform in 0..7",
+    "C3": "1 lane, gamma 15: 15 draft columns x V=248,046 bf16 quantised to 64 levels (heavy ties), k=20; "
+          "verify 3 lanes x 16 target columns",
+    "C4": "64 lanes x 7 drafts = 448 draft columns x V=248,046 bf16, 90% N(0,2) / 10% one logit +12, k=20; "
+          "verify 64 lanes x 8 target columns",
+    "C5": "256 lanes x 15 drafts = 3,840 draft columns x V=248,046 bf16 ~N(0,3), k={k}; verify 256 lanes x 16 "
+          "target columns",
+}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100_000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--config", default="C2", choices=sorted(WORKLOADS))
+    p.add_argument("--k", type=int, default=None, help="k for C5 (1, 8, 20 or 64)")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        if v > 0:
+            return v, "of measured"
+    except Exception:
+        pass
+    return FALLBACK_HBM_GBS, "of fallback"
+
+
+def source_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(config: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel
+    source has not changed since it was taken (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        e = t.get(config)
+        if e and e.get("source_sha256_16") == source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def make_workload(config: str, k: int | None, seed_offset: int = 0):
+    import synth
+    fn = synth.CONFIGS[config]
+    kw = {}
+    if config == "C5" and k is not None:
+        kw["k"] = k
+    if seed_offset:
+        import inspect
+        kw["seed"] = inspect.signature(fn).parameters["seed"].default + 1000 * seed_offset
+    return fn(**kw)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# multi-process plumbing (one process per GPU; replicas, no data exchange)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return world, rank, local
+
+
+def dist_init(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (plain max when there is one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_round(r, threads: int, cols=None, n: int | None = None):
+    """The oracle over a round (or over columns `cols` cut to their first n
+    elements); returns the logit bytes it read."""
+    import oracle
+    if cols is None:
+        oracle.topk(r.draft, r.k, threads=threads)
+        if r.target is not None:
+            oracle.verify(r.target, r.drafts, threads=threads)
+        return r.logit_bytes()
+    dc, tc = cols
+    nb = 0
+    if len(dc):
+        x = r.draft[dc, :n]
+        oracle.topk(x, min(r.k, x.shape[1]), threads=threads)
+        nb += x.size * 2
+    if len(tc):
+        t = r.target[tc, :n]
+        oracle.argmax(t, threads=threads)
+        nb += t.size * 2
+    return nb
+
+
+def cpu_baseline(r, budget_s: float = 3.0):
+    threads = os.cpu_count() or 1
+    oracle_round(r, threads)                 # warm (page in, build)
+    t0 = time.perf_counter()
+    rounds, nbytes = 0, 0
+    while True:
+        nbytes += oracle_round(r, threads)
+        rounds += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rounds} full rounds of the same workload ({r.cols} top-k columns + "
+                      f"{0 if r.target is None else r.target.shape[0]} verify columns each), "
+                      f"{dt:.2f} s wall on {threads} threads",
+            "us_per_round": round(dt / rounds * 1e6, 1)}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    r = make_workload(args.config, args.k)
+    threads = os.cpu_count() or 1
+    # per-step sample sized so that warm-up + steps stay within ~2 minutes
+    budget = min(0.5, 120.0 / max(1, args.steps + args.warmup))
+    t0 = time.perf_counter()
+    b = oracle_round(r, threads, cols=([0], [0] if r.target is not None else []), n=r.V)
+    per_byte = (time.perf_counter() - t0) / b
+    n_elems = max(64, int(budget / per_byte / 2 / 2))            # two columns per step, 2 bytes each
+    n_elems = min(n_elems, r.V)
+    nt = 0 if r.target is None else r.target.shape[0]
+
+    def step(i):
+        return oracle_round(r, threads, cols=([i % r.cols], [i % nt] if nt else []), n=n_elems)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for i in range(args.steps):
+        nbytes += step(i)
+    dt = time.perf_counter() - t0
+    gbs = nbytes / dt / 1e9
+    sample = (f"each step: the oracle's top-k over the first {n_elems} logits of one draft column"
+              + (" and its argmax over the first {0} logits of one target column".format(n_elems) if nt else "")
+              + f"; {threads} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(args, r, None),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(args, r, ring):
+    desc = WORKLOADS[args.config].format(k=r.k)
+    c = {"workload": f"{args.config}: {desc}", "cols": r.cols, "V": r.V, "k": r.k, "lanes": r.lanes,
+         "gamma": r.gamma, "bytes_per_round": r.logit_bytes(), "parallelism": "replicas (one independent round "
+         "per GPU, no data exchange)"}
+    if ring is not None:
+        c["l2"] = (f"inputs rotated through a ring of {ring[0]} copies ({ring[1] / 1e6:.0f} MB, > 4x the "
+                   f"{ring[2] / 1e6:.0f} MB L2): every round reads its logits from HBM")
+        c["launch"] = "spec_round: one kernel per round; K rounds replayed as CUDA graphs"
+    return c
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_env()
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device (there is no CPU fallback)"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    import speculative_decoding_draft_column_gb300 as sd
+
+    r = make_workload(args.config, args.k, seed_offset=rank)   # independent lanes per GPU
+    cols, V, k, lanes, gamma = r.cols, r.V, r.k, r.lanes, max(r.gamma, 1)
+    bytes_round = r.logit_bytes()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = max(2, math.ceil(4 * l2 / bytes_round))
+    xs = [torch.from_numpy(r.draft.view(np.int16)).to(dev) for _ in range(R)]
+    ts = [torch.from_numpy(r.target.view(np.int16)).to(dev) if lanes else None for _ in range(R)]
+    drafts = torch.from_numpy(r.drafts).to(dev) if lanes else None
+    vals = torch.empty((cols, k), dtype=torch.int16, device=dev)
+    ids = torch.empty((cols, k), dtype=torch.int32, device=dev)
+    acc = torch.empty(max(lanes, 1), dtype=torch.int32, device=dev)
+    com = torch.empty((max(lanes, 1), gamma + 1), dtype=torch.int32, device=dev)
+    sd.spec_reserve(cols, k, lanes, gamma)
+    stream = torch.cuda.Stream(device=dev)
+
+    def one(i):
+        sd.spec_round(xs[i % R], cols, V, k, vals, ids, ts[i % R], drafts, lanes, gamma, acc, com)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            one(i)
+    stream.synchronize()
+
+    K = args.steps
+    chunk = min(K, R * max(1, 1000 // R))
+    n_full, rem = divmod(K, chunk)
+    graphs = []
+    c0 = sd.spec_launch_count()
+    for n in ([chunk] + ([rem] if rem else [])):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                one(i)
+        graphs.append(g)
+    captured = sd.spec_launch_count() - c0
+    assert captured == chunk + rem
+    with torch.cuda.stream(stream):
+        graphs[0].replay()                   # untimed: upload / warm the graph
+    stream.synchronize()
+
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n_full):
+            graphs[0].replay()
+        if rem:
+            graphs[1].replay()
+        e1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    barrier(world, dev)
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(ms, world, dev)
+    launches = n_full * chunk + rem
+
+    # end to end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        hd = pin(r.draft.view(np.int16))
+        ht = pin(r.target.view(np.int16)) if lanes else None
+        hdr = pin(r.drafts) if lanes else None
+        hv = torch.empty((cols, k), dtype=torch.int16).pin_memory()
+        hi = torch.empty((cols, k), dtype=torch.int32).pin_memory()
+        ha = torch.empty(max(lanes, 1), dtype=torch.int32).pin_memory()
+        hc = torch.empty((max(lanes, 1), gamma + 1), dtype=torch.int32).pin_memory()
+        sd.spec_set_stream(stream)
+
+        def host_step():
+            sd.lib.spec_round_host(hd.data_ptr(), cols, V, k, hv.data_ptr(), hi.data_ptr(),
+                                   ht.data_ptr() if lanes else None, hdr.data_ptr() if lanes else None, lanes,
+                                   gamma, ha.data_ptr() if lanes else None, hc.data_ptr() if lanes else None)
+
+        for _ in range(5):
+            host_step()
+        n_e2e = max(20, min(K, 300))
+        barrier(world, dev)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            host_step()
+        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+        if sd.spec_last_error():
+            raise RuntimeError(sd.spec_last_error())
+        h2d = r.draft.nbytes + (r.target.nbytes + r.drafts.nbytes if lanes else 0)
+        d2h = vals.numel() * 2 + ids.numel() * 4 + (acc.numel() * 4 + com.numel() * 4 if lanes else 0)
+        e2e = {"value": round(world * bytes_round * n_e2e / dt / 1e9, 2), "unit": "GB/s",
+               "us_per_round": round(dt / n_e2e * 1e6, 2), "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
+               "api": "spec_round_host (pinned host buffers; H2D, kernel, D2H, stream sync per step)"}
+
+    if rank != 0:
+        return 0
+    peak, peak_src = hbm_peak()
+    us_round = ms_max * 1e3 / K
+    gbs = world * bytes_round * K / (ms_max * 1e-3) / 1e9
+    per_launch_us = ms * 1e3 / launches
+    achieved = bytes_round / (per_launch_us * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / K, 6), "us_per_round": round(us_round, 3),
+        "pct_of_hbm_peak": round(100 * gbs / world / peak, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; see synth/)",
+        "config": workload_config(args, r, (R, R * bytes_round, l2)),
+        "roofline": {"bound": "hbm", "kernel": "spec_round_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                     "traffic": recorded_traffic(args.config), "algorithmic_bytes_per_launch": bytes_round,
+                     "launch_us": round(per_launch_us, 3),
+                     "timing": "CUDA events around K graph-replayed launches on the launching stream; "
+                               "per-launch time includes the graph's inter-launch gap"},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(r)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,161 @@
+/*
+ * specsel.h -- C ABI of libspecsel.so: the selection step of one
+ * speculative-decoding round on one NVIDIA GB300 (sm_103a).
+ *
+ * Two operations, from "A drafter inside the artifact" (Ignis DFlash2 page):
+ *
+ *   top-k   section "How it works", third paragraph: for each draft column,
+ *           keep the k largest bf16 logits, largest first, ties going to
+ *           the smaller row (token) id.  The kernel splits the vocabulary
+ *           axis of every column across CTAs, filters 16-byte vectors
+ *           against a running k-th value held in registers, and merges the
+ *           per-CTA lists in the last CTA to finish a column -- the logits
+ *           are read from HBM exactly once.
+ *
+ *   verify  section "How it works", first paragraph: a verify round runs
+ *           every lane's anchor plus its drafts through the target model
+ *           once; each lane commits the longest run of drafts the target
+ *           itself would have picked, plus the target's own next token.
+ *           Under greedy decoding ("Speculative decoding, measured on my M4
+ *           Max", section 1) "would have picked" is the target argmax.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - bf16 values travel as uint16_t bit patterns.  Values compare as
+ *    numbers: -0 and +0 tie, +-Inf are ordinary values.  NaN is outside the
+ *    contract; the result for a column holding NaN is unspecified (but the
+ *    call still returns and touches only its own outputs).
+ *  - All data pointers are DEVICE pointers owned by the caller, except in
+ *    spec_round_host.  The library keeps no reference after return.
+ *  - Work is enqueued asynchronously on the calling thread's current stream
+ *    (spec_set_stream; default: the legacy default stream 0).  Results are
+ *    valid once that stream reaches the enqueued work.
+ *  - Return value: SPEC_OK (0) or a negative SPEC_ERR_* code; argument
+ *    errors are found on the host before anything is enqueued, and nothing
+ *    is written.  spec_last_error() gives a message for the calling thread.
+ *  - cols == 0 / lanes == 0 is a no-op that returns SPEC_OK.
+ *  - Scratch: the library owns one scratch area per device (per-column
+ *    tickets and partial lists, a few MB at most).  It grows on demand with
+ *    cudaMalloc outside stream capture; inside a capture a call that needs
+ *    more than spec_reserve set aside fails with SPEC_ERR_ALLOC.  Calls that
+ *    may run concurrently on the GPU (different streams, or different host
+ *    threads) share this scratch and race: issue them on one stream.
+ *  - Outputs must not alias inputs.
+ */
+#ifndef SPECSEL_H
+#define SPECSEL_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int spec_status;
+
+#define SPEC_OK 0
+#define SPEC_ERR_ARG (-1)    /* bad argument (null pointer, size, alignment, k, gamma) */
+#define SPEC_ERR_ALLOC (-2)  /* scratch could not be obtained (incl. during capture) */
+#define SPEC_ERR_CUDA (-3)   /* a CUDA runtime error; spec_last_error() has its text */
+
+/* Vocabulary of the drafter's and target's output head: 248,046 tokens
+   (same page, "How it works", third paragraph). spec_verify assumes it. */
+#define SPEC_VOCAB 248046
+/* Largest k: 64.  Largest gamma (drafts per lane): 15, the draft width of a
+   block size of 16 ("Apathy-Qwen3.8-27B-DFlash-drafter-v2" model card:
+   trained drafts = block_size - 1, and a larger gamma is refused). */
+#define SPEC_MAX_K 64
+#define SPEC_MAX_GAMMA 15
+
+/* Per-column exact top-k.
+ *   logits    bf16 [cols][V], row-major, contiguous, 2-byte aligned.  Column
+ *             c starts at logits + c*V (any 16-byte phase is accepted).
+ *   cols      number of draft columns, >= 0.
+ *   V         vocabulary size, 1 <= V <= 2^31-1.
+ *   k         1 <= k <= min(V, 64).
+ *   out_vals  bf16 [cols][k]: the selected values, largest first; each is
+ *             the selected element's own bit pattern.
+ *   out_ids   int32 [cols][k]: their ids in [0, V); equal values appear in
+ *             ascending id order.
+ * Errors: SPEC_ERR_ARG for a null pointer with cols > 0, V < 1, k out of
+ * range, or a misaligned pointer; SPEC_ERR_ALLOC; SPEC_ERR_CUDA. */
+spec_status spec_topk(const uint16_t *logits, int64_t cols, int64_t V, int32_t k,
+                      uint16_t *out_vals, int32_t *out_ids);
+
+/* Shortlist top-k ("How it works", second paragraph: an opt-in head over
+ * the 131,072 most frequent tokens).  As spec_topk over [cols][V] shortlist
+ * logits, where local id i stands for vocabulary id id_map[i]:
+ *   id_map    int32 [V], device, injective (distinct entries), values >= 0.
+ *   out_ids   vocabulary ids id_map[i]; ties go to the smaller VOCABULARY id.
+ * Duplicate entries in id_map are outside the contract. */
+spec_status spec_topk_mapped(const uint16_t *logits, int64_t cols, int64_t V, int32_t k,
+                             const int32_t *id_map, uint16_t *out_vals, int32_t *out_ids);
+
+/* Greedy verify over V = SPEC_VOCAB.
+ *   target_logits  bf16 [lanes][gamma+1][V], contiguous.  Column j of a lane
+ *                  is the target's next-token logits after the anchor and
+ *                  the first j drafts (j = 0 is the anchor's own).
+ *   drafts         int32 [lanes][gamma]: draft i is the token proposed for
+ *                  the position target column i predicts.  Ids outside
+ *                  [0, V) are not errors; they never match.
+ *   lanes >= 0, 1 <= gamma <= 15.
+ *   out_accept_len int32 [lanes]: a = the longest prefix with
+ *                  drafts[l][i] == argmax(target column i), 0 <= a <= gamma.
+ *   out_commit_ids int32 [lanes][gamma+1]: argmax of columns 0..a (the a
+ *                  accepted drafts, then the bonus token), -1 after.
+ *   The argmax breaks ties toward the smaller id.  Target logits are read
+ *   once; argmax and prefix match happen in the same launch. */
+spec_status spec_verify(const uint16_t *target_logits, const int32_t *drafts, int64_t lanes,
+                        int32_t gamma, int32_t *out_accept_len, int32_t *out_commit_ids);
+
+/* spec_verify with an explicit vocabulary size V (1 <= V <= 2^31-1). */
+spec_status spec_verify_v(const uint16_t *target_logits, const int32_t *drafts, int64_t lanes,
+                          int32_t gamma, int64_t V, int32_t *out_accept_len,
+                          int32_t *out_commit_ids);
+
+/* One whole selection step in ONE kernel launch: spec_topk over the draft
+ * columns and spec_verify_v over the target columns, same vocabulary V.
+ * Results are identical to the two separate calls.  Either part may be
+ * empty (cols == 0 or lanes == 0). */
+spec_status spec_round(const uint16_t *draft_logits, int64_t cols, int64_t V, int32_t k,
+                       uint16_t *out_vals, int32_t *out_ids,
+                       const uint16_t *target_logits, const int32_t *drafts, int64_t lanes,
+                       int32_t gamma, int32_t *out_accept_len, int32_t *out_commit_ids);
+
+/* spec_round for callers holding HOST buffers: every pointer is a host
+ * pointer (pinned memory copies fastest).  The call copies the inputs to
+ * library-owned device staging memory, runs spec_round, copies the outputs
+ * back and waits for the stream, so outputs are valid on return.  Staging
+ * grows with cudaMalloc as needed (not capturable). */
+spec_status spec_round_host(const uint16_t *draft_logits, int64_t cols, int64_t V, int32_t k,
+                            uint16_t *out_vals, int32_t *out_ids,
+                            const uint16_t *target_logits, const int32_t *drafts, int64_t lanes,
+                            int32_t gamma, int32_t *out_accept_len, int32_t *out_commit_ids);
+
+/* Set the stream (a cudaStream_t, may be NULL for the legacy default stream)
+ * that the calling thread's subsequent calls enqueue on.  Thread-local. */
+spec_status spec_set_stream(void *stream);
+void *spec_get_stream(void);
+
+/* Make sure the current device's scratch covers calls up to these sizes
+ * (so that later calls need no allocation, e.g. inside a CUDA graph
+ * capture).  max_cols counts draft columns, max_lanes/max_gamma the verify
+ * part.  Synchronises the device if it has to reallocate. */
+spec_status spec_reserve(int64_t max_cols, int32_t max_k, int64_t max_lanes, int32_t max_gamma);
+
+/* Free the scratch and staging of the current device (after synchronising
+ * it).  Later calls allocate again. */
+spec_status spec_release(void);
+
+/* Text of the last error raised on the calling thread ("" if none). */
+const char *spec_last_error(void);
+
+/* Number of kernel launches this process made through the library (all
+ * devices, all threads).  One per spec_topk / spec_verify / spec_round. */
+int64_t spec_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECSEL_H */

@@ -1,0 +1,217 @@
+"""Python binding of libspecsel (the C ABI declared in ``include/specsel.h``).
+
+Argument marshalling only: every function below with a C name forwards its
+arguments to the C entry point of the same name -- device tensors become
+device pointers, and the call is enqueued on PyTorch's current CUDA stream.
+All selection work runs in the CUDA kernels of ``csrc/specsel.cu``; there
+is no CPU or PyTorch fallback.  If the shared library has not been built
+(``__graft_entry__.build()``), importing this package raises ImportError.
+
+Tensor conventions: bf16 logits may be ``torch.bfloat16`` or a 16-bit
+integer view of the same bits; ids and lengths are ``torch.int32``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+__all__ = [
+    "SPEC_OK", "SPEC_ERR_ARG", "SPEC_ERR_ALLOC", "SPEC_ERR_CUDA", "SPEC_VOCAB", "SPEC_MAX_K",
+    "SPEC_MAX_GAMMA", "SpecError", "LIB_PATH", "lib",
+    "spec_topk", "spec_topk_mapped", "spec_verify", "spec_verify_v", "spec_round", "spec_round_host",
+    "spec_set_stream", "spec_get_stream", "spec_reserve", "spec_release", "spec_last_error",
+    "spec_launch_count", "topk", "topk_mapped", "verify", "round_step", "EXPORTS",
+]
+
+SPEC_OK, SPEC_ERR_ARG, SPEC_ERR_ALLOC, SPEC_ERR_CUDA = 0, -1, -2, -3
+SPEC_VOCAB, SPEC_MAX_K, SPEC_MAX_GAMMA = 248_046, 64, 15
+LIB_PATH = _build.LIB
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+                      "(the selection kernels have no CPU fallback)")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_p, _i64, _i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+_SIGS = {
+    "spec_topk": [_p, _i64, _i64, _i32, _p, _p],
+    "spec_topk_mapped": [_p, _i64, _i64, _i32, _p, _p, _p],
+    "spec_verify": [_p, _p, _i64, _i32, _p, _p],
+    "spec_verify_v": [_p, _p, _i64, _i32, _i64, _p, _p],
+    "spec_round": [_p, _i64, _i64, _i32, _p, _p, _p, _p, _i64, _i32, _p, _p],
+    "spec_round_host": [_p, _i64, _i64, _i32, _p, _p, _p, _p, _i64, _i32, _p, _p],
+    "spec_set_stream": [_p],
+    "spec_get_stream": [],
+    "spec_reserve": [_i64, _i32, _i64, _i32],
+    "spec_release": [],
+    "spec_last_error": [],
+    "spec_launch_count": [],
+}
+EXPORTS = tuple(_SIGS)
+for _name, _args in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.argtypes = _args
+    _f.restype = ctypes.c_int
+lib.spec_get_stream.restype = ctypes.c_void_p
+lib.spec_last_error.restype = ctypes.c_char_p
+lib.spec_launch_count.restype = ctypes.c_int64
+
+
+class SpecError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"status {status}: {message}")
+        self.status = status
+
+
+def _check(status: int) -> None:
+    if status != SPEC_OK:
+        raise SpecError(status, lib.spec_last_error().decode(errors="replace"))
+
+
+def _ptr(x):
+    """Device tensor -> pointer; None -> NULL; int -> itself."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _use_torch_stream():
+    import torch
+    if torch.cuda.is_available():
+        lib.spec_set_stream(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+# ---- same-name wrappers of the C entry points ------------------------------
+
+def spec_topk(logits, cols, V, k, out_vals, out_ids):
+    _use_torch_stream()
+    _check(lib.spec_topk(_ptr(logits), cols, V, k, _ptr(out_vals), _ptr(out_ids)))
+
+
+def spec_topk_mapped(logits, cols, V, k, id_map, out_vals, out_ids):
+    _use_torch_stream()
+    _check(lib.spec_topk_mapped(_ptr(logits), cols, V, k, _ptr(id_map), _ptr(out_vals), _ptr(out_ids)))
+
+
+def spec_verify(target_logits, drafts, lanes, gamma, out_accept_len, out_commit_ids):
+    _use_torch_stream()
+    _check(lib.spec_verify(_ptr(target_logits), _ptr(drafts), lanes, gamma, _ptr(out_accept_len),
+                           _ptr(out_commit_ids)))
+
+
+def spec_verify_v(target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids):
+    _use_torch_stream()
+    _check(lib.spec_verify_v(_ptr(target_logits), _ptr(drafts), lanes, gamma, V, _ptr(out_accept_len),
+                             _ptr(out_commit_ids)))
+
+
+def spec_round(draft_logits, cols, V, k, out_vals, out_ids, target_logits, drafts, lanes, gamma,
+               out_accept_len, out_commit_ids):
+    _use_torch_stream()
+    _check(lib.spec_round(_ptr(draft_logits), cols, V, k, _ptr(out_vals), _ptr(out_ids), _ptr(target_logits),
+                          _ptr(drafts), lanes, gamma, _ptr(out_accept_len), _ptr(out_commit_ids)))
+
+
+def spec_round_host(draft_logits, cols, V, k, out_vals, out_ids, target_logits, drafts, lanes, gamma,
+                    out_accept_len, out_commit_ids):
+    """Host buffers (CPU tensors, ideally pinned, or numpy arrays) in and out."""
+    _use_torch_stream()
+    hp = lambda a: None if a is None else (a.ctypes.data if hasattr(a, "ctypes") else a.data_ptr())
+    _check(lib.spec_round_host(hp(draft_logits), cols, V, k, hp(out_vals), hp(out_ids), hp(target_logits),
+                               hp(drafts), lanes, gamma, hp(out_accept_len), hp(out_commit_ids)))
+
+
+def spec_set_stream(stream):
+    """``stream``: a torch.cuda.Stream, a raw cudaStream_t (int) or None."""
+    h = getattr(stream, "cuda_stream", stream)
+    _check(lib.spec_set_stream(None if h is None else ctypes.c_void_p(h)))
+
+
+def spec_get_stream():
+    return lib.spec_get_stream()
+
+
+def spec_reserve(max_cols, max_k, max_lanes, max_gamma):
+    _check(lib.spec_reserve(max_cols, max_k, max_lanes, max_gamma))
+
+
+def spec_release():
+    _check(lib.spec_release())
+
+
+def spec_last_error() -> str:
+    return lib.spec_last_error().decode(errors="replace")
+
+
+def spec_launch_count() -> int:
+    return int(lib.spec_launch_count())
+
+
+# ---- allocating conveniences (outputs created with torch, work in the kernels)
+
+def _check_logits(x, name):
+    import torch
+    if not x.is_cuda or x.dim() != 2 or not x.is_contiguous() or x.element_size() != 2:
+        raise ValueError(f"{name}: need a contiguous 2-D CUDA tensor of 16-bit elements")
+    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise ValueError(f"{name}: dtype {x.dtype} is not bf16 bits")
+
+
+def topk(logits, k: int):
+    """(vals bf16 [cols,k], ids int32 [cols,k]) for a [cols, V] CUDA tensor."""
+    import torch
+    _check_logits(logits, "logits")
+    cols, V = logits.shape
+    vals = torch.empty((cols, k), dtype=logits.dtype, device=logits.device)
+    ids = torch.empty((cols, k), dtype=torch.int32, device=logits.device)
+    spec_topk(logits, cols, V, k, vals, ids)
+    return vals, ids
+
+
+def topk_mapped(logits, k: int, id_map):
+    import torch
+    _check_logits(logits, "logits")
+    cols, V = logits.shape
+    if id_map.dtype != torch.int32 or id_map.numel() != V or not id_map.is_cuda:
+        raise ValueError("id_map: need an int32 CUDA tensor with V entries")
+    vals = torch.empty((cols, k), dtype=logits.dtype, device=logits.device)
+    ids = torch.empty((cols, k), dtype=torch.int32, device=logits.device)
+    spec_topk_mapped(logits, cols, V, k, id_map, vals, ids)
+    return vals, ids
+
+
+def verify(target_logits, drafts):
+    """target [lanes*(gamma+1), V], drafts int32 [lanes, gamma] -> (accept_len, commit_ids)."""
+    import torch
+    _check_logits(target_logits, "target_logits")
+    lanes, gamma = drafts.shape
+    V = target_logits.shape[1]
+    if target_logits.shape[0] != lanes * (gamma + 1) or drafts.dtype != torch.int32 or not drafts.is_contiguous():
+        raise ValueError("shape mismatch between target_logits and drafts")
+    acc = torch.empty(lanes, dtype=torch.int32, device=drafts.device)
+    com = torch.empty((lanes, gamma + 1), dtype=torch.int32, device=drafts.device)
+    spec_verify_v(target_logits, drafts, lanes, gamma, V, acc, com)
+    return acc, com
+
+
+def round_step(draft_logits, k: int, target_logits, drafts):
+    """One fused launch: (vals, ids, accept_len, commit_ids)."""
+    import torch
+    _check_logits(draft_logits, "draft_logits")
+    _check_logits(target_logits, "target_logits")
+    cols, V = draft_logits.shape
+    lanes, gamma = drafts.shape
+    if target_logits.shape != (lanes * (gamma + 1), V):
+        raise ValueError("target_logits must be [lanes*(gamma+1), V] with the drafts' V")
+    dev = draft_logits.device
+    vals = torch.empty((cols, k), dtype=draft_logits.dtype, device=dev)
+    ids = torch.empty((cols, k), dtype=torch.int32, device=dev)
+    acc = torch.empty(lanes, dtype=torch.int32, device=dev)
+    com = torch.empty((lanes, gamma + 1), dtype=torch.int32, device=dev)
+    spec_round(draft_logits, cols, V, k, vals, ids, target_logits, drafts, lanes, gamma, acc, com)
+    return vals, ids, acc, com

@@ -1,0 +1,46 @@
+"""Build ``libspecsel.so`` in-tree with nvcc for sm_103a (GB300)."""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+SRC = os.path.join(PKG, "csrc", "specsel.cu")
+HDR = os.path.join(ROOT, "include", "specsel.h")
+LIB = os.path.join(PKG, "libspecsel.so")
+
+ARCH = "-gencode=arch=compute_103a,code=sm_103a"
+
+
+def nvcc() -> str:
+    for c in (os.environ.get("CUDA_HOME", ""), "/usr/local/cuda"):
+        p = os.path.join(c, "bin", "nvcc") if c else ""
+        if p and os.path.exists(p):
+            return p
+    p = shutil.which("nvcc")
+    if not p:
+        raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libspecsel")
+    return p
+
+
+def command(out: str = LIB, src: str = SRC, extra: tuple[str, ...] = ()) -> list[str]:
+    return [nvcc(), "-O3", "-std=c++17", ARCH, "-lineinfo", "-Xcompiler", "-fPIC", "-shared",
+            "-cudart", "shared", "-I", os.path.join(ROOT, "include"), *extra, "-o", out, src]
+
+
+def stale(out: str = LIB) -> bool:
+    if not os.path.exists(out):
+        return True
+    t = os.path.getmtime(out)
+    return any(os.path.getmtime(p) > t for p in (SRC, HDR))
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    if force or stale():
+        cmd = command()
+        if verbose:
+            print(" ".join(cmd), flush=True)
+        subprocess.run(cmd, check=True)
+    return LIB

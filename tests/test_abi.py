@@ -1,0 +1,81 @@
+"""The C ABI library: builds, loads, exports every declared symbol, and
+rejects bad arguments on the host before touching the GPU (no GPU needed)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specsel.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_0-9]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def sd():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    import __graft_entry__ as g
+    g._load_build_module().build()
+    import speculative_decoding_draft_column_gb300 as sd
+    return sd
+
+
+def test_every_declared_symbol_is_exported(sd):
+    names = declared_functions()
+    assert len(names) >= 12, names
+    raw = ctypes.CDLL(sd.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), f"{n} declared in specsel.h but not exported"
+    assert set(names) == set(sd.EXPORTS), "Python binding and header disagree"
+
+
+def test_host_argument_checks(sd):
+    lib = sd.lib
+    P = 0x100000          # never dereferenced: every call below fails its checks first
+    A = sd.SPEC_ERR_ARG
+    assert lib.spec_topk(None, 1, 10, 3, P, P) == A
+    assert lib.spec_topk(P, 1, 10, 0, P, P) == A
+    assert lib.spec_topk(P, 1, 10, 11, P, P) == A
+    assert lib.spec_topk(P, 1, 100, 65, P, P) == A
+    assert lib.spec_topk(P, 1, 0, 1, P, P) == A
+    assert lib.spec_topk(P, -1, 10, 1, P, P) == A
+    assert lib.spec_topk(P + 1, 1, 10, 1, P, P) == A        # logits not 2-byte aligned
+    assert lib.spec_topk(P, 1, 10, 1, P, P + 2) == A        # ids not 4-byte aligned
+    assert "aligned" in sd.spec_last_error()
+    assert lib.spec_topk_mapped(P, 1, 10, 2, None, P, P) == A
+    assert lib.spec_verify(P, P, 1, 0, P, P) == A
+    assert lib.spec_verify(P, P, 1, 16, P, P) == A
+    assert lib.spec_verify(None, P, 1, 7, P, P) == A
+    assert lib.spec_verify_v(P, P, 1, 7, 0, P, P) == A
+    assert lib.spec_round(P, 1, 10, 3, P, P, P, P, 1, 16, P, P) == A
+    assert "gamma" in sd.spec_last_error()
+    assert lib.spec_reserve(10, 65, 1, 1) == A
+    # empty problems are no-ops that succeed without any CUDA call
+    assert lib.spec_topk(None, 0, 10, 3, None, None) == sd.SPEC_OK
+    assert lib.spec_verify(None, None, 0, 7, None, None) == sd.SPEC_OK
+    assert lib.spec_round(None, 0, 10, 3, None, None, None, None, 0, 7, None, None) == sd.SPEC_OK
+    assert sd.spec_last_error() == ""
+    assert sd.spec_launch_count() == 0
+
+
+def test_python_binding_raises(sd):
+    with pytest.raises(sd.SpecError) as ei:
+        sd.spec_topk(None, 1, 10, 3, None, None)
+    assert ei.value.status == sd.SPEC_ERR_ARG
+
+
+def test_stream_is_thread_local(sd):
+    import threading
+    sd.lib.spec_set_stream(ctypes.c_void_p(0x1234))
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(sd.lib.spec_get_stream()))
+    t.start(); t.join()
+    assert sd.lib.spec_get_stream() == 0x1234 and seen == [None]
+    sd.lib.spec_set_stream(None)

@@ -1,0 +1,290 @@
+"""CUDA path vs the CPU oracle, element by element and bit-exact: top-k ids and
+bf16 bits, accept lengths and committed ids.  Every call goes through the C
+ABI (via the thin binding).  Needs a GPU."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__ as g
+    g._load_build_module().build()
+    oracle.load()
+    import speculative_decoding_draft_column_gb300 as sd
+    return sd
+
+
+# ---------------------------------------------------------------------------
+# the five workloads
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["C1", "C2", "C3", "C4"])
+def test_workload_full_size(name):
+    r = synth.CONFIGS[name]()
+    want_t = oracle.topk(r.draft, r.k)
+    want_v = oracle.verify(r.target, r.drafts)
+    gu.assert_topk_equal(gu.run_topk(r.draft, r.k), want_t, f"{name} spec_topk")
+    gu.assert_verify_equal(gu.run_verify(r.target, r.drafts), want_v, f"{name} spec_verify")
+    v, i, a, c = gu.run_round(r.draft, r.k, r.target, r.drafts)
+    gu.assert_topk_equal((v, i), want_t, f"{name} spec_round top-k")
+    gu.assert_verify_equal((a, c), want_v, f"{name} spec_round verify")
+    assert want_v[0].tolist() == r.planted_accept.tolist()
+    if r.planted_draft_top is not None:
+        assert np.array_equal(i[:, :3], r.planted_draft_top)
+
+
+@pytest.mark.parametrize("k", [1, 8, 20, 64])
+def test_c5_k_sweep_reduced(k):
+    r = synth.make_c5(k=k, lanes=24, gamma=15, cols=480)
+    gu.assert_topk_equal(gu.run_topk(r.draft, k), oracle.topk(r.draft, k), f"C5 k={k}")
+    v, i, a, c = gu.run_round(r.draft, k, r.target, r.drafts)
+    gu.assert_topk_equal((v, i), oracle.topk(r.draft, k), f"C5 round k={k}")
+    gu.assert_verify_equal((a, c), oracle.verify(r.target, r.drafts), f"C5 round verify k={k}")
+    assert a.tolist() == r.planted_accept.tolist()
+
+
+def _torch_topk_properties(x_dev, V, k, vals, ids):
+    """Properties that hold at any size, checked on the device for every
+    column: ids distinct and in range, values are the elements' own bits,
+    non-increasing, ties ascending, and nothing omitted beats the last one."""
+    import torch
+    cols = x_dev.shape[0]
+    idl = ids.long()
+    assert int(idl.min()) >= 0 and int(idl.max()) < V
+    srt = torch.sort(idl, dim=1).values
+    assert bool((srt[:, 1:] != srt[:, :-1]).all()), "duplicate ids"
+    got_bits = torch.gather(x_dev, 1, idl)
+    assert torch.equal(got_bits, vals), "values are not the selected elements' bits"
+    xf = (x_dev.to(torch.int32) & 0xFFFF).bitwise_left_shift(16).view(torch.float32)
+    vf = (vals.to(torch.int32) & 0xFFFF).bitwise_left_shift(16).view(torch.float32)
+    assert bool((vf[:, 1:] <= vf[:, :-1]).all()), "values not non-increasing"
+    tie = vf[:, 1:] == vf[:, :-1]
+    assert bool(((idl[:, 1:] > idl[:, :-1]) | ~tie).all()), "ties not in ascending id order"
+    last = vf[:, -1:]
+    gt = (xf > last).sum(dim=1)
+    assert bool((gt <= k - 1).all()), "an element above the last selected value was omitted"
+    eq_before = ((xf == last) & (torch.arange(V, device=x_dev.device)[None, :] < idl[:, -1:])).sum(dim=1)
+    sel_eq_before = ((vf == last) & (idl < idl[:, -1:])).sum(dim=1)
+    assert torch.equal(eq_before, sel_eq_before), "an omitted tie has a smaller id"
+    del cols
+
+
+def test_c5_full_size_sampled():
+    """3,840 x 248,046 draft columns (k = 64) and 256 x 16 verify columns in
+    one launch; every column checked by properties on the device, 64 sampled
+    columns and every verify lane against the oracle."""
+    import torch
+    sd = gu.sd_module()
+    r = synth.make_c5(k=64)
+    cols, V, k = r.cols, r.V, r.k
+    x = gu.dev_u16(r.draft)
+    t = gu.dev_u16(r.target)
+    vals = torch.empty((cols, k), dtype=torch.int16, device="cuda")
+    ids = torch.empty((cols, k), dtype=torch.int32, device="cuda")
+    acc = torch.empty(r.lanes, dtype=torch.int32, device="cuda")
+    com = torch.empty((r.lanes, r.gamma + 1), dtype=torch.int32, device="cuda")
+    sd.spec_round(x, cols, V, k, vals, ids, t, gu.dev_i32(r.drafts), r.lanes, r.gamma, acc, com)
+    torch.cuda.synchronize()
+    for c0 in range(0, cols, 256):
+        _torch_topk_properties(x[c0:c0 + 256], V, k, vals[c0:c0 + 256], ids[c0:c0 + 256])
+    pick = np.sort(synth.rng(99, 0).choice(cols, size=64, replace=False))
+    wv, wi = oracle.topk(r.draft[pick], k)
+    gu.assert_topk_equal((vals.cpu().numpy().view(np.uint16)[pick], ids.cpu().numpy()[pick]), (wv, wi), "C5 sampled")
+    gu.assert_verify_equal((acc.cpu().numpy(), com.cpu().numpy()), oracle.verify(r.target, r.drafts), "C5 verify")
+    assert acc.cpu().numpy().tolist() == r.planted_accept.tolist()
+
+
+@pytest.mark.parametrize("k", [1, 8, 20, 64])
+def test_c5_shortlist_reduced(k):
+    r = synth.make_c5s(k=k, cols=384)
+    got = gu.run_topk(r.draft, k, id_map=r.id_map)
+    gu.assert_topk_equal(got, oracle.topk_mapped(r.draft, k, r.id_map), f"C5s k={k}")
+
+
+def test_c5_shortlist_full_size_sampled():
+    import torch
+    sd = gu.sd_module()
+    r = synth.make_c5s(k=20)
+    cols, V, k = r.cols, r.V, r.k
+    x = gu.dev_u16(r.draft)
+    vals = torch.empty((cols, k), dtype=torch.int16, device="cuda")
+    ids = torch.empty((cols, k), dtype=torch.int32, device="cuda")
+    sd.spec_topk_mapped(x, cols, V, k, gu.dev_i32(r.id_map), vals, ids)
+    torch.cuda.synchronize()
+    pick = np.sort(synth.rng(98, 0).choice(cols, size=96, replace=False))
+    gu.assert_topk_equal((vals.cpu().numpy().view(np.uint16)[pick], ids.cpu().numpy()[pick]),
+                         oracle.topk_mapped(r.draft[pick], k, r.id_map), "C5s sampled")
+    # every column: mapped ids lie in the map's image and values match
+    inv = torch.full((synth.VOCAB,), -1, dtype=torch.int64, device="cuda")
+    inv[gu.dev_i32(r.id_map).long()] = torch.arange(V, device="cuda")
+    loc = inv[ids.long()]
+    assert int(loc.min()) >= 0
+    assert torch.equal(torch.gather(x, 1, loc), vals)
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------
+
+EDGE_V = [1, 2, 7, 8, 9, 15, 16, 17, 255, 256, 257, 2047, 2048, 2049, 65535, 65536, 65537, 131072, 248046]
+EDGE_K = [1, 2, 7, 8, 20, 32, 33, 64]
+
+
+def _edge_block(kind: int, seed: int, cols: int, V: int) -> np.ndarray:
+    if kind == 0:
+        return synth.random_bits_block(seed, cols, V)
+    if kind == 1:
+        return synth.levels_block(seed, cols, V, [-1.0, -0.0, 0.0, 3.0, float("inf")])
+    if kind == 2:
+        return np.full((cols, V), synth.bf16_bits(-2.25), dtype=np.uint16)
+    return synth._draft_block(seed, cols, V, 3.0, quant=True)
+
+
+@pytest.mark.parametrize("V", EDGE_V)
+def test_topk_edge_sweep(V):
+    n = 0
+    for k in EDGE_K + [V]:
+        if k > V or k > 64:
+            continue
+        for cols in (1, 7):
+            kind = (n + V) % 4
+            off = (n * 3 + V) % 8
+            x = _edge_block(kind, 1000 + n + V, cols, V)
+            gu.assert_topk_equal(gu.run_topk(x, k, offset=off), oracle.topk(x, k),
+                                 f"V={V} k={k} cols={cols} kind={kind} offset={off}")
+            n += 1
+
+
+@pytest.mark.parametrize("offset", range(8))
+def test_every_16_byte_phase(offset):
+    x = synth.random_bits_block(77 + offset, 9, 20_011)
+    gu.assert_topk_equal(gu.run_topk(x, 20, offset=offset), oracle.topk(x, 20), f"offset {offset}")
+
+
+def test_many_columns_tiny_v():
+    x = synth.levels_block(5, 3000, 5, [0.0, 1.0, -0.0])
+    gu.assert_topk_equal(gu.run_topk(x, 3), oracle.topk(x, 3), "3000 x 5")
+
+
+def test_ties_everywhere_large():
+    x = np.full((56, 248_046), synth.bf16_bits(1.5), dtype=np.uint16)
+    for k in (1, 8, 64):
+        v, i = gu.run_topk(x, k)
+        assert np.all(i == np.arange(k)[None, :]) and np.all(v == synth.bf16_bits(1.5))
+
+
+def test_signed_zero_and_inf():
+    V = 70_001
+    x = np.full((4, V), 0xFF80, dtype=np.uint16)                  # all -inf
+    g = synth.rng(3, 3)
+    for c in range(4):
+        p = g.choice(V, size=40, replace=False)
+        x[c, p[:20]] = 0x8000                                     # -0
+        x[c, p[20:]] = 0x0000                                     # +0
+    x[3, 12345] = 0x7F80                                          # one +inf
+    for k in (1, 20, 41, 64):
+        gu.assert_topk_equal(gu.run_topk(x, k), oracle.topk(x, k), f"zeros/inf k={k}")
+
+
+@pytest.mark.parametrize("k", [1, 20, 64])
+def test_shortlist_ties_by_vocab_id(k):
+    V = 131_072
+    x = synth.levels_block(8, 24, V, [0.0, 2.0, -1.0])
+    m = synth.shortlist_map(8, V)
+    gu.assert_topk_equal(gu.run_topk(x, k, id_map=m), oracle.topk_mapped(x, k, m), f"mapped ties k={k}")
+
+
+@pytest.mark.parametrize("gamma", [1, 7, 15])
+def test_verify_edges(gamma):
+    for V, lanes in ((1, 3), (2, 5), (17, 64), (4099, 33), (248_046, 2)):
+        tgt, drafts, acc_p, _ = synth.planted_verify(100 + V, lanes, gamma, V)
+        got = gu.run_verify(tgt, drafts, offset=(V + gamma) % 8)
+        gu.assert_verify_equal(got, oracle.verify(tgt, drafts), f"planted V={V} gamma={gamma}")
+        assert got[0].tolist() == acc_p.tolist()
+        # heavy ties and out-of-range drafts
+        x = synth.levels_block(200 + V, lanes * (gamma + 1), V, [0.0, 1.0, -0.0])
+        d = synth.random_drafts(300 + V, lanes, gamma, V + 3) - 1       # some -1 and >= V
+        d[::2] = 0
+        gu.assert_verify_equal(gu.run_verify(x, d), oracle.verify(x, d), f"ties V={V} gamma={gamma}")
+
+
+def test_round_matches_separate_calls_and_repeats():
+    """Tickets are reset by the kernel: back-to-back launches on fresh data."""
+    for rep in range(3):
+        r = synth.make_c2(seed=20 + rep, V=50_000 + 7 * rep)
+        v, i, a, c = gu.run_round(r.draft, r.k, r.target, r.drafts, offset=rep)
+        gu.assert_topk_equal((v, i), oracle.topk(r.draft, r.k), f"repeat {rep}")
+        gu.assert_verify_equal((a, c), oracle.verify(r.target, r.drafts), f"repeat {rep}")
+
+
+def test_empty_and_rejected_calls_write_nothing():
+    import torch
+    sd = gu.sd_module()
+    x = gu.dev_u16(np.zeros((3, 100), dtype=np.uint16))
+    vals = gu.Guarded(3 * 8, torch.int16)
+    ids = gu.Guarded(3 * 8, torch.int32)
+    sd.spec_topk(x, 0, 100, 8, vals.view, ids.view)
+    with pytest.raises(sd.SpecError):
+        sd.spec_topk(x, 3, 100, 101, vals.view, ids.view)
+    torch.cuda.synchronize()
+    for g in (vals, ids):
+        g.check_guards()
+        assert np.all(g.host() == g.sent)
+
+
+def test_side_stream_and_graph_capture():
+    import torch
+    sd = gu.sd_module()
+    r = synth.make_c1(seed=4, V=100_003)
+    r2 = synth.make_c1(seed=5, V=100_003)
+    x = gu.dev_u16(r.draft)
+    t = gu.dev_u16(r.target)
+    d = gu.dev_i32(r.drafts)
+    cols, V, k, lanes, gamma = r.cols, r.V, r.k, r.lanes, r.gamma
+    vals = torch.empty((cols, k), dtype=torch.int16, device="cuda")
+    ids = torch.empty((cols, k), dtype=torch.int32, device="cuda")
+    acc = torch.empty(lanes, dtype=torch.int32, device="cuda")
+    com = torch.empty((lanes, gamma + 1), dtype=torch.int32, device="cuda")
+    sd.spec_reserve(cols, k, lanes, gamma)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        sd.spec_round(x, cols, V, k, vals, ids, t, d, lanes, gamma, acc, com)
+    s.synchronize()
+    gu.assert_topk_equal((vals.cpu().numpy().view(np.uint16), ids.cpu().numpy()), oracle.topk(r.draft, k), "stream")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        sd.spec_round(x, cols, V, k, vals, ids, t, d, lanes, gamma, acc, com)
+    for rr in (r2, r, r2):
+        x.copy_(torch.from_numpy(rr.draft.view(np.int16)))
+        t.copy_(torch.from_numpy(rr.target.view(np.int16)))
+        d.copy_(torch.from_numpy(rr.drafts))
+        g.replay()
+        torch.cuda.synchronize()
+        gu.assert_topk_equal((vals.cpu().numpy().view(np.uint16), ids.cpu().numpy()), oracle.topk(rr.draft, k),
+                             "graph replay")
+        gu.assert_verify_equal((acc.cpu().numpy(), com.cpu().numpy()), oracle.verify(rr.target, rr.drafts),
+                               "graph replay verify")
+    sd.spec_set_stream(None)
+
+
+def test_round_host_buffers():
+    sd = gu.sd_module()
+    r = synth.make_c2(seed=9, V=30_000)
+    vals = np.zeros((r.cols, r.k), dtype=np.uint16)
+    ids = np.zeros((r.cols, r.k), dtype=np.int32)
+    acc = np.zeros(r.lanes, dtype=np.int32)
+    com = np.zeros((r.lanes, r.gamma + 1), dtype=np.int32)
+    sd.spec_round_host(r.draft, r.cols, r.V, r.k, vals, ids, r.target, r.drafts, r.lanes, r.gamma, acc, com)
+    gu.assert_topk_equal((vals, ids), oracle.topk(r.draft, r.k), "host buffers")
+    gu.assert_verify_equal((acc, com), oracle.verify(r.target, r.drafts), "host buffers")
