@@ -132,6 +132,32 @@ spec_status spec_round_host(const uint16_t *draft_logits, int64_t cols, int64_t 
                             const uint16_t *target_logits, const int32_t *drafts, int64_t lanes,
                             int32_t gamma, int32_t *out_accept_len, int32_t *out_commit_ids);
 
+/* spec_round without any allocation, for callers that cannot let a library
+ * call cudaMalloc: an inference engine that serves every byte of device memory
+ * from its own pool, a serving loop that cannot afford the device-wide
+ * synchronisation of cudaFree, or a host under a fixed memory budget.  The
+ * pages describe no such entry point; it is an addition of this library.
+ *
+ * Same arguments, results and errors as spec_round (all device pointers, the
+ * calling thread's stream), except:
+ *   - its scratch is one fixed device array inside the library (about 1.1
+ *     MB), which every GPU that loads the library keeps until the process
+ *     exits; nothing is ever allocated or freed (no cudaMalloc, no cudaFree);
+ *   - sizes are limited: cols + lanes*(gamma+1) <= SPEC_NOALLOC_MAX_COLS and
+ *     lanes <= SPEC_NOALLOC_MAX_LANES; larger calls return SPEC_ERR_ARG with
+ *     a message naming the limit;
+ *   - the first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture;
+ *   - every call shares the one array and starts by clearing its tickets on
+ *     the stream, so calls that overlap on the GPU (different streams, or
+ *     different host threads) race and must not be issued that way. */
+#define SPEC_NOALLOC_MAX_COLS 8192
+#define SPEC_NOALLOC_MAX_LANES 512
+spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t cols, int64_t V, int32_t k,
+                               uint16_t *out_vals, int32_t *out_ids,
+                               const uint16_t *target_logits, const int32_t *drafts, int64_t lanes,
+                               int32_t gamma, int32_t *out_accept_len, int32_t *out_commit_ids);
+
 /* Set the stream (a cudaStream_t, may be NULL for the legacy default stream)
  * that the calling thread's subsequent calls enqueue on.  Thread-local. */
 spec_status spec_set_stream(void *stream);

@@ -21,6 +21,7 @@ __all__ = [
     "SPEC_OK", "SPEC_ERR_ARG", "SPEC_ERR_ALLOC", "SPEC_ERR_CUDA", "SPEC_VOCAB", "SPEC_MAX_K",
     "SPEC_MAX_GAMMA", "SpecError", "LIB_PATH", "lib",
     "spec_topk", "spec_topk_mapped", "spec_verify", "spec_verify_v", "spec_round", "spec_round_host",
+    "spec_round_noalloc",
     "spec_set_stream", "spec_get_stream", "spec_reserve", "spec_release", "spec_last_error",
     "spec_launch_count", "topk", "topk_mapped", "verify", "round_step", "EXPORTS",
 ]
@@ -43,6 +44,7 @@ _SIGS = {
     "spec_verify_v": [_p, _p, _i64, _i32, _i64, _p, _p],
     "spec_round": [_p, _i64, _i64, _i32, _p, _p, _p, _p, _i64, _i32, _p, _p],
     "spec_round_host": [_p, _i64, _i64, _i32, _p, _p, _p, _p, _i64, _i32, _p, _p],
+    "spec_round_noalloc": [_p, _i64, _i64, _i32, _p, _p, _p, _p, _i64, _i32, _p, _p],
     "spec_set_stream": [_p],
     "spec_get_stream": [],
     "spec_reserve": [_i64, _i32, _i64, _i32],
@@ -115,6 +117,16 @@ def spec_round(draft_logits, cols, V, k, out_vals, out_ids, target_logits, draft
     _use_torch_stream()
     _check(lib.spec_round(_ptr(draft_logits), cols, V, k, _ptr(out_vals), _ptr(out_ids), _ptr(target_logits),
                           _ptr(drafts), lanes, gamma, _ptr(out_accept_len), _ptr(out_commit_ids)))
+
+
+def spec_round_noalloc(draft_logits, cols, V, k, out_vals, out_ids, target_logits, drafts, lanes, gamma,
+                       out_accept_len, out_commit_ids):
+    """spec_round with its scratch in a fixed device array: allocates nothing
+    (for callers whose device memory all comes from their own pool)."""
+    _use_torch_stream()
+    _check(lib.spec_round_noalloc(_ptr(draft_logits), cols, V, k, _ptr(out_vals), _ptr(out_ids),
+                                  _ptr(target_logits), _ptr(drafts), lanes, gamma, _ptr(out_accept_len),
+                                  _ptr(out_commit_ids)))
 
 
 def spec_round_host(draft_logits, cols, V, k, out_vals, out_ids, target_logits, drafts, lanes, gamma,

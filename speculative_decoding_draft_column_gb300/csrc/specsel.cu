@@ -958,3 +958,117 @@ const char *spec_last_error(void) { return t_err.c_str(); }
 int64_t spec_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// spec_round_noalloc: the same round, with its scratch in a fixed device array
+// ---------------------------------------------------------------------------
+//
+// Some callers cannot let this library call cudaMalloc: an inference engine
+// that hands out every byte of device memory from its own pool (a stray
+// allocation breaks its accounting and can fail once the pool has taken the
+// free memory), a serving loop that must never pay the device-wide
+// synchronisation that cudaFree implies, or a C host that runs under a fixed
+// memory budget.  For them this entry point keeps its scratch (column and lane
+// tickets, target argmaxes, partial lists) in one statically sized device
+// array, so it allocates nothing, ever.  The array costs every GPU that loads
+// the library its size until the process exits.
+
+namespace {
+
+constexpr int64_t kNoAllocMaxCols = SPEC_NOALLOC_MAX_COLS;     // draft + target columns
+constexpr int64_t kNoAllocMaxLanes = SPEC_NOALLOC_MAX_LANES;
+constexpr int64_t kNoAllocPartials = 131072;                    // partial-list entries (1 MiB)
+constexpr size_t kNoAllocColTicket = 0;
+constexpr size_t kNoAllocLaneTicket = kNoAllocColTicket + ((kNoAllocMaxCols * 4 + 255) & ~int64_t(255));
+constexpr size_t kNoAllocArgmax = kNoAllocLaneTicket + ((kNoAllocMaxLanes * 4 + 255) & ~int64_t(255));
+constexpr size_t kNoAllocPart = kNoAllocArgmax + ((kNoAllocMaxCols * 4 + 255) & ~int64_t(255));
+constexpr size_t kNoAllocBytes = kNoAllocPart + kNoAllocPartials * 8;
+constexpr size_t kNoAllocTicketBytes = kNoAllocArgmax;         // both ticket arrays, cleared per call
+
+// Device scratch of spec_round_noalloc.  In host code this name only stands
+// for the symbol; the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Once per device, with that device current: look up the array's address.
+spec_status noalloc_scratch(void **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(SPEC_ERR_CUDA, "device ordinal %d unsupported", dev);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t cols, int64_t V, int32_t k,
+                                          uint16_t *out_vals, int32_t *out_ids, const uint16_t *target_logits,
+                                          const int32_t *drafts, int64_t lanes, int32_t gamma,
+                                          int32_t *out_accept_len, int32_t *out_commit_ids)
+{
+    t_err.clear();
+    spec_status st = check_topk_args(draft_logits, cols, V, k, out_vals, out_ids);
+    if (st != SPEC_OK) return st;
+    st = check_verify_args(target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids);
+    if (st != SPEC_OK) return st;
+    if (cols == 0 && lanes == 0) return SPEC_OK;
+    const int64_t t_cols = lanes * (gamma + 1);
+    if (cols + t_cols > kNoAllocMaxCols)
+        return fail(SPEC_ERR_ARG, "spec_round_noalloc: %lld draft + target columns exceed its fixed scratch "
+                    "limit of %lld", (long long)(cols + t_cols), (long long)kNoAllocMaxCols);
+    if (lanes > kNoAllocMaxLanes)
+        return fail(SPEC_ERR_ARG, "spec_round_noalloc: %lld lanes exceed its fixed scratch limit of %lld",
+                    (long long)lanes, (long long)kNoAllocMaxLanes);
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState *d = nullptr;
+    st = device_state(&d);
+    if (st != SPEC_OK) return st;
+    void *base = nullptr;
+    st = noalloc_scratch(&base);
+    if (st != SPEC_OK) return st;
+
+    const int slots = (cols > 0 && k > 32) ? 2 : 1;
+    const int64_t max_ctas = (int64_t)d->sms * d->occ[slots - 1][0];
+    RoundArgs a;
+    memset(&a, 0, sizeof a);
+    a.draft = draft_logits; a.d_cols = cols; a.d_V = cols ? V : 1; a.k = cols ? k : 1;
+    a.out_vals = out_vals; a.out_ids = out_ids;
+    a.target = target_logits; a.t_cols = t_cols; a.t_V = lanes ? V : 1; a.gamma = gamma;
+    a.drafts = drafts; a.out_accept = out_accept_len; a.out_commit = out_commit_ids;
+    a.pstride = a.k;
+    // parts per column as in spec_round, capped so the partial lists fit
+    int parts = choose_parts(cols + t_cols, V, max_ctas);
+    const int64_t cap = kNoAllocPartials / ((cols + t_cols) * (int64_t)a.pstride);
+    if (parts > cap) parts = cap < 1 ? 1 : (int)cap;        // one part per column needs no partials
+    a.d_parts = a.t_parts = parts;
+    a.d_units = cols * parts;
+    a.n_units = a.d_units + t_cols * parts;
+    char *p = static_cast<char *>(base);
+    a.col_ticket = reinterpret_cast<unsigned int *>(p + kNoAllocColTicket);
+    a.lane_ticket = reinterpret_cast<unsigned int *>(p + kNoAllocLaneTicket);
+    a.t_argmax = reinterpret_cast<int32_t *>(p + kNoAllocArgmax);
+    a.partials = reinterpret_cast<unsigned long long *>(p + kNoAllocPart);
+
+    cudaStream_t stream = t_stream;
+    // the array keeps whatever the last call left: start every ticket at zero
+    cudaError_t e = cudaMemsetAsync(base, 0, kNoAllocTicketBytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch tickets)");
+    const int64_t grid64 = a.n_units < max_ctas ? a.n_units : max_ctas;
+    const dim3 grid((unsigned)grid64), block(kThreads);
+    if (slots == 1) spec_round_kernel<1, false><<<grid, block, 0, stream>>>(a);
+    else spec_round_kernel<2, false><<<grid, block, 0, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return SPEC_OK;
+}
