@@ -176,6 +176,13 @@ spec_status spec_release(void);
 /* Text of the last error raised on the calling thread ("" if none). */
 const char *spec_last_error(void);
 
+/* Waits for the calling thread's stream, then reports whether any kernel
+ * of the library gave up a bounded wait on its copy pipeline since the last
+ * call (SPEC_ERR_CUDA, and the flag is cleared) or not (SPEC_OK).  Every
+ * wait in the kernels is bounded, so a broken pipeline ends the kernel with
+ * invalid results and this flag set, instead of hanging the GPU. */
+spec_status spec_device_status(void);
+
 /* Number of kernel launches this process made through the library (all
  * devices, all threads).  One per spec_topk / spec_verify / spec_round. */
 int64_t spec_launch_count(void);

@@ -23,7 +23,7 @@ __all__ = [
     "spec_topk", "spec_topk_mapped", "spec_verify", "spec_verify_v", "spec_round", "spec_round_host",
     "spec_round_noalloc",
     "spec_set_stream", "spec_get_stream", "spec_reserve", "spec_release", "spec_last_error",
-    "spec_launch_count", "topk", "topk_mapped", "verify", "round_step", "EXPORTS",
+    "spec_launch_count", "spec_device_status", "topk", "topk_mapped", "verify", "round_step", "EXPORTS",
 ]
 
 SPEC_OK, SPEC_ERR_ARG, SPEC_ERR_ALLOC, SPEC_ERR_CUDA = 0, -1, -2, -3
@@ -51,6 +51,7 @@ _SIGS = {
     "spec_release": [],
     "spec_last_error": [],
     "spec_launch_count": [],
+    "spec_device_status": [],
 }
 EXPORTS = tuple(_SIGS)
 for _name, _args in _SIGS.items():
@@ -162,6 +163,11 @@ def spec_last_error() -> str:
 
 def spec_launch_count() -> int:
     return int(lib.spec_launch_count())
+
+
+def spec_device_status():
+    """Raise SpecError if a kernel gave up a bounded wait since the last check."""
+    _check(lib.spec_device_status())
 
 
 # ---- allocating conveniences (outputs created with torch, work in the kernels)

@@ -11,36 +11,38 @@
 //
 // Design (one streaming pass over the logits, no tensor cores -- the step is
 // a pure reduction bound by HBM bandwidth):
-//   * Work units.  Every column is cut into P equal parts; a unit is one part
-//     of one column.  A persistent grid of (SMs x resident CTAs) walks the
-//     units round-robin.  P is chosen on the host so that the units spread
-//     evenly over the CTAs (the pages' prior kernel gave one warp to each of
-//     7 columns and sat 1,500x off its bandwidth floor).
-//   * Inside a unit, the 8 warps take interleaved blocks of 256 16-byte
-//     vectors (2,048 bf16); every lane issues its 8 vector loads before
-//     looking at any of them.  A warp therefore walks its share of the unit
-//     in increasing id order, which is what lets a tie with the running k-th
-//     value be rejected without comparing ids.
-//   * Per warp, the current top-k lives in registers, one (value, id) entry
-//     per lane (two for k > 32).  A block is skipped after one bf16x2 max
-//     tree and one compare against the running k-th value; only blocks with
-//     a candidate take the slow path, which inserts candidates in id order
-//     with a ballot/shuffle insertion.  The first block of a unit seeds the
-//     threshold exactly from group maxima (the k-th largest of them, found
-//     by a 16-step bisection on order-preserving keys), so the list fills
-//     with ~k candidates instead of every element of the block.
-//   * The 8 warp lists are merged in shared memory by rank (each entry
-//     counts, by binary search, the better entries of the other lists).
-//     If the column has several units, the CTA writes its list to scratch,
-//     takes a ticket, and the last CTA to finish the column merges the
-//     partial lists the same way -- no second pass over the logits, and no
-//     spin-wait anywhere (nothing can hang).
-//   * Verify columns are the k = 1 instance of the same path; the CTA that
-//     finishes the last of a lane's gamma+1 columns runs the prefix match.
-//   * Masked elements (outside the unit, or the ragged 16-byte edges of a
-//     column) are bf16 NaN: bf16 max ignores them, ordered compares reject
-//     them.  Edge vectors are read element by element, so no load ever
-//     touches memory outside the caller's buffer.
+//   * Every warp of a full-GPU grid (16 warps per CTA, one CTA per SM) owns a
+//     contiguous slice of the flat run of logits (draft columns one after the
+//     other, then target columns), the same number of 16-byte vectors for
+//     every warp.  A slice may start or end inside a column.  The warps never
+//     wait on one another in the streaming loop.
+//   * Each warp streams its slice through its own ring of three 4 KiB stages
+//     in shared memory, filled by one-dimensional bulk copies
+//     (cp.async.bulk, completion on an mbarrier); lane 0 refills a stage as
+//     soon as the warp is done with it, so 12 KiB per warp (192 KiB per SM)
+//     stay in flight.
+//   * Per column segment the warp keeps a candidate buffer in shared memory:
+//     packed (value key, id, bits) entries appended in increasing id order.
+//     A stage is skipped after one bf16x2 max tree per lane and one compare
+//     against the column's threshold.  The threshold is a certificate: a key
+//     that kk elements already reach.  It is seeded from the first stage
+//     (the kk-th largest of the lane maxima) and tightened by pruning the
+//     buffer to its kk best (a bisection over the 16 key bits); since the warp
+//     meets elements in id order, a later element equal to the threshold is
+//     worse than every kept entry and is rejected (strict filter).
+//   * A column seen whole by one warp is emitted by it.  Otherwise every warp
+//     that saw part of it publishes its kk best (and their certificate) to
+//     scratch and takes the column's ticket; the warp that completes the
+//     column merges the lists in slice order -- the logits are read once.
+//   * Verify columns are the k = 1 instance; the warp that completes the last
+//     of a lane's gamma+1 columns runs the prefix match (one lane per
+//     position).  Tickets are reset by their last user, so launches replay.
+//   * Masked elements (past a column or the buffer) are bf16 NaN: bf16 max
+//     ignores them, ordered compares reject them.  The buffer's ragged first
+//     and last 16-byte vectors are read element by element, so no load or
+//     copy touches memory outside the caller's buffer.
+//   * Every mbarrier wait is bounded in time; a wait that gives up sets a flag
+//     (spec_device_status) and the kernel still ends.
 
 #include <cuda_runtime.h>
 #include <stdarg.h>
@@ -56,55 +58,50 @@
 
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kU = 8;                       // 16-byte vectors per lane per block
-constexpr int kBlockVec = 32 * kU;          // vectors per warp block (4 KiB)
-constexpr int kListStride = 64;             // entries per list slot in shared memory
-constexpr int kMaxParts = 32;               // parts per column (shared merge buffer)
-constexpr int kMergeCap = 2048;             // entries in the shared merge buffer
+constexpr int kWarpsPerCta = 16;
+constexpr int kThreads = kWarpsPerCta * 32;
+constexpr int kStageVec = 256;                     // 16-byte vectors per warp stage (4 KiB)
+constexpr int kLaneVec = kStageVec / 32;           // vectors per lane per stage
+constexpr int kStages = 3;                         // per-warp ring depth (12 KiB in flight per warp)
+constexpr int kBufCap = 128;                       // per-warp candidate buffer (entries)
+constexpr int kMinSliceVec = 2 * kStageVec;        // smallest slice a warp is given
+constexpr uint64_t kWaitLimitNs = 4000000000ull;   // bound on any mbarrier wait: 4 s of wall time
 constexpr unsigned kFull = 0xffffffffu;
-constexpr uint32_t kNaN2 = 0x7FFF7FFFu;     // two bf16 NaNs: the mask value
+constexpr uint32_t kNaN2 = 0x7FFF7FFFu;            // two bf16 NaNs: the mask value
 
-static_assert(kWarps * kListStride <= kMergeCap, "warp lists must fit the merge buffer");
-static_assert(kMaxParts * SPEC_MAX_K <= kMergeCap, "partials must fit the merge buffer");
+static_assert(kBufCap >= 2 * SPEC_MAX_K && kBufCap % 32 == 0, "a pruned buffer must leave room");
 
 struct RoundArgs {
     // top-k part (draft columns)
     const uint16_t *draft;
     int64_t d_cols, d_V;
-    int32_t k, d_parts;
+    int32_t k;
     const int32_t *id_map;
     uint16_t *out_vals;
     int32_t *out_ids;
     // verify part (target columns)
     const uint16_t *target;
     int64_t t_cols, t_V;
-    int32_t t_parts, gamma;
+    int32_t gamma;
     const int32_t *drafts;
     int32_t *out_accept;
     int32_t *out_commit;
+    // warps [0, d_warps) stream the draft logits, [d_warps, d_warps + t_warps) the target logits
+    int32_t d_warps, t_warps;
     // scratch
-    unsigned long long *partials;   // [n_units][pstride]
+    unsigned long long *partials;   // [(d_warps + t_warps) * 2][pstride = k + 1]
     unsigned int *col_ticket;       // [d_cols + t_cols]
     unsigned int *lane_ticket;      // [lanes]
     int32_t *t_argmax;              // [t_cols]
     int32_t pstride;
-    int64_t d_units, n_units;
 };
+
+// Set (bit 0) when a bounded wait gave up; read and cleared by spec_device_status.
+__device__ unsigned int g_wait_timeouts;
 
 // ---------------------------------------------------------------------------
 // device helpers
 // ---------------------------------------------------------------------------
-
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p)
-{
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
-    return r;
-}
 
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b)
 {
@@ -172,6 +169,7 @@ __device__ __forceinline__ unsigned long long pack_entry(float v, uint32_t id)
     return ((unsigned long long)order_key(raw) << 48) | ((unsigned long long)(~id) << 16) | raw;
 }
 
+__device__ __forceinline__ uint32_t entry_key(unsigned long long e) { return (uint32_t)(e >> 48); }
 __device__ __forceinline__ uint32_t entry_id(unsigned long long e) { return ~(uint32_t)(e >> 16); }
 __device__ __forceinline__ uint16_t entry_raw(unsigned long long e) { return (uint16_t)(e & 0xFFFFu); }
 
@@ -196,333 +194,574 @@ __device__ __forceinline__ uint4 load_edge(const uint16_t *buf, int64_t j, int m
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Insert candidate (cv, cid) into the warp-distributed sorted list.  Entry
-// index s*32+lane lives in Lv[s]/Li[s].  Without an id map, candidates reach
-// the list in increasing id order, so an equal value already in the list is
-// better; with an id map, ties compare the mapped ids.
-template <int SLOTS, bool MAPPED>
-__device__ __forceinline__ void list_insert(float (&Lv)[SLOTS], uint32_t (&Li)[SLOTS], float cv,
-                                            uint32_t cid, int kk, int lane)
+__device__ __forceinline__ uint32_t lanemask_lt()
 {
-    int pos = 0;
-#pragma unroll
-    for (int s = 0; s < SLOTS; ++s) {
-        bool better = MAPPED ? (Lv[s] > cv || (Lv[s] == cv && Li[s] < cid)) : (Lv[s] >= cv);
-        better = better && (s * 32 + lane < kk);
-        pos += __popc(__ballot_sync(kFull, better));
-    }
-    if (pos >= kk) return;
-    const float up0 = __shfl_up_sync(kFull, Lv[0], 1);
-    const uint32_t ui0 = __shfl_up_sync(kFull, Li[0], 1);
-    if constexpr (SLOTS == 2) {
-        const float last0 = __shfl_sync(kFull, Lv[0], 31);
-        const uint32_t lasti0 = __shfl_sync(kFull, Li[0], 31);
-        float up1 = __shfl_up_sync(kFull, Lv[1], 1);
-        uint32_t ui1 = __shfl_up_sync(kFull, Li[1], 1);
-        if (lane == 0) { up1 = last0; ui1 = lasti0; }
-        const int i1 = 32 + lane;
-        if (i1 > pos) { Lv[1] = up1; Li[1] = ui1; }
-        else if (i1 == pos) { Lv[1] = cv; Li[1] = cid; }
-    }
-    if (lane > pos) { Lv[0] = up0; Li[0] = ui0; }
-    else if (lane == pos) { Lv[0] = cv; Li[0] = cid; }
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
 }
 
-template <int SLOTS>
-__device__ __forceinline__ float list_kth(const float (&Lv)[SLOTS], int kk)
+// ---- mbarrier / bulk-copy primitives (inline PTX, sm_90+) -------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {
-    const int i = kk - 1;
-    float t = __shfl_sync(kFull, Lv[0], i & 31);
-    if constexpr (SLOTS == 2) {
-        const float t1 = __shfl_sync(kFull, Lv[1], i & 31);
-        if (i >= 32) t = t1;
-    }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
 
-// Loads one warp block (kU vectors per lane) of the unit: interior vectors
-// with 16-byte loads, the unit's two edge vectors element by element, and
-// vectors past the unit as masked NaNs.
-__device__ __forceinline__ void load_block(uint4 (&x)[kU], const uint16_t *__restrict__ buf, const uint4 *vb,
-                                           int64_t jb, int64_t jf, int64_t jl, int mis, int64_t g0, int64_t g1,
-                                           int lane)
+// Wait for the phase with the given parity to complete, for at most
+// kWaitLimitNs of wall time; on giving up, flag the error and report false
+// (the data is then garbage, but the kernel still terminates).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
-    if (jb > jf && jb + kBlockVec - 1 < jl) {
-#pragma unroll
-        for (int u = 0; u < kU; ++u) x[u] = ld_stream(vb + jb + u * 32 + lane);
-    } else {
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int64_t j = jb + u * 32 + lane;
-            if (j > jf && j < jl) x[u] = ld_stream(vb + j);
-            else if (j == jf || j == jl) x[u] = load_edge(buf, j, mis, g0, g1);
-            else x[u] = make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(&g_wait_timeouts, 1u);
+            return false;
         }
     }
 }
 
-// Threshold of a list: kk entries >= it exist (a certificate).  Candidates
-// must be >= `thr` (inclusive) or, when `strict`, > `thr`.
-struct Threshold {
+// One bulk copy global -> shared, completing on `bar` with its byte count.
+// src, dst 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+// ---- candidate buffers ------------------------------------------------------
+
+// Prune the warp buffer wb[0..n) (n >= kk, entries in increasing id order) to
+// its kk best entries, keeping their order; returns kk and, in tkey, the
+// kk-th largest key (kk entries reach it: a certificate).  Without an id map
+// ties at that key go to the earliest entries (smallest ids); with one, to
+// the smallest mapped ids.
+struct Pruned {
+    int n;       // entries kept (kk)
+    uint32_t t;  // their certificate: the kk-th largest key
+};
+
+template <bool MAPPED>
+__device__ __noinline__ Pruned buf_prune(unsigned long long *wb, int n, int kk, int lane)
+{
+    constexpr int Q = kBufCap / 32;
+    unsigned long long e[Q];
+    uint32_t key[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        const int idx = q * 32 + lane;
+        e[q] = idx < n ? wb[idx] : 0ull;
+        key[q] = entry_key(e[q]);
+    }
+    uint32_t t = 0;   // kk-th largest key: bisection over the 16 key bits
+#pragma unroll 1
+    for (int bit = 15; bit >= 0; --bit) {
+        const uint32_t tr = t | (1u << bit);
+        int cnt = 0;
+#pragma unroll
+        for (int q = 0; q < Q; ++q) cnt += __popc(__ballot_sync(kFull, key[q] >= tr));
+        if (cnt >= kk) t = tr;
+    }
+    int cgt = 0;
+#pragma unroll
+    for (int q = 0; q < Q; ++q) cgt += __popc(__ballot_sync(kFull, key[q] > t));
+    const int quota = kk - cgt;   // entries with key == t that survive
+    bool keep[Q];
+    if constexpr (!MAPPED) {
+        int seen = 0;
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            const bool eq = key[q] == t && e[q] != 0ull;
+            const uint32_t bal = __ballot_sync(kFull, eq);
+            keep[q] = key[q] > t || (eq && seen + __popc(bal & lanemask_lt()) < quota);
+            seen += __popc(bal);
+        }
+    } else {
+        uint32_t mid[Q];
+#pragma unroll
+        for (int q = 0; q < Q; ++q) mid[q] = (key[q] == t && e[q] != 0ull) ? entry_id(e[q]) : 0xFFFFFFFFu;
+        uint32_t m = 0;   // the quota-th smallest mapped id among the ties (ids < 2^31)
+#pragma unroll 1
+        for (int bit = 30; bit >= 0; --bit) {
+            const uint32_t tr = m | (1u << bit);
+            int cnt = 0;
+#pragma unroll
+            for (int q = 0; q < Q; ++q) cnt += __popc(__ballot_sync(kFull, mid[q] < tr));
+            if (cnt < quota) m = tr;
+        }
+#pragma unroll
+        for (int q = 0; q < Q; ++q) keep[q] = key[q] > t || (mid[q] != 0xFFFFFFFFu && mid[q] <= m);
+    }
+    __syncwarp();
+    int out = 0;
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        const uint32_t bal = __ballot_sync(kFull, keep[q]);
+        if (keep[q]) wb[out + __popc(bal & lanemask_lt())] = e[q];
+        out += __popc(bal);
+    }
+    __syncwarp();
+    return Pruned{out, t};
+}
+
+// Filter: candidates must be > thr (strict) or >= thr.
+struct Filter {
     float thr;
     uint32_t thr2;   // thr as a bf16 pair
     bool strict;
 };
 
-__device__ __forceinline__ Threshold make_threshold(uint32_t cta_key, float own, bool own_full, bool mapped)
+// own_key: the warp's certified key for the column (0: none), strict unless
+// mapped; cert_key: another certificate for the column (inclusive).
+__device__ __forceinline__ Filter make_filter(uint32_t own_key, uint32_t cert_key, bool mapped)
 {
-    // cta_key: order key certified for the whole CTA (0 = none yet)
-    Threshold t;
-    const uint32_t own_key = own_full ? order_key(__float_as_uint(own) >> 16) : 0u;
-    if (own_full && own_key >= cta_key) {
-        t.thr = own;
-        t.strict = !mapped;
+    Filter f;
+    uint32_t key;
+    if (own_key != 0 && own_key >= cert_key) {
+        key = own_key;
+        f.strict = !mapped;
     } else {
-        t.thr = cta_key ? bf16_as_float(key_to_raw(cta_key)) : -INFINITY;
-        t.strict = false;
+        key = cert_key;
+        f.strict = false;
     }
-    const uint32_t raw = __float_as_uint(t.thr) >> 16;
-    t.thr2 = raw | (raw << 16);
-    return t;
+    const uint32_t raw = key ? key_to_raw(key) : 0xFF80u;   // no certificate: >= -Inf
+    f.thr = bf16_as_float(raw);
+    f.thr2 = raw | (raw << 16);
+    return f;
 }
 
-// One warp's pass over its blocks of one unit; leaves its list (packed,
-// sorted, empty slots = 0) in lists[warp * kListStride + i], i < kk.
-//
-// The CTA shares one threshold key in *cta_thr: whenever a warp's list is
-// full, its kk-th value certifies kk elements of the unit at or above it, so
-// no element below it can be in the unit's top-k.  Every warp filters
-// against the larger of that key and its own list's kk-th value (strictly,
-// for its own value: the warp sees its elements in id order, so an equal
-// value arriving later has the larger id).  All threads of the CTA must
-// call this (it contains one CTA barrier); *cta_thr must be 0 on entry.
-template <int SLOTS, bool MAPPED>
-__device__ __forceinline__ void scan_unit(const uint16_t *__restrict__ buf, int64_t V, int64_t col,
-                                          int64_t e0, int64_t e1, int kk,
-                                          const int32_t *__restrict__ id_map,
-                                          unsigned long long *lists, unsigned int *cta_thr)
+__device__ __forceinline__ uint32_t elem_mask(const uint4 &q, const Filter &f)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(buf);
-    const int mis = (int)((a0 >> 1) & 7);                      // element phase of buf in 16 B
-    const uint4 *vb = reinterpret_cast<const uint4 *>(a0 - 2 * (uintptr_t)mis);
-    const int64_t colbase = col * V;
-    const int64_t g0 = colbase + e0, g1 = colbase + e1;       // element range in buf
-    const int64_t jf = (g0 + mis) >> 3, jl = (g1 - 1 + mis) >> 3;
-    const int64_t nblk = (jl - jf + kBlockVec) / kBlockVec;
-
-    float Lv[SLOTS];
-    uint32_t Li[SLOTS];
+    uint32_t cm = 0;
 #pragma unroll
-    for (int s = 0; s < SLOTS; ++s) { Lv[s] = __uint_as_float(0x7FC00000u); Li[s] = 0xFFFFFFFFu; }
-    bool full = false;
-    volatile unsigned int *vthr = cta_thr;
-
-    // Seed: from its first block each warp certifies the kk-th largest of
-    // its group maxima (kk distinct elements are at or above it); the CTA
-    // keeps the largest certificate.
-    uint4 x[kU];
-    int64_t b = warp;
-    if (b < nblk) {
-        load_block(x, buf, vb, jf + b * kBlockVec, jf, jl, mis, g0, g1, lane);
-        constexpr int G = (SLOTS == 1) ? 1 : 4;
-        constexpr int PER = kU / G;
-        uint32_t key[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            uint32_t m = vmax(x[g * PER]);
-#pragma unroll
-            for (int u = 1; u < PER; ++u) m = bmax2(m, vmax(x[g * PER + u]));
-            key[g] = order_key(hmax_splat(m) & 0xFFFFu);
-        }
-        uint32_t t = 0;
-        if (kk == 1) {
-            t = __reduce_max_sync(kFull, key[0]);
-        } else {
-#pragma unroll 1
-            for (int bit = 15; bit >= 0; --bit) {
-                const uint32_t tr = t | (1u << bit);
-                int cnt = 0;
-#pragma unroll
-                for (int g = 0; g < G; ++g) cnt += __popc(__ballot_sync(kFull, key[g] >= tr));
-                if (cnt >= kk) t = tr;
-            }
-        }
-        if (lane == 0 && t != 0) atomicMax(cta_thr, t);
+    for (int e = 0; e < 8; ++e) {
+        const float v = elem8(q, e);
+        cm |= (uint32_t)(f.strict ? (v > f.thr) : (v >= f.thr)) << e;
     }
-    __syncthreads();
-
-    for (; b < nblk; b += kWarps) {
-        const int64_t jb = jf + b * kBlockVec;
-        if (b != warp) load_block(x, buf, vb, jb, jf, jl, mis, g0, g1, lane);
-        const Threshold T = make_threshold(*vthr, list_kth<SLOTS>(Lv, kk), full, MAPPED);
-
-        uint32_t m = vmax(x[0]);
-#pragma unroll
-        for (int u = 1; u < kU; ++u) m = bmax2(m, vmax(x[u]));
-        const bool pass = T.strict ? any_gt(m, T.thr2) : any_ge(m, T.thr2);
-        if (!__ballot_sync(kFull, pass)) continue;
-
-        // Slow path: insert this block's candidates in increasing id order
-        // (vector u, then lane, then element).
-        const int64_t id_lane = 8 * (jb + lane) - mis - colbase;   // id of element 0, vector 0
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const bool pu = pass && (T.strict ? any_gt(vmax(x[u]), T.thr2) : any_ge(vmax(x[u]), T.thr2));
-            if (!__ballot_sync(kFull, pu)) continue;
-            uint32_t cm = 0;
-            if (pu) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float v = elem8(x[u], e);
-                    cm |= (uint32_t)(T.strict ? (v > T.thr) : (v >= T.thr)) << e;
-                }
-            }
-            uint32_t act = __ballot_sync(kFull, cm != 0);
-            while (act) {
-                const int src = __ffs(act) - 1;
-                float cv = 0.f;
-                uint32_t cid = 0;
-                if (lane == src) {
-                    const int e = __ffs(cm) - 1;
-                    cm &= cm - 1;
-                    cv = elem8(x[u], e);
-                    cid = (uint32_t)(id_lane + 256 * u + e);
-                    if (MAPPED) cid = (uint32_t)__ldg(id_map + cid);
-                }
-                cv = __shfl_sync(kFull, cv, src);
-                cid = __shfl_sync(kFull, cid, src);
-                list_insert<SLOTS, MAPPED>(Lv, Li, cv, cid, kk, lane);
-                act = __ballot_sync(kFull, cm != 0);
-            }
-        }
-        const float tv = list_kth<SLOTS>(Lv, kk);
-        full = (tv == tv);
-        if (full && lane == 0) {
-            const uint32_t kkey = order_key(__float_as_uint(tv) >> 16);
-            if (kkey > *vthr) atomicMax(cta_thr, kkey);
-        }
-    }
-
-#pragma unroll
-    for (int s = 0; s < SLOTS; ++s) {
-        const int i = s * 32 + lane;
-        if (i < kk) lists[warp * kListStride + i] = pack_entry(Lv[s], Li[s]);
-    }
+    return cm;
 }
 
-// out[0..kk) = the kk best of nl sorted lists (stride apart, kk long, empty
-// slots 0 at the tail).  Caller zeroes out and synchronises around the call.
-__device__ __forceinline__ void rank_merge(const unsigned long long *lists, int nl, int stride, int kk,
-                                           unsigned long long *out)
-{
-    for (int idx = threadIdx.x; idx < nl * kk; idx += blockDim.x) {
-        const int li = idx / kk, r = idx - li * kk;
-        const unsigned long long e = lists[li * stride + r];
-        if (e == 0ull) continue;
-        int rank = r;
-        for (int o = 0; o < nl && rank < kk; ++o) {
-            if (o == li) continue;
-            const unsigned long long *L = lists + o * stride;
-            int lo = 0, hi = kk;
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (L[mid] > e) lo = mid + 1;
-                else hi = mid;
-            }
-            rank += lo;
-        }
-        if (rank < kk) out[rank] = e;
-    }
-}
-
-struct Shared {
-    unsigned long long buf[kMergeCap];
-    unsigned long long out[SPEC_MAX_K];
-    unsigned int thr;   // CTA-wide certified threshold key of the current unit
-    int flag;
+struct ColState {
+    int n;          // entries in the buffer
+    uint32_t own;   // own certified key (last prune)
+    uint32_t cert;  // certificate from elsewhere (seed or merge), inclusive
+    bool open;      // the warp has started this column
+    int seen;       // elements of the column this warp has scanned (saturating)
 };
 
-// A column's final list is in s.out[0..kk): write the top-k outputs, or, for
-// a target column, record its argmax and run the lane's prefix match if this
-// was the lane's last column.
-__device__ __forceinline__ void finish_column(const RoundArgs &a, bool draft, int64_t col, int kk,
-                                              const Shared &s)
+// Append one packed entry per lane (lanes with `valid`) in lane order, after
+// filtering against the column's current threshold; prunes when full.
+template <bool MAPPED>
+__device__ __noinline__ void append_entries(unsigned long long *wb, ColState &cs, int kk, int lane,
+                                            unsigned long long e, bool valid)
 {
-    if (draft) {
-        for (int i = threadIdx.x; i < kk; i += blockDim.x) {
-            const unsigned long long e = s.out[i];
-            a.out_vals[col * kk + i] = entry_raw(e);
-            a.out_ids[col * kk + i] = (int32_t)entry_id(e);
+    for (;;) {
+        const Filter f = make_filter(cs.own, cs.cert, MAPPED);
+        const float v = bf16_as_float(entry_raw(e));
+        const bool ok = valid && e != 0ull && (f.strict ? v > f.thr : v >= f.thr);
+        const uint32_t bal = __ballot_sync(kFull, ok);
+        const int total = __popc(bal);
+        if (total == 0) return;
+        const int space = kBufCap - cs.n;
+        const int r = __popc(bal & lanemask_lt());
+        if (ok && r < space) wb[cs.n + r] = e;
+        __syncwarp();
+        if (total <= space) {
+            cs.n += total;
+            return;
         }
+        valid = ok && r >= space;                    // the rest, after a prune
+        { const Pruned pq = buf_prune<MAPPED>(wb, kBufCap, kk, lane); cs.n = pq.n; cs.own = pq.t; }
+    }
+}
+
+// ---- the per-warp stream ------------------------------------------------------
+
+// Shared memory of one warp: its copy ring, candidate buffer and barriers.
+struct WarpSmem {
+    uint4 ring[kStages][kStageVec];
+    unsigned long long buf[kBufCap];
+    uint64_t full[kStages];
+};
+
+constexpr size_t kSmemBytes = (size_t)kWarpsPerCta * sizeof(WarpSmem);
+
+// One buffer (draft or target logits) seen as a flat run of N = cols * V
+// elements on the 16-byte vector grid: vector j holds elements
+// [8j - mis, 8j - mis + 8).  The run is cut into W slices of whole vectors;
+// slice w = vectors [start(w), start(w+1)), start(w) = floor(w * NV / W).
+struct Run {
+    const uint16_t *buf;
+    const uint4 *vb;          // 16-byte aligned base, at or just below buf
+    int64_t V, N, NV;
+    int64_t jlo, jhi;         // vectors [jlo, jhi) lie wholly inside the buffer
+    int W, gw0;               // warps on this run; global index of its slice 0
+    int kk;
+    int mis;
+    bool draft;
+};
+
+__device__ __forceinline__ int64_t slice_start(const Run &r, int64_t w) { return w * r.NV / r.W; }
+__device__ __forceinline__ int64_t owner(const Run &r, int64_t j) { return ((j + 1) * r.W - 1) / r.NV; }
+__device__ __forceinline__ int64_t first_elem(const Run &r, int64_t w)
+{
+    const int64_t g = 8 * slice_start(r, w) - r.mis;
+    return g > 0 ? g : 0;
+}
+
+// The list slot of warp w for column c: 0 if c is the first column of the
+// slice, else 1 (a slice holds part of at most two columns).
+__device__ __forceinline__ unsigned long long *list_slot(const RoundArgs &a, const Run &r, int64_t w, int64_t c)
+{
+    const int sl = (c == first_elem(r, w) / r.V) ? 0 : 1;
+    return a.partials + ((int64_t)(r.gw0 + w) * 2 + sl) * a.pstride;
+}
+
+// Write a finished column: its best entries (in the buffer, id order) are
+// ranked by value; top-k outputs, or for a target column the argmax and, for
+// the lane's last column, the prefix match (one lane per position).
+__device__ __noinline__ void emit_column(const RoundArgs &a, const Run &r, int64_t c,
+                                         const unsigned long long *wb, int n, int lane)
+{
+    const int kk = r.kk;
+    for (int i = lane; i < n; i += 32) {
+        const unsigned long long e = wb[i];
+        int rank = 0;
+        for (int j = 0; j < n; ++j) rank += wb[j] > e;
+        if (r.draft) {
+            a.out_vals[c * kk + rank] = entry_raw(e);
+            a.out_ids[c * kk + rank] = (int32_t)entry_id(e);
+        } else if (rank == 0) {
+            a.t_argmax[c] = (int32_t)entry_id(e);
+        }
+    }
+    if (r.draft) return;
+    const int gp1 = a.gamma + 1;
+    const int64_t ln = c / gp1;
+    __threadfence();
+    __syncwarp();
+    unsigned last = 0;
+    if (lane == 0) last = atomicAdd(a.lane_ticket + ln, 1u) == (unsigned)a.gamma;
+    if (!__shfl_sync(kFull, last, 0)) return;
+    __threadfence();
+    const int32_t tj = lane < gp1 ? __ldcg(a.t_argmax + ln * gp1 + lane) : 0;
+    const int32_t dj = lane < a.gamma ? __ldg(a.drafts + ln * a.gamma + lane) : 0;
+    const uint32_t miss = __ballot_sync(kFull, lane < a.gamma && dj != tj);
+    const int acc = miss ? __ffs(miss) - 1 : a.gamma;
+    if (lane < gp1) a.out_commit[ln * gp1 + lane] = lane <= acc ? tj : -1;
+    if (lane == 0) {
+        a.out_accept[ln] = acc;
+        a.lane_ticket[ln] = 0u;   // ready for the next launch
+    }
+}
+
+// Column c's segment in this warp is over.  If the warp saw the whole column,
+// emit it; otherwise publish the warp's list and take the column's ticket;
+// the warp that completes the column merges every warp's list (in slice
+// order, hence in id order) and emits it.
+template <bool MAPPED>
+__device__ __noinline__ void finish_column(const RoundArgs &a, const Run &r, int w, int64_t c,
+                                           unsigned long long *wb, int n_in, uint32_t own_in, int lane)
+{
+    ColState cs = {n_in, own_in, 0u, true, 0};
+    const int kk = r.kk;
+    if (cs.n > kk) { const Pruned pq = buf_prune<MAPPED>(wb, cs.n, kk, lane); cs.n = pq.n; cs.own = pq.t; }
+    const int64_t wf = owner(r, (c * r.V + r.mis) >> 3);
+    const int64_t wl = owner(r, ((c + 1) * r.V - 1 + r.mis) >> 3);
+    if (wf == wl) {
+        emit_column(a, r, c, wb, cs.n, lane);
         return;
     }
-    if (threadIdx.x != 0) return;
-    const int gp1 = a.gamma + 1;
-    const int64_t lane = col / gp1;
-    a.t_argmax[col] = (int32_t)entry_id(s.out[0]);
+    // publish: the list (kk entries, id order, 0-padded) and, in slot kk, its
+    // certificate -- the smallest key of a full list (kk entries reach it)
+    uint32_t mk = 0xFFFFFFFFu;
+    for (int i = lane; i < cs.n; i += 32) {
+        const uint32_t ky = entry_key(wb[i]);
+        mk = ky < mk ? ky : mk;
+    }
+    mk = __reduce_min_sync(kFull, mk);
+    unsigned long long *mine = list_slot(a, r, w, c);
+    for (int i = lane; i <= kk; i += 32)
+        mine[i] = i < cs.n ? wb[i] : (i == kk ? (unsigned long long)(cs.n == kk ? mk : 0u) : 0ull);
     __threadfence();
-    const unsigned old = atomicAdd(a.lane_ticket + lane, 1u);
-    if (old != (unsigned)a.gamma) return;
+    __syncwarp();
+    const int64_t tix = r.draft ? c : a.d_cols + c;
+    unsigned last = 0;
+    if (lane == 0) last = atomicAdd(a.col_ticket + tix, 1u) == (unsigned)(wl - wf);
+    if (!__shfl_sync(kFull, last, 0)) return;
     __threadfence();
-    const int32_t *ta = a.t_argmax + lane * gp1;
-    const int32_t *dr = a.drafts + lane * a.gamma;
-    int acc = 0;
-    while (acc < a.gamma && __ldg(dr + acc) == __ldcg(ta + acc)) ++acc;
-    a.out_accept[lane] = acc;
-    for (int j = 0; j < gp1; ++j) a.out_commit[lane * gp1 + j] = (j <= acc) ? __ldcg(ta + j) : -1;
-    a.lane_ticket[lane] = 0u;   // ready for the next launch
+    // merge: the best certificate first, then every list in slice order
+    // (hence id order) through the buffer, 32 entries per round, several
+    // rounds of loads in flight
+    cs.n = 0;
+    cs.own = 0;
+    cs.cert = 0;
+    const int64_t nparts = wl - wf + 1;
+    for (int64_t q0 = 0; q0 < nparts; q0 += 32) {
+        uint32_t key = 0;
+        if (q0 + lane < nparts) key = (uint32_t)__ldcg(list_slot(a, r, wf + q0 + lane, c) + kk);
+        key = __reduce_max_sync(kFull, key);
+        cs.cert = key > cs.cert ? key : cs.cert;
+    }
+    const int64_t total = nparts * kk;
+    auto fetch = [&](int64_t p) { return p < total ? __ldcg(list_slot(a, r, wf + p / kk, c) + p % kk) : 0ull; };
+    constexpr int kAhead = 4;
+    unsigned long long q[kAhead];
+#pragma unroll
+    for (int d = 0; d < kAhead; ++d) q[d] = fetch(32 * d + lane);
+    for (int64_t p0 = 0; p0 < total; p0 += 32 * kAhead) {
+#pragma unroll
+        for (int d = 0; d < kAhead; ++d) {
+            const unsigned long long cur = q[d];
+            q[d] = fetch(p0 + 32 * (d + kAhead) + lane);
+            if (p0 + 32 * d < total) append_entries<MAPPED>(wb, cs, kk, lane, cur, p0 + 32 * d + lane < total);
+        }
+    }
+    if (cs.n > kk) { const Pruned pq = buf_prune<MAPPED>(wb, cs.n, kk, lane); cs.n = pq.n; cs.own = pq.t; }
+    emit_column(a, r, c, wb, cs.n, lane);
+    if (lane == 0) a.col_ticket[tix] = 0u;   // ready for the next launch
+}
+
+// Issue the bulk copy of stage i of slice [J0, J1) into ring slot i % kStages.
+// Only vectors wholly inside the buffer are copied; the (at most two) edge
+// vectors of the buffer are read element by element by the consumer.
+__device__ __forceinline__ void issue_stage(const Run &r, WarpSmem &ws, int64_t J0, int64_t J1, int64_t i)
+{
+    const int st = (int)(i % kStages);
+    const int64_t vs = J0 + i * kStageVec;
+    const int64_t ve = vs + kStageVec < J1 ? vs + kStageVec : J1;
+    const int64_t is = vs > r.jlo ? vs : r.jlo;
+    const int64_t ie = ve < r.jhi ? ve : r.jhi;
+    const uint32_t bytes = ie > is ? (uint32_t)((ie - is) * 16) : 0u;
+    fence_proxy_async();
+    mbar_arrive_expect_tx(&ws.full[st], bytes);
+    if (bytes) bulk_g2s(&ws.ring[st][is - vs], r.vb + is, bytes, &ws.full[st]);
+}
+
+// One warp streams its slice w of run r: every column segment gets a
+// candidate buffer and a threshold; finished columns are emitted or merged.
+template <int SLOTS, bool MAPPED>
+__device__ __forceinline__ void stream_slice(const RoundArgs &a, const Run &r, int w,
+                                             const int32_t *__restrict__ id_map, WarpSmem &ws, int lane)
+{
+    const int64_t J0 = slice_start(r, w), J1 = slice_start(r, w + 1);
+    if (J1 <= J0) return;
+    const int64_t nst = (J1 - J0 + kStageVec - 1) / kStageVec;
+    const int kk = r.kk;
+    unsigned long long *wb = ws.buf;
+    if (lane == 0)
+        for (int64_t i = 0; i < nst && i < kStages; ++i) issue_stage(r, ws, J0, J1, i);
+
+    int64_t c = first_elem(r, w) / r.V;       // current column
+    ColState cs = {0, 0u, 0u, false, 0};
+
+    for (int64_t i = 0; i < nst; ++i) {
+        const int st = (int)(i % kStages);
+        mbar_wait(&ws.full[st], (uint32_t)(i / kStages) & 1u);
+        const int64_t vs = J0 + i * kStageVec;
+        const int64_t ve = vs + kStageVec < J1 ? vs + kStageVec : J1;
+        const int64_t g_first = 8 * vs - r.mis > 0 ? 8 * vs - r.mis : 0;
+        const int64_t g_end = 8 * ve - r.mis < r.N ? 8 * ve - r.mis : r.N;   // exclusive
+        for (;;) {
+            // the part of column c inside this stage, elements outside as NaN
+            const int64_t cb = c * r.V, ce = cb + r.V;
+            const bool whole = cb <= g_first && ce >= g_end;
+            uint4 y[kLaneVec];
+            if (whole && ve - vs == kStageVec && vs >= r.jlo && ve <= r.jhi) {
+                // the common case: a full stage, inside one column, no buffer edge
+                const uint4 *src = &ws.ring[st][lane];
+#pragma unroll
+                for (int u = 0; u < kLaneVec; ++u) y[u] = src[u * 32];
+            } else {
+#pragma unroll
+                for (int u = 0; u < kLaneVec; ++u) {
+                    const int64_t j = vs + u * 32 + lane;
+                    if (j >= ve) y[u] = make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
+                    else if (j < r.jlo || j >= r.jhi) {
+                        y[u] = load_edge(r.buf, j, r.mis, cb, ce < r.N ? ce : r.N);
+                        ws.ring[st][j - vs] = y[u];   // edge vectors are not copied in: keep them here
+                    }
+                    else y[u] = ws.ring[st][j - vs];
+                    if (!whole) {
+                        const int64_t g0 = 8 * j - r.mis;
+                        uint32_t wv[4] = {y[u].x, y[u].y, y[u].z, y[u].w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const int64_t ga = g0 + 2 * h;
+                            if (ga < cb || ga >= ce) wv[h] = (wv[h] & 0xFFFF0000u) | 0x7FFFu;
+                            if (ga + 1 < cb || ga + 1 >= ce) wv[h] = (wv[h] & 0x0000FFFFu) | 0x7FFF0000u;
+                        }
+                        y[u] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    }
+                }
+            }
+
+            cs.open = true;
+            if (cs.seen < 8 * kStageVec) {
+                // seed, until the warp has seen a full stage of the column: the
+                // kk-th largest of the group maxima certifies kk elements
+                constexpr int G = (SLOTS == 1) ? 1 : 4;
+                constexpr int PER = kLaneVec / G;
+                uint32_t key[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    uint32_t m = vmax(y[g * PER]);
+#pragma unroll
+                    for (int u = 1; u < PER; ++u) m = bmax2(m, vmax(y[g * PER + u]));
+                    key[g] = order_key(hmax_splat(m) & 0xFFFFu);
+                }
+                uint32_t seed = 0;
+                if (kk == 1) {
+                    seed = __reduce_max_sync(kFull, key[0]);
+                } else {
+#pragma unroll 1
+                    for (int bit = 15; bit >= 0; --bit) {
+                        const uint32_t tr = seed | (1u << bit);
+                        int cnt = 0;
+#pragma unroll
+                        for (int g = 0; g < G; ++g) cnt += __popc(__ballot_sync(kFull, key[g] >= tr));
+                        if (cnt >= kk) seed = tr;
+                    }
+                }
+                cs.cert = seed > cs.cert ? seed : cs.cert;
+                const int64_t lo = cb > g_first ? cb : g_first, hi = ce < g_end ? ce : g_end;
+                cs.seen += (int)(hi - lo);
+            }
+            Filter f = make_filter(cs.own, cs.cert, MAPPED);
+            uint32_t m = vmax(y[0]);
+#pragma unroll
+            for (int u = 1; u < kLaneVec; ++u) m = bmax2(m, vmax(y[u]));
+            const bool pass = f.strict ? any_gt(m, f.thr2) : any_ge(m, f.thr2);
+            if (__ballot_sync(kFull, pass)) {
+                // append the candidates in increasing id order (vector u, then
+                // lane, then element); each is written by its own lane while
+                // the warp walks them with ballots
+                const int64_t id_lane = 8 * (vs + lane) - r.mis - cb;   // id of element 0, vector 0
+                const uint16_t *sv = reinterpret_cast<const uint16_t *>(&ws.ring[st][0]);
+                uint64_t bits = 0;   // this lane's candidates: bit 8u+e = element e of vector u
+#pragma unroll
+                for (int u = 0; u < kLaneVec; ++u)
+                    if (pass && (f.strict ? any_gt(vmax(y[u]), f.thr2) : any_ge(vmax(y[u]), f.thr2)))
+                        bits |= (uint64_t)elem_mask(y[u], f) << (8 * u);
+#pragma unroll 1
+                for (int u = 0; u < kLaneVec; ++u) {
+                    uint32_t cm = (uint32_t)(bits >> (8 * u)) & 0xFFu;
+                    const uint16_t *vv = sv + 8 * (u * 32 + lane);   // this lane's vector u in the stage
+                    uint32_t act = __ballot_sync(kFull, cm != 0u);
+                    while (act) {
+                        if (cs.n == kBufCap) {
+                            { const Pruned pq = buf_prune<MAPPED>(wb, cs.n, kk, lane); cs.n = pq.n; cs.own = pq.t; }
+                            f = make_filter(cs.own, cs.cert, MAPPED);
+                            uint32_t keep = 0;
+                            for (uint32_t rest = cm; rest; rest &= rest - 1) {
+                                const int e = __ffs(rest) - 1;
+                                const float v = bf16_as_float(vv[e]);
+                                if (f.strict ? v > f.thr : v >= f.thr) keep |= 1u << e;
+                            }
+                            cm = keep;
+                            act = __ballot_sync(kFull, cm != 0u);
+                            if (!act) break;
+                        }
+                        const int src = __ffs(act) - 1;
+                        if (lane == src) {
+                            const int e = __ffs(cm) - 1;
+                            cm &= cm - 1;
+                            uint32_t cid = (uint32_t)(id_lane + 256 * u + e);
+                            if (MAPPED) cid = (uint32_t)__ldg(id_map + cid);
+                            wb[cs.n] = pack_entry(bf16_as_float(vv[e]), cid);
+                        }
+                        ++cs.n;
+                        act = __ballot_sync(kFull, cm != 0u);
+                    }
+                }
+                __syncwarp();
+                // tighten the threshold once enough candidates have gathered
+                if (cs.n >= kk && (cs.own == 0 || cs.n >= kk + 16))
+                    { const Pruned pq = buf_prune<MAPPED>(wb, cs.n, kk, lane); cs.n = pq.n; cs.own = pq.t; }
+            }
+
+            if (ce > g_end) break;                    // column c goes on past this stage
+            finish_column<MAPPED>(a, r, w, c, wb, cs.n, cs.own, lane);
+            cs = {0, 0u, 0u, false, 0};
+            ++c;
+            if (c * r.V >= g_end) break;              // next column starts in a later stage
+        }
+        __syncwarp();                                  // every lane is done with the slot
+        if (lane == 0 && i + kStages < nst) issue_stage(r, ws, J0, J1, i + kStages);
+    }
+    // the slice ended inside column c: publish what this warp saw of it
+    if (cs.open) finish_column<MAPPED>(a, r, w, c, wb, cs.n, cs.own, lane);
 }
 
 template <int SLOTS, bool MAPPED>
-__global__ void __launch_bounds__(kThreads, 2) spec_round_kernel(const RoundArgs a)
+__global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_constant__ RoundArgs a)
 {
-    __shared__ Shared s;
-    for (int64_t u = blockIdx.x; u < a.n_units; u += gridDim.x) {
-        const bool draft = u < a.d_units;
-        const int64_t v = draft ? u : u - a.d_units;
-        const int parts = draft ? a.d_parts : a.t_parts;
-        const int64_t V = draft ? a.d_V : a.t_V;
-        const int64_t col = v / parts;
-        const int p = (int)(v - col * parts);
-        const int64_t e0 = (int64_t)p * V / parts, e1 = (int64_t)(p + 1) * V / parts;
-        const int kk = draft ? a.k : 1;
-
-        if (threadIdx.x == 0) s.thr = 0u;      // nobody reads it past the last unit's scan
-        __syncthreads();                       // previous unit's use of s is over
-        if (draft) scan_unit<SLOTS, MAPPED>(a.draft, V, col, e0, e1, kk, a.id_map, s.buf, &s.thr);
-        else scan_unit<1, false>(a.target, V, col, e0, e1, 1, nullptr, s.buf, &s.thr);
-        for (int i = threadIdx.x; i < kk; i += blockDim.x) s.out[i] = 0ull;
-        __syncthreads();
-        rank_merge(s.buf, kWarps, kListStride, kk, s.out);
-        __syncthreads();
-
-        if (parts == 1) {
-            finish_column(a, draft, col, kk, s);
-            continue;
-        }
-        // several units per column: publish, take a ticket, last one merges
-        unsigned long long *mine = a.partials + u * a.pstride;
-        for (int i = threadIdx.x; i < kk; i += blockDim.x) mine[i] = s.out[i];
-        __threadfence();
-        __syncthreads();
-        const int64_t tix = draft ? col : a.d_cols + col;
-        if (threadIdx.x == 0) s.flag = (atomicAdd(a.col_ticket + tix, 1u) == (unsigned)(parts - 1));
-        __syncthreads();
-        if (!s.flag) continue;
-        __threadfence();
-        const unsigned long long *first = a.partials + (u - p) * a.pstride;
-        for (int idx = threadIdx.x; idx < parts * kk; idx += blockDim.x) {
-            const int li = idx / kk, r = idx - li * kk;
-            s.buf[idx] = __ldcg(first + (int64_t)li * a.pstride + r);
-        }
-        for (int i = threadIdx.x; i < kk; i += blockDim.x) s.out[i] = 0ull;
-        __syncthreads();
-        rank_merge(s.buf, parts, kk, kk, s.out);
-        __syncthreads();
-        finish_column(a, draft, col, kk, s);
-        if (threadIdx.x == 0) a.col_ticket[tix] = 0u;   // ready for the next launch
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+    WarpSmem &ws = reinterpret_cast<WarpSmem *>(smem)[threadIdx.x >> 5];
+    if (gw >= a.d_warps + a.t_warps) return;
+    if (lane == 0) {
+        for (int st = 0; st < kStages; ++st) mbar_init(&ws.full[st], 1);
+        fence_mbar_init();
     }
+    __syncwarp();
+
+    Run r;
+    const bool draft = gw < a.d_warps;
+    r.draft = draft;
+    r.buf = draft ? a.draft : a.target;
+    r.V = draft ? a.d_V : a.t_V;
+    r.N = (draft ? a.d_cols : a.t_cols) * r.V;
+    r.W = draft ? a.d_warps : a.t_warps;
+    r.gw0 = draft ? 0 : a.d_warps;
+    r.kk = draft ? a.k : 1;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(r.buf);
+    r.mis = (int)((a0 >> 1) & 7);                       // element phase of buf in 16 B
+    r.vb = reinterpret_cast<const uint4 *>(a0 - 2 * (uintptr_t)r.mis);
+    r.NV = (r.N + r.mis + 7) >> 3;
+    r.jlo = r.mis ? 1 : 0;
+    r.jhi = ((r.N + r.mis) & 7) ? r.NV - 1 : r.NV;
+    if (r.jhi < r.jlo) r.jhi = r.jlo;
+    const int w = gw - r.gw0;
+    if (draft) stream_slice<SLOTS, MAPPED>(a, r, w, a.id_map, ws, lane);
+    else stream_slice<1, false>(a, r, w, nullptr, ws, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -585,7 +824,9 @@ spec_status device_state(DeviceState **out)
                           {kernel_ptr<2, false>(), kernel_ptr<2, true>()}};
         for (int s = 0; s < 2; ++s)
             for (int m = 0; m < 2; ++m) {
-                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ[s][m], kp[s][m], kThreads, 0);
+                e = cudaFuncSetAttribute(kp[s][m], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+                if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ[s][m], kp[s][m], kThreads, kSmemBytes);
                 if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
                 if (d.occ[s][m] < 1) d.occ[s][m] = 1;
             }
@@ -677,25 +918,40 @@ spec_status ensure_scratch(DeviceState &d, const ScratchCaps &need, cudaStream_t
     return SPEC_OK;
 }
 
-// Choose the number of parts per column: minimise the slowest CTA's work
-// (units are handed out round-robin), counting a fixed cost per unit and
-// per cross-CTA merge, in element-equivalents.
-int choose_parts(int64_t n_cols, int64_t V, int64_t max_ctas)
+int64_t vectors_of(const void *buf, int64_t n_elems)
 {
-    const int64_t kUnitCost = 3000, kMergeCost = 6000;
-    int64_t pmax = V / 2048;
-    if (pmax < 1) pmax = 1;
-    if (pmax > kMaxParts) pmax = kMaxParts;
-    int best = 1;
-    int64_t best_cost = INT64_MAX;
-    for (int64_t P = 1; P <= pmax; ++P) {
-        const int64_t units = n_cols * P;
-        const int64_t ctas = units < max_ctas ? units : max_ctas;
-        const int64_t rounds = (units + ctas - 1) / ctas;
-        const int64_t cost = rounds * ((V + P - 1) / P + kUnitCost) + (P > 1 ? kMergeCost : 0);
-        if (cost < best_cost) { best_cost = cost; best = (int)P; }
+    const int64_t mis = (int64_t)((reinterpret_cast<uintptr_t>(buf) >> 1) & 7);
+    return (n_elems + mis + 7) >> 3;
+}
+
+// Split the warps of a full-GPU grid between the draft and the target logits
+// in proportion to their 16-byte vectors, so that every warp streams the same
+// number of bytes.  No slice is made smaller than kMinSliceVec vectors, and
+// the published lists (two per warp, kk_stride entries each) must fit in
+// max_partials entries.
+void split_warps(int64_t nv_d, int64_t nv_t, int64_t max_warps, int kk_stride, int64_t max_partials,
+                 int32_t *w_d, int32_t *w_t)
+{
+    int64_t total = max_warps;
+    const int64_t cap = max_partials / (2 * (int64_t)kk_stride);
+    if (total > cap) total = cap;
+    if (total < 2) total = 2;
+    auto limit = [](int64_t nv) { const int64_t m = nv / kMinSliceVec; return m < 1 ? (int64_t)1 : m; };
+    int64_t d = 0, t = 0;
+    if (nv_d > 0 && nv_t > 0) {
+        d = (int64_t)((double)total * (double)nv_d / (double)(nv_d + nv_t) + 0.5);
+        if (d < 1) d = 1;
+        if (d > total - 1) d = total - 1;
+        t = total - d;
+    } else if (nv_d > 0) {
+        d = total;
+    } else {
+        t = total;
     }
-    return best;
+    if (nv_d > 0 && d > limit(nv_d)) d = limit(nv_d);
+    if (nv_t > 0 && t > limit(nv_t)) t = limit(nv_t);
+    *w_d = (int32_t)d;
+    *w_t = (int32_t)t;
 }
 
 bool misaligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
@@ -751,17 +1007,12 @@ spec_status launch_round(const uint16_t *draft, int64_t cols, int64_t V, int32_t
     a.id_map = id_map; a.out_vals = vals; a.out_ids = ids;
     a.target = target; a.t_cols = t_cols; a.t_V = lanes ? tV : 1; a.gamma = gamma;
     a.drafts = drafts; a.out_accept = acc; a.out_commit = com;
-    if (cols > 0 && lanes > 0 && V == tV) {
-        a.d_parts = a.t_parts = choose_parts(cols + t_cols, V, max_ctas);
-    } else {
-        a.d_parts = cols ? choose_parts(cols, V, max_ctas) : 1;
-        a.t_parts = lanes ? choose_parts(t_cols, tV, max_ctas) : 1;
-    }
-    a.d_units = cols * a.d_parts;
-    a.n_units = a.d_units + t_cols * a.t_parts;
-    a.pstride = a.k;
+    a.pstride = a.k + 1;
+    split_warps(cols ? vectors_of(draft, cols * V) : 0, lanes ? vectors_of(target, t_cols * tV) : 0,
+                max_ctas * kWarpsPerCta, a.pstride, INT64_MAX / 4, &a.d_warps, &a.t_warps);
     cudaStream_t stream = t_stream;
-    const ScratchCaps need = {cols + t_cols, lanes, t_cols, a.n_units * a.pstride};
+    const int64_t nwarps = (int64_t)a.d_warps + a.t_warps;
+    const ScratchCaps need = {cols + t_cols, lanes, t_cols, nwarps * 2 * a.pstride};
     st = ensure_scratch(*d, need, stream);
     if (st != SPEC_OK) return st;
     const ScratchPtrs sp = scratch_ptrs(*d);
@@ -770,12 +1021,11 @@ spec_status launch_round(const uint16_t *draft, int64_t cols, int64_t V, int32_t
     a.lane_ticket = sp.lane_ticket;
     a.t_argmax = sp.t_argmax;
 
-    const int64_t grid64 = a.n_units < max_ctas ? a.n_units : max_ctas;
-    const dim3 grid((unsigned)grid64), block(kThreads);
-    if (slots == 1 && !mapped) spec_round_kernel<1, false><<<grid, block, 0, stream>>>(a);
-    else if (slots == 1) spec_round_kernel<1, true><<<grid, block, 0, stream>>>(a);
-    else if (!mapped) spec_round_kernel<2, false><<<grid, block, 0, stream>>>(a);
-    else spec_round_kernel<2, true><<<grid, block, 0, stream>>>(a);
+    const dim3 grid((unsigned)((nwarps + kWarpsPerCta - 1) / kWarpsPerCta)), block(kThreads);
+    if (slots == 1 && !mapped) spec_round_kernel<1, false><<<grid, block, kSmemBytes, stream>>>(a);
+    else if (slots == 1) spec_round_kernel<1, true><<<grid, block, kSmemBytes, stream>>>(a);
+    else if (!mapped) spec_round_kernel<2, false><<<grid, block, kSmemBytes, stream>>>(a);
+    else spec_round_kernel<2, true><<<grid, block, kSmemBytes, stream>>>(a);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -929,7 +1179,8 @@ spec_status spec_reserve(int64_t max_cols, int32_t max_k, int64_t max_lanes, int
     spec_status st = device_state(&d);
     if (st != SPEC_OK) return st;
     const int64_t t_cols = max_lanes * (max_gamma + 1);
-    const ScratchCaps need = {max_cols + t_cols, max_lanes, t_cols, (max_cols + t_cols) * kMaxParts * max_k};
+    const ScratchCaps need = {max_cols + t_cols, max_lanes, t_cols,
+                              (int64_t)d->sms * d->occ[max_k > 32 ? 1 : 0][0] * kWarpsPerCta * 2 * (max_k + 1)};
     return ensure_scratch(*d, need, t_stream);
 }
 
@@ -956,6 +1207,20 @@ spec_status spec_release(void)
 const char *spec_last_error(void) { return t_err.c_str(); }
 
 int64_t spec_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+spec_status spec_device_status(void)
+{
+    t_err.clear();
+    cudaError_t e = cudaStreamSynchronize(t_stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned int flags = 0, zero = 0;
+    e = cudaMemcpyFromSymbol(&flags, g_wait_timeouts, sizeof flags);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol");
+    if (flags == 0) return SPEC_OK;
+    e = cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
+    return fail(SPEC_ERR_CUDA, "a kernel gave up a bounded wait on its copy pipeline; its results are invalid");
+}
 
 }  // extern "C"
 
@@ -1045,14 +1310,11 @@ extern "C" spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t 
     a.out_vals = out_vals; a.out_ids = out_ids;
     a.target = target_logits; a.t_cols = t_cols; a.t_V = lanes ? V : 1; a.gamma = gamma;
     a.drafts = drafts; a.out_accept = out_accept_len; a.out_commit = out_commit_ids;
-    a.pstride = a.k;
-    // parts per column as in spec_round, capped so the partial lists fit
-    int parts = choose_parts(cols + t_cols, V, max_ctas);
-    const int64_t cap = kNoAllocPartials / ((cols + t_cols) * (int64_t)a.pstride);
-    if (parts > cap) parts = cap < 1 ? 1 : (int)cap;        // one part per column needs no partials
-    a.d_parts = a.t_parts = parts;
-    a.d_units = cols * parts;
-    a.n_units = a.d_units + t_cols * parts;
+    a.pstride = a.k + 1;
+    // warps as in spec_round, fewer if their published lists would not fit
+    split_warps(cols ? vectors_of(draft_logits, cols * V) : 0, lanes ? vectors_of(target_logits, t_cols * V) : 0,
+                max_ctas * kWarpsPerCta, a.pstride, kNoAllocPartials, &a.d_warps, &a.t_warps);
+    const int64_t nwarps = (int64_t)a.d_warps + a.t_warps;
     char *p = static_cast<char *>(base);
     a.col_ticket = reinterpret_cast<unsigned int *>(p + kNoAllocColTicket);
     a.lane_ticket = reinterpret_cast<unsigned int *>(p + kNoAllocLaneTicket);
@@ -1063,10 +1325,9 @@ extern "C" spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t 
     // the array keeps whatever the last call left: start every ticket at zero
     cudaError_t e = cudaMemsetAsync(base, 0, kNoAllocTicketBytes, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch tickets)");
-    const int64_t grid64 = a.n_units < max_ctas ? a.n_units : max_ctas;
-    const dim3 grid((unsigned)grid64), block(kThreads);
-    if (slots == 1) spec_round_kernel<1, false><<<grid, block, 0, stream>>>(a);
-    else spec_round_kernel<2, false><<<grid, block, 0, stream>>>(a);
+    const dim3 grid((unsigned)((nwarps + kWarpsPerCta - 1) / kWarpsPerCta)), block(kThreads);
+    if (slots == 1) spec_round_kernel<1, false><<<grid, block, kSmemBytes, stream>>>(a);
+    else spec_round_kernel<2, false><<<grid, block, kSmemBytes, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);

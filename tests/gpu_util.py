@@ -64,6 +64,7 @@ def run_topk(x_host: np.ndarray, k: int, offset: int = 0, id_map: np.ndarray | N
     else:
         sd.spec_topk_mapped(x, cols, V, k, dev_i32(id_map), vals.view, ids.view)
     torch.cuda.synchronize()
+    sd.spec_device_status()
     vals.check_guards()
     ids.check_guards()
     return vals.host().view(np.uint16).reshape(cols, k), ids.host().reshape(cols, k)
@@ -79,6 +80,7 @@ def run_verify(t_host: np.ndarray, drafts: np.ndarray, offset: int = 0):
     com = Guarded(lanes * (gamma + 1), torch.int32)
     sd.spec_verify_v(t, dev_i32(drafts), lanes, gamma, V, acc.view, com.view)
     torch.cuda.synchronize()
+    sd.spec_device_status()
     acc.check_guards()
     com.check_guards()
     return acc.host(), com.host().reshape(lanes, gamma + 1)
@@ -97,6 +99,7 @@ def run_round(x_host, k, t_host, drafts, offset: int = 0):
     com = Guarded(lanes * (gamma + 1), torch.int32)
     sd.spec_round(x, cols, V, k, vals.view, ids.view, t, dev_i32(drafts), lanes, gamma, acc.view, com.view)
     torch.cuda.synchronize()
+    sd.spec_device_status()
     for g in (vals, ids, acc, com):
         g.check_guards()
     return (vals.host().view(np.uint16).reshape(cols, k), ids.host().reshape(cols, k), acc.host(),
