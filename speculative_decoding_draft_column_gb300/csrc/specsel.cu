@@ -89,8 +89,9 @@ struct RoundArgs {
     // warps [0, d_warps) stream the draft logits, [d_warps, d_warps + t_warps) the target logits
     int32_t d_warps, t_warps;
     // scratch
-    unsigned long long *partials;   // [(d_warps + t_warps) * 2][pstride = k + 1]
+    unsigned long long *partials;   // [(d_warps + t_warps) * 2][pstride = k + 2]
     unsigned int *col_ticket;       // [d_cols + t_cols]
+    unsigned int *col_cert;         // [d_cols + t_cols]: best certified key published for a split column
     unsigned int *lane_ticket;      // [lanes]
     int32_t *t_argmax;              // [t_cols]
     int32_t pstride;
@@ -201,6 +202,27 @@ __device__ __forceinline__ uint32_t lanemask_lt()
     return m;
 }
 
+// Exclusive prefix sum of v over the warp; also returns the warp total.
+__device__ __forceinline__ int warp_exclusive_sum(int v, int lane, int &total)
+{
+    int incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, d);
+        if (lane >= d) incl += y;
+    }
+    total = __shfl_sync(kFull, incl, 31);
+    return incl - v;
+}
+
+// A 32-bit word other SMs update with atomics, read through L2.
+__device__ __forceinline__ uint32_t ld_relaxed(const unsigned int *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // ---- mbarrier / bulk-copy primitives (inline PTX, sm_90+) -------------------
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -267,17 +289,16 @@ __device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier
 
 // ---- candidate buffers ------------------------------------------------------
 
-// Prune the warp buffer wb[0..n) (n >= kk, entries in increasing id order) to
-// its kk best entries, keeping their order; returns kk and, in tkey, the
-// kk-th largest key (kk entries reach it: a certificate).  Without an id map
-// ties at that key go to the earliest entries (smallest ids); with one, to
-// the smallest mapped ids.
 struct Pruned {
     int n;       // entries kept (kk)
     uint32_t t;  // their certificate: the kk-th largest key
 };
 
-template <bool MAPPED>
+// Prune the warp buffer wb[0..n) (n >= kk, any order) to its kk best
+// entries; returns kk and the kk-th largest key t (kk entries reach it: a
+// certificate).  Ties at t go to the smallest ids (token ids, or mapped
+// vocabulary ids for a shortlist), found by a bisection over the id bits only
+// when there are more ties than places.
 __device__ __noinline__ Pruned buf_prune(unsigned long long *wb, int n, int kk, int lane)
 {
     constexpr int Q = kBufCap / 32;
@@ -298,42 +319,35 @@ __device__ __noinline__ Pruned buf_prune(unsigned long long *wb, int n, int kk, 
         for (int q = 0; q < Q; ++q) cnt += __popc(__ballot_sync(kFull, key[q] >= tr));
         if (cnt >= kk) t = tr;
     }
-    int cgt = 0;
+    int cgt = 0, ceq = 0;
 #pragma unroll
-    for (int q = 0; q < Q; ++q) cgt += __popc(__ballot_sync(kFull, key[q] > t));
+    for (int q = 0; q < Q; ++q) {
+        cgt += __popc(__ballot_sync(kFull, key[q] > t));
+        ceq += __popc(__ballot_sync(kFull, key[q] == t && e[q] != 0ull));
+    }
     const int quota = kk - cgt;   // entries with key == t that survive
-    bool keep[Q];
-    if constexpr (!MAPPED) {
-        int seen = 0;
+    uint32_t tid[Q];
 #pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            const bool eq = key[q] == t && e[q] != 0ull;
-            const uint32_t bal = __ballot_sync(kFull, eq);
-            keep[q] = key[q] > t || (eq && seen + __popc(bal & lanemask_lt()) < quota);
-            seen += __popc(bal);
-        }
-    } else {
-        uint32_t mid[Q];
-#pragma unroll
-        for (int q = 0; q < Q; ++q) mid[q] = (key[q] == t && e[q] != 0ull) ? entry_id(e[q]) : 0xFFFFFFFFu;
-        uint32_t m = 0;   // the quota-th smallest mapped id among the ties (ids < 2^31)
+    for (int q = 0; q < Q; ++q) tid[q] = (key[q] == t && e[q] != 0ull) ? entry_id(e[q]) : 0xFFFFFFFFu;
+    uint32_t m = 0x7FFFFFFFu;     // ties kept: id <= m (ids < 2^31)
+    if (ceq > quota) {
+        m = 0;   // the quota-th smallest id among the ties
 #pragma unroll 1
         for (int bit = 30; bit >= 0; --bit) {
             const uint32_t tr = m | (1u << bit);
             int cnt = 0;
 #pragma unroll
-            for (int q = 0; q < Q; ++q) cnt += __popc(__ballot_sync(kFull, mid[q] < tr));
+            for (int q = 0; q < Q; ++q) cnt += __popc(__ballot_sync(kFull, tid[q] < tr));
             if (cnt < quota) m = tr;
         }
-#pragma unroll
-        for (int q = 0; q < Q; ++q) keep[q] = key[q] > t || (mid[q] != 0xFFFFFFFFu && mid[q] <= m);
     }
     __syncwarp();
     int out = 0;
 #pragma unroll
     for (int q = 0; q < Q; ++q) {
-        const uint32_t bal = __ballot_sync(kFull, keep[q]);
-        if (keep[q]) wb[out + __popc(bal & lanemask_lt())] = e[q];
+        const bool keep = key[q] > t || (tid[q] != 0xFFFFFFFFu && tid[q] <= m);
+        const uint32_t bal = __ballot_sync(kFull, keep);
+        if (keep) wb[out + __popc(bal & lanemask_lt())] = e[q];
         out += __popc(bal);
     }
     __syncwarp();
@@ -384,32 +398,6 @@ struct ColState {
     bool open;      // the warp has started this column
     int seen;       // elements of the column this warp has scanned (saturating)
 };
-
-// Append one packed entry per lane (lanes with `valid`) in lane order, after
-// filtering against the column's current threshold; prunes when full.
-template <bool MAPPED>
-__device__ __noinline__ void append_entries(unsigned long long *wb, ColState &cs, int kk, int lane,
-                                            unsigned long long e, bool valid)
-{
-    for (;;) {
-        const Filter f = make_filter(cs.own, cs.cert, MAPPED);
-        const float v = bf16_as_float(entry_raw(e));
-        const bool ok = valid && e != 0ull && (f.strict ? v > f.thr : v >= f.thr);
-        const uint32_t bal = __ballot_sync(kFull, ok);
-        const int total = __popc(bal);
-        if (total == 0) return;
-        const int space = kBufCap - cs.n;
-        const int r = __popc(bal & lanemask_lt());
-        if (ok && r < space) wb[cs.n + r] = e;
-        __syncwarp();
-        if (total <= space) {
-            cs.n += total;
-            return;
-        }
-        valid = ok && r >= space;                    // the rest, after a prune
-        { const Pruned pq = buf_prune<MAPPED>(wb, kBufCap, kk, lane); cs.n = pq.n; cs.own = pq.t; }
-    }
-}
 
 // ---- the per-warp stream ------------------------------------------------------
 
@@ -501,15 +489,16 @@ __device__ __noinline__ void finish_column(const RoundArgs &a, const Run &r, int
 {
     ColState cs = {n_in, own_in, 0u, true, 0};
     const int kk = r.kk;
-    if (cs.n > kk) { const Pruned pq = buf_prune<MAPPED>(wb, cs.n, kk, lane); cs.n = pq.n; cs.own = pq.t; }
+    if (cs.n > kk) { const Pruned pq = buf_prune(wb, cs.n, kk, lane); cs.n = pq.n; cs.own = pq.t; }
     const int64_t wf = owner(r, (c * r.V + r.mis) >> 3);
     const int64_t wl = owner(r, ((c + 1) * r.V - 1 + r.mis) >> 3);
     if (wf == wl) {
         emit_column(a, r, c, wb, cs.n, lane);
         return;
     }
-    // publish: the list (kk entries, id order, 0-padded) and, in slot kk, its
-    // certificate -- the smallest key of a full list (kk entries reach it)
+    // publish: the list (kk entries, id order, 0-padded), in slot kk its
+    // certificate -- the smallest key of a full list (kk entries reach it) --
+    // and in slot kk + 1 its length
     uint32_t mk = 0xFFFFFFFFu;
     for (int i = lane; i < cs.n; i += 32) {
         const uint32_t ky = entry_key(wb[i]);
@@ -517,8 +506,11 @@ __device__ __noinline__ void finish_column(const RoundArgs &a, const Run &r, int
     }
     mk = __reduce_min_sync(kFull, mk);
     unsigned long long *mine = list_slot(a, r, w, c);
-    for (int i = lane; i <= kk; i += 32)
-        mine[i] = i < cs.n ? wb[i] : (i == kk ? (unsigned long long)(cs.n == kk ? mk : 0u) : 0ull);
+    for (int i = lane; i < cs.n; i += 32) mine[i] = wb[i];
+    if (lane == 0) {
+        mine[kk] = cs.n == kk ? mk : 0u;
+        mine[kk + 1] = (unsigned long long)cs.n;
+    }
     __threadfence();
     __syncwarp();
     const int64_t tix = r.draft ? c : a.d_cols + c;
@@ -526,12 +518,13 @@ __device__ __noinline__ void finish_column(const RoundArgs &a, const Run &r, int
     if (lane == 0) last = atomicAdd(a.col_ticket + tix, 1u) == (unsigned)(wl - wf);
     if (!__shfl_sync(kFull, last, 0)) return;
     __threadfence();
-    // merge: the best certificate first, then every list in slice order
-    // (hence id order) through the buffer, 32 entries per round, several
-    // rounds of loads in flight
+    // merge.  The best certificate (the column's shared one, or any full
+    // list's) bounds the column's kk-th key; only entries at or above it are
+    // gathered, list by list in slice order (hence id order), each lane
+    // loading one list, all lists in flight at once.
     cs.n = 0;
     cs.own = 0;
-    cs.cert = 0;
+    cs.cert = ld_relaxed(a.col_cert + tix);
     const int64_t nparts = wl - wf + 1;
     for (int64_t q0 = 0; q0 < nparts; q0 += 32) {
         uint32_t key = 0;
@@ -539,23 +532,54 @@ __device__ __noinline__ void finish_column(const RoundArgs &a, const Run &r, int
         key = __reduce_max_sync(kFull, key);
         cs.cert = key > cs.cert ? key : cs.cert;
     }
-    const int64_t total = nparts * kk;
-    auto fetch = [&](int64_t p) { return p < total ? __ldcg(list_slot(a, r, wf + p / kk, c) + p % kk) : 0ull; };
-    constexpr int kAhead = 4;
-    unsigned long long q[kAhead];
+    for (int64_t q0 = 0; q0 < nparts; q0 += 32) {
+        const bool mine_l = q0 + lane < nparts;
+        const unsigned long long *lst = mine_l ? list_slot(a, r, wf + q0 + lane, c) : nullptr;
+        const int len = mine_l ? (int)__ldcg(lst + kk + 1) : 0;
+        const int maxlen = __reduce_max_sync(kFull, len);
+        for (int i0 = 0; i0 < maxlen; i0 += 8) {
+            unsigned long long e8[8];
 #pragma unroll
-    for (int d = 0; d < kAhead; ++d) q[d] = fetch(32 * d + lane);
-    for (int64_t p0 = 0; p0 < total; p0 += 32 * kAhead) {
+            for (int i = 0; i < 8; ++i) e8[i] = i0 + i < len ? __ldcg(lst + i0 + i) : 0ull;
+            uint32_t ok = 0;
 #pragma unroll
-        for (int d = 0; d < kAhead; ++d) {
-            const unsigned long long cur = q[d];
-            q[d] = fetch(p0 + 32 * (d + kAhead) + lane);
-            if (p0 + 32 * d < total) append_entries<MAPPED>(wb, cs, kk, lane, cur, p0 + 32 * d + lane < total);
+            for (int i = 0; i < 8; ++i) ok |= (uint32_t)(e8[i] != 0ull && entry_key(e8[i]) >= cs.cert) << i;
+            for (;;) {
+                int total;
+                const int excl = warp_exclusive_sum(__popc(ok), lane, total);
+                if (total == 0) break;
+                const int space = kBufCap - cs.n;
+                int pos = excl;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if ((ok >> i) & 1u) {
+                        if (pos < space) {
+                            wb[cs.n + pos] = e8[i];
+                            ok &= ~(1u << i);
+                        }
+                        ++pos;
+                    }
+                __syncwarp();
+                if (total <= space) {
+                    cs.n += total;
+                    break;
+                }
+                const Pruned pq = buf_prune(wb, kBufCap, kk, lane);
+                cs.n = pq.n;
+                cs.own = pq.t;
+                if (cs.own > cs.cert) cs.cert = cs.own;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (entry_key(e8[i]) < cs.cert) ok &= ~(1u << i);
+            }
         }
     }
-    if (cs.n > kk) { const Pruned pq = buf_prune<MAPPED>(wb, cs.n, kk, lane); cs.n = pq.n; cs.own = pq.t; }
+    if (cs.n > kk) { const Pruned pq = buf_prune(wb, cs.n, kk, lane); cs.n = pq.n; cs.own = pq.t; }
     emit_column(a, r, c, wb, cs.n, lane);
-    if (lane == 0) a.col_ticket[tix] = 0u;   // ready for the next launch
+    if (lane == 0) {
+        a.col_ticket[tix] = 0u;   // ready for the next launch
+        a.col_cert[tix] = 0u;
+    }
 }
 
 // Issue the bulk copy of stage i of slice [J0, J1) into ring slot i % kStages.
@@ -590,6 +614,12 @@ __device__ __forceinline__ void stream_slice(const RoundArgs &a, const Run &r, i
 
     int64_t c = first_elem(r, w) / r.V;       // current column
     ColState cs = {0, 0u, 0u, false, 0};
+    // a column split across warps has a shared certificate in global memory:
+    // every warp raises it with its own certified keys and filters against
+    // it (read one stage late, so the load latency hides behind the stream)
+    bool shared = false;
+    int64_t tix = 0;
+    uint32_t gcert = 0;
 
     for (int64_t i = 0; i < nst; ++i) {
         const int st = (int)(i % kStages);
@@ -632,7 +662,13 @@ __device__ __forceinline__ void stream_slice(const RoundArgs &a, const Run &r, i
                 }
             }
 
-            cs.open = true;
+            if (!cs.open) {
+                cs.open = true;
+                shared = owner(r, (c * r.V + r.mis) >> 3) != owner(r, ((c + 1) * r.V - 1 + r.mis) >> 3);
+                tix = r.draft ? c : a.d_cols + c;
+                gcert = 0;
+            }
+            if (gcert > cs.cert) cs.cert = gcert;
             if (cs.seen < 8 * kStageVec) {
                 // seed, until the warp has seen a full stage of the column: the
                 // kk-th largest of the group maxima certifies kk elements
@@ -660,6 +696,7 @@ __device__ __forceinline__ void stream_slice(const RoundArgs &a, const Run &r, i
                     }
                 }
                 cs.cert = seed > cs.cert ? seed : cs.cert;
+                if (shared && lane == 0 && seed > gcert) atomicMax(a.col_cert + tix, seed);
                 const int64_t lo = cb > g_first ? cb : g_first, hi = ce < g_end ? ce : g_end;
                 cs.seen += (int)(hi - lo);
             }
@@ -669,9 +706,9 @@ __device__ __forceinline__ void stream_slice(const RoundArgs &a, const Run &r, i
             for (int u = 1; u < kLaneVec; ++u) m = bmax2(m, vmax(y[u]));
             const bool pass = f.strict ? any_gt(m, f.thr2) : any_ge(m, f.thr2);
             if (__ballot_sync(kFull, pass)) {
-                // append the candidates in increasing id order (vector u, then
-                // lane, then element); each is written by its own lane while
-                // the warp walks them with ballots
+                // append the candidates: one warp prefix sum gives every lane
+                // its places, each lane writes its own (their order in the
+                // buffer does not matter, ties are settled by id when pruning)
                 const int64_t id_lane = 8 * (vs + lane) - r.mis - cb;   // id of element 0, vector 0
                 const uint16_t *sv = reinterpret_cast<const uint16_t *>(&ws.ring[st][0]);
                 uint64_t bits = 0;   // this lane's candidates: bit 8u+e = element e of vector u
@@ -679,41 +716,49 @@ __device__ __forceinline__ void stream_slice(const RoundArgs &a, const Run &r, i
                 for (int u = 0; u < kLaneVec; ++u)
                     if (pass && (f.strict ? any_gt(vmax(y[u]), f.thr2) : any_ge(vmax(y[u]), f.thr2)))
                         bits |= (uint64_t)elem_mask(y[u], f) << (8 * u);
-#pragma unroll 1
-                for (int u = 0; u < kLaneVec; ++u) {
-                    uint32_t cm = (uint32_t)(bits >> (8 * u)) & 0xFFu;
-                    const uint16_t *vv = sv + 8 * (u * 32 + lane);   // this lane's vector u in the stage
-                    uint32_t act = __ballot_sync(kFull, cm != 0u);
-                    while (act) {
-                        if (cs.n == kBufCap) {
-                            { const Pruned pq = buf_prune<MAPPED>(wb, cs.n, kk, lane); cs.n = pq.n; cs.own = pq.t; }
-                            f = make_filter(cs.own, cs.cert, MAPPED);
-                            uint32_t keep = 0;
-                            for (uint32_t rest = cm; rest; rest &= rest - 1) {
-                                const int e = __ffs(rest) - 1;
-                                const float v = bf16_as_float(vv[e]);
-                                if (f.strict ? v > f.thr : v >= f.thr) keep |= 1u << e;
-                            }
-                            cm = keep;
-                            act = __ballot_sync(kFull, cm != 0u);
-                            if (!act) break;
-                        }
-                        const int src = __ffs(act) - 1;
-                        if (lane == src) {
-                            const int e = __ffs(cm) - 1;
-                            cm &= cm - 1;
-                            uint32_t cid = (uint32_t)(id_lane + 256 * u + e);
-                            if (MAPPED) cid = (uint32_t)__ldg(id_map + cid);
-                            wb[cs.n] = pack_entry(bf16_as_float(vv[e]), cid);
-                        }
-                        ++cs.n;
-                        act = __ballot_sync(kFull, cm != 0u);
+                for (;;) {
+                    int total;
+                    const int excl = warp_exclusive_sum(__popcll(bits), lane, total);
+                    if (total == 0) break;
+                    const int space = kBufCap - cs.n;
+                    int pos = excl;
+                    uint64_t rest = bits;
+                    while (rest && pos < space) {
+                        const int b = __ffsll((long long)rest) - 1;
+                        rest &= rest - 1;
+                        const int u = b >> 3, e = b & 7;
+                        uint32_t cid = (uint32_t)(id_lane + 256 * u + e);
+                        if (MAPPED) cid = (uint32_t)__ldg(id_map + cid);
+                        wb[cs.n + pos] = pack_entry(bf16_as_float(sv[8 * (u * 32 + lane) + e]), cid);
+                        ++pos;
                     }
+                    __syncwarp();
+                    if (total <= space) {
+                        cs.n += total;
+                        break;
+                    }
+                    // the buffer is full: prune it, then keep only what still
+                    // reaches the new key (inclusively: the rest of this
+                    // stage may hold smaller ids than entries just kept)
+                    const Pruned pq = buf_prune(wb, kBufCap, kk, lane);
+                    cs.n = pq.n;
+                    cs.own = pq.t;
+                    const float tv = bf16_as_float(key_to_raw(cs.own));
+                    uint64_t keep = 0;
+                    for (uint64_t q = rest; q; q &= q - 1) {
+                        const int b = __ffsll((long long)q) - 1;
+                        if (bf16_as_float(sv[8 * ((b >> 3) * 32 + lane) + (b & 7)]) >= tv) keep |= 1ull << b;
+                    }
+                    bits = keep;
                 }
                 __syncwarp();
                 // tighten the threshold once enough candidates have gathered
-                if (cs.n >= kk && (cs.own == 0 || cs.n >= kk + 16))
-                    { const Pruned pq = buf_prune<MAPPED>(wb, cs.n, kk, lane); cs.n = pq.n; cs.own = pq.t; }
+                if (cs.n >= kk && (cs.own == 0 || cs.n >= kk + 16)) {
+                    const Pruned pq = buf_prune(wb, cs.n, kk, lane);
+                    cs.n = pq.n;
+                    cs.own = pq.t;
+                    if (shared && lane == 0 && cs.own > cs.cert) atomicMax(a.col_cert + tix, cs.own);
+                }
             }
 
             if (ce > g_end) break;                    // column c goes on past this stage
@@ -724,6 +769,7 @@ __device__ __forceinline__ void stream_slice(const RoundArgs &a, const Run &r, i
         }
         __syncwarp();                                  // every lane is done with the slot
         if (lane == 0 && i + kStages < nst) issue_stage(r, ws, J0, J1, i + kStages);
+        if (cs.open && shared) gcert = ld_relaxed(a.col_cert + tix);
     }
     // the slice ended inside column c: publish what this warp saw of it
     if (cs.open) finish_column<MAPPED>(a, r, w, c, wb, cs.n, cs.own, lane);
@@ -1007,17 +1053,18 @@ spec_status launch_round(const uint16_t *draft, int64_t cols, int64_t V, int32_t
     a.id_map = id_map; a.out_vals = vals; a.out_ids = ids;
     a.target = target; a.t_cols = t_cols; a.t_V = lanes ? tV : 1; a.gamma = gamma;
     a.drafts = drafts; a.out_accept = acc; a.out_commit = com;
-    a.pstride = a.k + 1;
+    a.pstride = a.k + 2;
     split_warps(cols ? vectors_of(draft, cols * V) : 0, lanes ? vectors_of(target, t_cols * tV) : 0,
                 max_ctas * kWarpsPerCta, a.pstride, INT64_MAX / 4, &a.d_warps, &a.t_warps);
     cudaStream_t stream = t_stream;
     const int64_t nwarps = (int64_t)a.d_warps + a.t_warps;
-    const ScratchCaps need = {cols + t_cols, lanes, t_cols, nwarps * 2 * a.pstride};
+    const ScratchCaps need = {2 * (cols + t_cols), lanes, t_cols, nwarps * 2 * a.pstride};
     st = ensure_scratch(*d, need, stream);
     if (st != SPEC_OK) return st;
     const ScratchPtrs sp = scratch_ptrs(*d);
     a.partials = sp.partials;
     a.col_ticket = sp.col_ticket;
+    a.col_cert = sp.col_ticket + (cols + t_cols);
     a.lane_ticket = sp.lane_ticket;
     a.t_argmax = sp.t_argmax;
 
@@ -1179,8 +1226,8 @@ spec_status spec_reserve(int64_t max_cols, int32_t max_k, int64_t max_lanes, int
     spec_status st = device_state(&d);
     if (st != SPEC_OK) return st;
     const int64_t t_cols = max_lanes * (max_gamma + 1);
-    const ScratchCaps need = {max_cols + t_cols, max_lanes, t_cols,
-                              (int64_t)d->sms * d->occ[max_k > 32 ? 1 : 0][0] * kWarpsPerCta * 2 * (max_k + 1)};
+    const ScratchCaps need = {2 * (max_cols + t_cols), max_lanes, t_cols,
+                              (int64_t)d->sms * d->occ[max_k > 32 ? 1 : 0][0] * kWarpsPerCta * 2 * (max_k + 2)};
     return ensure_scratch(*d, need, t_stream);
 }
 
@@ -1244,11 +1291,11 @@ constexpr int64_t kNoAllocMaxCols = SPEC_NOALLOC_MAX_COLS;     // draft + target
 constexpr int64_t kNoAllocMaxLanes = SPEC_NOALLOC_MAX_LANES;
 constexpr int64_t kNoAllocPartials = 131072;                    // partial-list entries (1 MiB)
 constexpr size_t kNoAllocColTicket = 0;
-constexpr size_t kNoAllocLaneTicket = kNoAllocColTicket + ((kNoAllocMaxCols * 4 + 255) & ~int64_t(255));
+constexpr size_t kNoAllocLaneTicket = kNoAllocColTicket + ((2 * kNoAllocMaxCols * 4 + 255) & ~int64_t(255));
 constexpr size_t kNoAllocArgmax = kNoAllocLaneTicket + ((kNoAllocMaxLanes * 4 + 255) & ~int64_t(255));
 constexpr size_t kNoAllocPart = kNoAllocArgmax + ((kNoAllocMaxCols * 4 + 255) & ~int64_t(255));
 constexpr size_t kNoAllocBytes = kNoAllocPart + kNoAllocPartials * 8;
-constexpr size_t kNoAllocTicketBytes = kNoAllocArgmax;         // both ticket arrays, cleared per call
+constexpr size_t kNoAllocTicketBytes = kNoAllocArgmax;         // tickets and column certificates, cleared per call
 
 // Device scratch of spec_round_noalloc.  In host code this name only stands
 // for the symbol; the device address comes from cudaGetSymbolAddress.
@@ -1310,13 +1357,14 @@ extern "C" spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t 
     a.out_vals = out_vals; a.out_ids = out_ids;
     a.target = target_logits; a.t_cols = t_cols; a.t_V = lanes ? V : 1; a.gamma = gamma;
     a.drafts = drafts; a.out_accept = out_accept_len; a.out_commit = out_commit_ids;
-    a.pstride = a.k + 1;
+    a.pstride = a.k + 2;
     // warps as in spec_round, fewer if their published lists would not fit
     split_warps(cols ? vectors_of(draft_logits, cols * V) : 0, lanes ? vectors_of(target_logits, t_cols * V) : 0,
                 max_ctas * kWarpsPerCta, a.pstride, kNoAllocPartials, &a.d_warps, &a.t_warps);
     const int64_t nwarps = (int64_t)a.d_warps + a.t_warps;
     char *p = static_cast<char *>(base);
     a.col_ticket = reinterpret_cast<unsigned int *>(p + kNoAllocColTicket);
+    a.col_cert = a.col_ticket + (cols + t_cols);
     a.lane_ticket = reinterpret_cast<unsigned int *>(p + kNoAllocLaneTicket);
     a.t_argmax = reinterpret_cast<int32_t *>(p + kNoAllocArgmax);
     a.partials = reinterpret_cast<unsigned long long *>(p + kNoAllocPart);
