@@ -252,17 +252,21 @@ def run_reference(args):
         return 0
     r = make_workload(args.config, args.k)
     threads = os.cpu_count() or 1
-    # per-step sample sized so that warm-up + steps stay within ~2 minutes
+    nt = 0 if r.target is None else r.target.shape[0]
+    # A step is a bounded sample of the round: `m` draft columns (top-k) and
+    # `m` target columns (argmax), one per host thread, each cut to its first
+    # n logits, with n sized so that warm-up + steps stay within ~2 minutes.
+    m = min(threads, r.cols, nt) if nt else min(threads, r.cols)
     budget = min(0.5, 120.0 / max(1, args.steps + args.warmup))
     t0 = time.perf_counter()
-    b = oracle_round(r, threads, cols=([0], [0] if r.target is not None else []), n=r.V)
+    b = oracle_round(r, threads, cols=(list(range(m)), list(range(m)) if nt else []), n=r.V)
     per_byte = (time.perf_counter() - t0) / b
-    n_elems = max(64, int(budget / per_byte / 2 / 2))            # two columns per step, 2 bytes each
-    n_elems = min(n_elems, r.V)
-    nt = 0 if r.target is None else r.target.shape[0]
+    n_elems = max(64, min(r.V, int(budget / per_byte / (2 * m * (2 if nt else 1)))))
 
     def step(i):
-        return oracle_round(r, threads, cols=([i % r.cols], [i % nt] if nt else []), n=n_elems)
+        dc = [(i * m + j) % r.cols for j in range(m)]
+        tc = [(i * m + j) % nt for j in range(m)] if nt else []
+        return oracle_round(r, threads, cols=(dc, tc), n=n_elems)
 
     for i in range(args.warmup):
         step(i)
@@ -272,15 +276,15 @@ def run_reference(args):
         nbytes += step(i)
     dt = time.perf_counter() - t0
     gbs = nbytes / dt / 1e9
-    sample = (f"each step: the oracle's top-k over the first {n_elems} logits of one draft column"
-              + (" and its argmax over the first {0} logits of one target column".format(n_elems) if nt else "")
-              + f"; {threads} threads")
+    sample = (f"each step: the oracle's top-k over the first {n_elems} logits of {m} draft columns"
+              + (f" and its argmax over the first {n_elems} logits of {m} target columns" if nt else "")
+              + f", one column per thread ({m} threads)")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(args, r, None),
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": m, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

@@ -752,8 +752,10 @@ __device__ __forceinline__ void stream_slice(const RoundArgs &a, const Run &r, i
                     bits = keep;
                 }
                 __syncwarp();
-                // tighten the threshold once enough candidates have gathered
-                if (cs.n >= kk && (cs.own == 0 || cs.n >= kk + 16)) {
+                // a first threshold as soon as kk candidates are in; after
+                // that, prune only when the buffer is three-quarters full (an
+                // append is cheap, a prune is a 16-step bisection)
+                if (cs.n >= kk && (cs.own == 0 || cs.n >= kBufCap * 3 / 4)) {
                     const Pruned pq = buf_prune(wb, cs.n, kk, lane);
                     cs.n = pq.n;
                     cs.own = pq.t;
