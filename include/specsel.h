@@ -158,6 +158,25 @@ spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t cols, int64
                                const uint16_t *target_logits, const int32_t *drafts, int64_t lanes,
                                int32_t gamma, int32_t *out_accept_len, int32_t *out_commit_ids);
 
+/* Which streaming kernel runs a round.  Both compute the same results (every
+ * output is the unique exact answer); they differ only in speed:
+ *   SPEC_KERNEL_CTA  -- the CTAs of a full-GPU grid each stream a contiguous
+ *                       slice in 60 KiB chunks; per column one threshold per
+ *                       CTA (the k-th best the CTA has seen), kept by a
+ *                       merging warp.  Fastest while each SM streams little
+ *                       (rounds of up to ~150 MB of logits).
+ *   SPEC_KERNEL_WARP -- every warp streams its own slice with its own ring,
+ *                       buffer and threshold; no coordination inside the
+ *                       stream.  Fastest for large rounds.
+ *   SPEC_KERNEL_AUTO -- (default) CTA while the round's logits are at most
+ *                       1 MiB per SM, WARP above.
+ * The choice is process-wide; SPEC_ERR_ARG for any other value. */
+#define SPEC_KERNEL_AUTO 0
+#define SPEC_KERNEL_WARP 1
+#define SPEC_KERNEL_CTA 2
+spec_status spec_set_kernel(int32_t which);
+int32_t spec_get_kernel(void);
+
 /* Set the stream (a cudaStream_t, may be NULL for the legacy default stream)
  * that the calling thread's subsequent calls enqueue on.  Thread-local. */
 spec_status spec_set_stream(void *stream);

@@ -22,12 +22,14 @@ __all__ = [
     "SPEC_MAX_GAMMA", "SpecError", "LIB_PATH", "lib",
     "spec_topk", "spec_topk_mapped", "spec_verify", "spec_verify_v", "spec_round", "spec_round_host",
     "spec_round_noalloc",
+    "spec_set_kernel", "spec_get_kernel", "SPEC_KERNEL_AUTO", "SPEC_KERNEL_WARP", "SPEC_KERNEL_CTA",
     "spec_set_stream", "spec_get_stream", "spec_reserve", "spec_release", "spec_last_error",
     "spec_launch_count", "spec_device_status", "topk", "topk_mapped", "verify", "round_step", "EXPORTS",
 ]
 
 SPEC_OK, SPEC_ERR_ARG, SPEC_ERR_ALLOC, SPEC_ERR_CUDA = 0, -1, -2, -3
 SPEC_VOCAB, SPEC_MAX_K, SPEC_MAX_GAMMA = 248_046, 64, 15
+SPEC_KERNEL_AUTO, SPEC_KERNEL_WARP, SPEC_KERNEL_CTA = 0, 1, 2
 LIB_PATH = _build.LIB
 
 if not os.path.exists(LIB_PATH):
@@ -45,6 +47,8 @@ _SIGS = {
     "spec_round": [_p, _i64, _i64, _i32, _p, _p, _p, _p, _i64, _i32, _p, _p],
     "spec_round_host": [_p, _i64, _i64, _i32, _p, _p, _p, _p, _i64, _i32, _p, _p],
     "spec_round_noalloc": [_p, _i64, _i64, _i32, _p, _p, _p, _p, _i64, _i32, _p, _p],
+    "spec_set_kernel": [_i32],
+    "spec_get_kernel": [],
     "spec_set_stream": [_p],
     "spec_get_stream": [],
     "spec_reserve": [_i64, _i32, _i64, _i32],
@@ -137,6 +141,15 @@ def spec_round_host(draft_logits, cols, V, k, out_vals, out_ids, target_logits, 
     hp = lambda a: None if a is None else (a.ctypes.data if hasattr(a, "ctypes") else a.data_ptr())
     _check(lib.spec_round_host(hp(draft_logits), cols, V, k, hp(out_vals), hp(out_ids), hp(target_logits),
                                hp(drafts), lanes, gamma, hp(out_accept_len), hp(out_commit_ids)))
+
+
+def spec_set_kernel(which: int):
+    """Choose the streaming kernel: SPEC_KERNEL_AUTO (default), _WARP or _CTA."""
+    _check(lib.spec_set_kernel(which))
+
+
+def spec_get_kernel() -> int:
+    return int(lib.spec_get_kernel())
 
 
 def spec_set_stream(stream):

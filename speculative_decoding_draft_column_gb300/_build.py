@@ -7,7 +7,8 @@ import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SRC = os.path.join(PKG, "csrc", "specsel.cu")
+CSRC = os.path.join(PKG, "csrc")
+SRC = os.path.join(CSRC, "specsel.cu")
 HDR = os.path.join(ROOT, "include", "specsel.h")
 LIB = os.path.join(PKG, "libspecsel.so")
 
@@ -27,14 +28,15 @@ def nvcc() -> str:
 
 def command(out: str = LIB, src: str = SRC, extra: tuple[str, ...] = ()) -> list[str]:
     return [nvcc(), "-O3", "-std=c++17", ARCH, "-lineinfo", "-Xcompiler", "-fPIC", "-shared",
-            "-cudart", "shared", "-I", os.path.join(ROOT, "include"), *extra, "-o", out, src]
+            "-cudart", "shared", "-I", os.path.join(ROOT, "include"), "-I", CSRC, *extra, "-o", out, src]
 
 
 def stale(out: str = LIB) -> bool:
     if not os.path.exists(out):
         return True
     t = os.path.getmtime(out)
-    return any(os.path.getmtime(p) > t for p in (SRC, HDR))
+    deps = [HDR] + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh"))]
+    return any(os.path.getmtime(p) > t for p in deps)
 
 
 def build(force: bool = False, verbose: bool = False) -> str:

@@ -1,0 +1,389 @@
+// Device pieces shared by the two streaming kernels of libspecsel: the
+// round's arguments, bf16 order keys and packed entries, bf16x2 max trees and
+// compares, masked edge loads, mbarrier / bulk-copy primitives with bounded
+// waits, candidate-buffer pruning and the flat-run slicing.
+//
+// The operations ("A drafter inside the artifact", Ignis DFlash2 page,
+// section "How it works"): top-k over each draft column (largest first, ties
+// to the smaller token id) and greedy verify (per target column the argmax,
+// then per lane the longest matching draft prefix plus the bonus token).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "specsel.h"
+
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 4000000000ull;   // bound on any mbarrier wait: 4 s of wall time
+constexpr unsigned kFull = 0xffffffffu;
+constexpr uint32_t kNaN2 = 0x7FFF7FFFu;            // two bf16 NaNs: the mask value
+
+struct RoundArgs {
+    // top-k part (draft columns)
+    const uint16_t *draft;
+    int64_t d_cols, d_V;
+    int32_t k;
+    const int32_t *id_map;
+    uint16_t *out_vals;
+    int32_t *out_ids;
+    // verify part (target columns)
+    const uint16_t *target;
+    int64_t t_cols, t_V;
+    int32_t gamma;
+    const int32_t *drafts;
+    int32_t *out_accept;
+    int32_t *out_commit;
+    // streaming units (warps or CTAs, by kernel): [0, d_units) stream the
+    // draft logits, [d_units, d_units + t_units) the target logits
+    int32_t d_units, t_units;
+    // scratch
+    unsigned long long *partials;   // [(d_units + t_units) * 2][pstride]: published lists
+    unsigned int *col_ticket;       // [d_cols + t_cols]
+    unsigned int *col_cert;         // [d_cols + t_cols]: best certified key published for a split column
+    unsigned int *lane_ticket;      // [lanes]
+    int32_t *t_argmax;              // [t_cols]
+    int32_t pstride;
+};
+
+// Set (bit 0) when a bounded wait gave up; read and cleared by spec_device_status.
+__device__ unsigned int g_wait_timeouts;
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// true if either bf16 half of a is > (or >=) the bf16 in both halves of t2;
+// NaN halves compare false.
+__device__ __forceinline__ bool any_gt(uint32_t a, uint32_t t2)
+{
+    uint32_t r;
+    asm("{\n\t.reg .pred p, q;\n\t"
+        "setp.gt.bf16x2 p|q, %1, %2;\n\t"
+        "or.pred p, p, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(a), "r"(t2));
+    return r != 0;
+}
+
+__device__ __forceinline__ bool any_ge(uint32_t a, uint32_t t2)
+{
+    uint32_t r;
+    asm("{\n\t.reg .pred p, q;\n\t"
+        "setp.ge.bf16x2 p|q, %1, %2;\n\t"
+        "or.pred p, p, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(a), "r"(t2));
+    return r != 0;
+}
+
+__device__ __forceinline__ float bf16_as_float(uint32_t raw16) { return __uint_as_float(raw16 << 16); }
+
+// element e (0..7) of a 16-byte vector, widened exactly to float
+__device__ __forceinline__ float elem8(const uint4 &q, int e)
+{
+    const uint32_t w = (e & 4) ? ((e & 2) ? q.w : q.z) : ((e & 2) ? q.y : q.x);
+    return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
+
+// order-preserving 16-bit key of a bf16: -0 and +0 share a key; -Inf -> 0x80;
+// NaN (the mask value) -> 0, below every real key.
+__device__ __forceinline__ uint32_t order_key(uint32_t raw16)
+{
+    const uint32_t m = raw16 & 0x7FFFu;
+    if (m > 0x7F80u) return 0u;
+    return (raw16 & 0x8000u) ? (0x8000u - m) : (0x8000u + m);
+}
+
+__device__ __forceinline__ uint32_t key_to_raw(uint32_t key)
+{
+    const int s = (int)key - 0x8000;
+    return s >= 0 ? (uint32_t)s : (0x8000u | (uint32_t)(-s));
+}
+
+// larger packed value = better entry: (key desc, id asc); low 16 bits keep the
+// element's own bit pattern (so -0 survives); 0 = empty slot.
+__device__ __forceinline__ unsigned long long pack_entry(float v, uint32_t id)
+{
+    if (v != v) return 0ull;
+    const uint32_t raw = __float_as_uint(v) >> 16;
+    return ((unsigned long long)order_key(raw) << 48) | ((unsigned long long)(~id) << 16) | raw;
+}
+
+__device__ __forceinline__ uint32_t entry_key(unsigned long long e) { return (uint32_t)(e >> 48); }
+__device__ __forceinline__ uint32_t entry_id(unsigned long long e) { return ~(uint32_t)(e >> 16); }
+__device__ __forceinline__ uint16_t entry_raw(unsigned long long e) { return (uint16_t)(e & 0xFFFFu); }
+
+// bf16x2 max over one 16-byte vector
+__device__ __forceinline__ uint32_t vmax(const uint4 &q) { return bmax2(bmax2(q.x, q.y), bmax2(q.z, q.w)); }
+
+// both halves hold max(lo, hi)
+__device__ __forceinline__ uint32_t hmax_splat(uint32_t m2) { return bmax2(m2, __byte_perm(m2, 0, 0x1032)); }
+
+// Masked load of an edge vector: element by element, only inside [g0, g1).
+__device__ __forceinline__ uint4 load_edge(const uint16_t *buf, int64_t j, int mis, int64_t g0, int64_t g1)
+{
+    uint32_t w[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        uint32_t lo = 0x7FFFu, hi = 0x7FFFu;
+        const int64_t ga = 8 * j + 2 * h - mis, gb = ga + 1;
+        if (ga >= g0 && ga < g1) lo = __ldg(buf + ga);
+        if (gb >= g0 && gb < g1) hi = __ldg(buf + gb);
+        w[h] = lo | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt()
+{
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Exclusive prefix sum of v over the warp; also returns the warp total.
+__device__ __forceinline__ int warp_exclusive_sum(int v, int lane, int &total)
+{
+    int incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, d);
+        if (lane >= d) incl += y;
+    }
+    total = __shfl_sync(kFull, incl, 31);
+    return incl - v;
+}
+
+// A 32-bit word other SMs update with atomics, read through L2.
+__device__ __forceinline__ uint32_t ld_relaxed(const unsigned int *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// ---- mbarrier / bulk-copy primitives (inline PTX, sm_90+) -------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// Test the phase; a thread whose phase is not complete may sleep in the
+// instruction until it completes (at most the hinted 20 us), instead of
+// spinning on the issue slots.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity), "n"(20000)
+                 : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Set by a thread of the CTA whose wait gave up: the CTA's other waits then
+// give up at once, so a launch ends within one time limit.
+__shared__ unsigned int s_gave_up;
+
+// Wait for the phase with the given parity to complete, for at most
+// kWaitLimitNs of wall time; on giving up, flag the error and report false
+// (the data is then garbage, but the kernel still terminates).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*reinterpret_cast<volatile unsigned int *>(&s_gave_up)) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            s_gave_up = 1u;
+            atomicOr(&g_wait_timeouts, 1u);
+            return false;
+        }
+    }
+}
+
+// One bulk copy global -> shared, completing on `bar` with its byte count.
+// src, dst 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// ---- candidate buffers ------------------------------------------------------
+
+struct Pruned {
+    int n;       // entries kept (kk)
+    uint32_t t;  // their certificate: the kk-th largest key
+};
+
+// Prune the buffer wb[0..n) (kk <= n <= 32 * Q, any order) to its kk best
+// entries; returns kk and the kk-th largest key t (kk entries reach it: a
+// certificate).  Ties at t go to the smallest ids (token ids, or mapped
+// vocabulary ids for a shortlist), found by a bisection over the id bits only
+// when there are more ties than places.
+template <int Q>
+__device__ __noinline__ Pruned buf_prune(unsigned long long *wb, int n, int kk, int lane)
+{
+    unsigned long long e[Q];
+    uint32_t key[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        const int idx = q * 32 + lane;
+        e[q] = idx < n ? wb[idx] : 0ull;
+        key[q] = entry_key(e[q]);
+    }
+    uint32_t t = 0;   // kk-th largest key: bisection over the 16 key bits
+#pragma unroll 1
+    for (int bit = 15; bit >= 0; --bit) {
+        const uint32_t tr = t | (1u << bit);
+        int cnt = 0;
+#pragma unroll
+        for (int q = 0; q < Q; ++q) cnt += __popc(__ballot_sync(kFull, key[q] >= tr));
+        if (cnt >= kk) t = tr;
+    }
+    int cgt = 0, ceq = 0;
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        cgt += __popc(__ballot_sync(kFull, key[q] > t));
+        ceq += __popc(__ballot_sync(kFull, key[q] == t && e[q] != 0ull));
+    }
+    const int quota = kk - cgt;   // entries with key == t that survive
+    uint32_t tid[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) tid[q] = (key[q] == t && e[q] != 0ull) ? entry_id(e[q]) : 0xFFFFFFFFu;
+    uint32_t m = 0x7FFFFFFFu;     // ties kept: id <= m (ids < 2^31)
+    if (ceq > quota) {
+        m = 0;   // the quota-th smallest id among the ties
+#pragma unroll 1
+        for (int bit = 30; bit >= 0; --bit) {
+            const uint32_t tr = m | (1u << bit);
+            int cnt = 0;
+#pragma unroll
+            for (int q = 0; q < Q; ++q) cnt += __popc(__ballot_sync(kFull, tid[q] < tr));
+            if (cnt < quota) m = tr;
+        }
+    }
+    __syncwarp();
+    int out = 0;
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        const bool keep = key[q] > t || (tid[q] != 0xFFFFFFFFu && tid[q] <= m);
+        const uint32_t bal = __ballot_sync(kFull, keep);
+        if (keep) wb[out + __popc(bal & lanemask_lt())] = e[q];
+        out += __popc(bal);
+    }
+    __syncwarp();
+    return Pruned{out, t};
+}
+
+// Filter: candidates must be > thr (strict) or >= thr.
+struct Filter {
+    float thr;
+    uint32_t thr2;   // thr as a bf16 pair
+    bool strict;
+};
+
+// own_key: the warp's certified key for the column (0: none), strict unless
+// mapped; cert_key: another certificate for the column (inclusive).
+__device__ __forceinline__ Filter make_filter(uint32_t own_key, uint32_t cert_key, bool mapped)
+{
+    Filter f;
+    uint32_t key;
+    if (own_key != 0 && own_key >= cert_key) {
+        key = own_key;
+        f.strict = !mapped;
+    } else {
+        key = cert_key;
+        f.strict = false;
+    }
+    const uint32_t raw = key ? key_to_raw(key) : 0xFF80u;   // no certificate: >= -Inf
+    f.thr = bf16_as_float(raw);
+    f.thr2 = raw | (raw << 16);
+    return f;
+}
+
+__device__ __forceinline__ uint32_t elem_mask(const uint4 &q, const Filter &f)
+{
+    uint32_t cm = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float v = elem8(q, e);
+        cm |= (uint32_t)(f.strict ? (v > f.thr) : (v >= f.thr)) << e;
+    }
+    return cm;
+}
+
+// One buffer (draft or target logits) seen as a flat run of N = cols * V
+// elements on the 16-byte vector grid: vector j holds elements
+// [8j - mis, 8j - mis + 8).  The run is cut into W slices of whole vectors,
+// one per streaming unit (a warp or a CTA); slice b = vectors
+// [start(b), start(b+1)), start(b) = floor(b * NV / W).
+struct Run {
+    const uint16_t *buf;
+    const uint4 *vb;          // 16-byte aligned base, at or just below buf
+    int64_t V, N, NV;
+    int64_t jlo, jhi;         // vectors [jlo, jhi) lie wholly inside the buffer
+    int W, gw0;               // units on this run; global index of its slice 0
+    int kk;
+    int mis;
+    bool draft;
+};
+
+__device__ __forceinline__ int64_t slice_start(const Run &r, int64_t w) { return w * r.NV / r.W; }
+__device__ __forceinline__ int64_t owner(const Run &r, int64_t j) { return ((j + 1) * r.W - 1) / r.NV; }
+__device__ __forceinline__ int64_t first_elem(const Run &r, int64_t w)
+{
+    const int64_t g = 8 * slice_start(r, w) - r.mis;
+    return g > 0 ? g : 0;
+}
+
+// The list slot of slice w for column c: 0 if c is the first column of the
+// slice, else 1 (a slice holds part of at most two columns that it shares).
+__device__ __forceinline__ unsigned long long *list_slot(const RoundArgs &a, const Run &r, int64_t w, int64_t c)
+{
+    const int sl = (c == first_elem(r, w) / r.V) ? 0 : 1;
+    return a.partials + ((int64_t)(r.gw0 + w) * 2 + sl) * a.pstride;
+}
+
+}  // namespace

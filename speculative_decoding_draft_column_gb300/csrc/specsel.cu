@@ -1,5 +1,6 @@
 // libspecsel: exact per-column top-k and fused greedy verify over bf16 logits
-// for one GB300 (sm_103a).
+// for one GB300 (sm_103a) -- host side: argument checks, kernel plans,
+// scratch, streams and the C ABI.
 //
 // The operations ("A drafter inside the artifact", Ignis DFlash2 page,
 // section "How it works"):
@@ -9,40 +10,10 @@
 //     lane the longest run of drafts equal to those argmaxes, committed
 //     together with the target's own next token (first paragraph).
 //
-// Design (one streaming pass over the logits, no tensor cores -- the step is
-// a pure reduction bound by HBM bandwidth):
-//   * Every warp of a full-GPU grid (16 warps per CTA, one CTA per SM) owns a
-//     contiguous slice of the flat run of logits (draft columns one after the
-//     other, then target columns), the same number of 16-byte vectors for
-//     every warp.  A slice may start or end inside a column.  The warps never
-//     wait on one another in the streaming loop.
-//   * Each warp streams its slice through its own ring of three 4 KiB stages
-//     in shared memory, filled by one-dimensional bulk copies
-//     (cp.async.bulk, completion on an mbarrier); lane 0 refills a stage as
-//     soon as the warp is done with it, so 12 KiB per warp (192 KiB per SM)
-//     stay in flight.
-//   * Per column segment the warp keeps a candidate buffer in shared memory:
-//     packed (value key, id, bits) entries appended in increasing id order.
-//     A stage is skipped after one bf16x2 max tree per lane and one compare
-//     against the column's threshold.  The threshold is a certificate: a key
-//     that kk elements already reach.  It is seeded from the first stage
-//     (the kk-th largest of the lane maxima) and tightened by pruning the
-//     buffer to its kk best (a bisection over the 16 key bits); since the warp
-//     meets elements in id order, a later element equal to the threshold is
-//     worse than every kept entry and is rejected (strict filter).
-//   * A column seen whole by one warp is emitted by it.  Otherwise every warp
-//     that saw part of it publishes its kk best (and their certificate) to
-//     scratch and takes the column's ticket; the warp that completes the
-//     column merges the lists in slice order -- the logits are read once.
-//   * Verify columns are the k = 1 instance; the warp that completes the last
-//     of a lane's gamma+1 columns runs the prefix match (one lane per
-//     position).  Tickets are reset by their last user, so launches replay.
-//   * Masked elements (past a column or the buffer) are bf16 NaN: bf16 max
-//     ignores them, ordered compares reject them.  The buffer's ragged first
-//     and last 16-byte vectors are read element by element, so no load or
-//     copy touches memory outside the caller's buffer.
-//   * Every mbarrier wait is bounded in time; a wait that gives up sets a flag
-//     (spec_device_status) and the kernel still ends.
+// One kernel launch does a whole round (one streaming pass over the draft and
+// target logits; no tensor cores -- the step is a pure reduction bound by HBM
+// bandwidth).  Two streaming kernels implement it (round_cta.cuh,
+// round_warp.cuh); the host picks by how much each SM streams.
 
 #include <cuda_runtime.h>
 #include <stdarg.h>
@@ -55,762 +26,11 @@
 #include <string>
 
 #include "specsel.h"
+#include "common.cuh"
+#include "round_cta.cuh"
+#include "round_warp.cuh"
 
 namespace {
-
-constexpr int kWarpsPerCta = 16;
-constexpr int kThreads = kWarpsPerCta * 32;
-constexpr int kStageVec = 256;                     // 16-byte vectors per warp stage (4 KiB)
-constexpr int kLaneVec = kStageVec / 32;           // vectors per lane per stage
-constexpr int kStages = 3;                         // per-warp ring depth (12 KiB in flight per warp)
-constexpr int kBufCap = 128;                       // per-warp candidate buffer (entries)
-constexpr int kMinSliceVec = 2 * kStageVec;        // smallest slice a warp is given
-constexpr uint64_t kWaitLimitNs = 4000000000ull;   // bound on any mbarrier wait: 4 s of wall time
-constexpr unsigned kFull = 0xffffffffu;
-constexpr uint32_t kNaN2 = 0x7FFF7FFFu;            // two bf16 NaNs: the mask value
-
-static_assert(kBufCap >= 2 * SPEC_MAX_K && kBufCap % 32 == 0, "a pruned buffer must leave room");
-
-struct RoundArgs {
-    // top-k part (draft columns)
-    const uint16_t *draft;
-    int64_t d_cols, d_V;
-    int32_t k;
-    const int32_t *id_map;
-    uint16_t *out_vals;
-    int32_t *out_ids;
-    // verify part (target columns)
-    const uint16_t *target;
-    int64_t t_cols, t_V;
-    int32_t gamma;
-    const int32_t *drafts;
-    int32_t *out_accept;
-    int32_t *out_commit;
-    // warps [0, d_warps) stream the draft logits, [d_warps, d_warps + t_warps) the target logits
-    int32_t d_warps, t_warps;
-    // scratch
-    unsigned long long *partials;   // [(d_warps + t_warps) * 2][pstride = k + 2]
-    unsigned int *col_ticket;       // [d_cols + t_cols]
-    unsigned int *col_cert;         // [d_cols + t_cols]: best certified key published for a split column
-    unsigned int *lane_ticket;      // [lanes]
-    int32_t *t_argmax;              // [t_cols]
-    int32_t pstride;
-};
-
-// Set (bit 0) when a bounded wait gave up; read and cleared by spec_device_status.
-__device__ unsigned int g_wait_timeouts;
-
-// ---------------------------------------------------------------------------
-// device helpers
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b)
-{
-    uint32_t d;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-// true if either bf16 half of a is > (or >=) the bf16 in both halves of t2;
-// NaN halves compare false.
-__device__ __forceinline__ bool any_gt(uint32_t a, uint32_t t2)
-{
-    uint32_t r;
-    asm("{\n\t.reg .pred p, q;\n\t"
-        "setp.gt.bf16x2 p|q, %1, %2;\n\t"
-        "or.pred p, p, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(a), "r"(t2));
-    return r != 0;
-}
-
-__device__ __forceinline__ bool any_ge(uint32_t a, uint32_t t2)
-{
-    uint32_t r;
-    asm("{\n\t.reg .pred p, q;\n\t"
-        "setp.ge.bf16x2 p|q, %1, %2;\n\t"
-        "or.pred p, p, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(a), "r"(t2));
-    return r != 0;
-}
-
-__device__ __forceinline__ float bf16_as_float(uint32_t raw16) { return __uint_as_float(raw16 << 16); }
-
-// element e (0..7) of a 16-byte vector, widened exactly to float
-__device__ __forceinline__ float elem8(const uint4 &q, int e)
-{
-    const uint32_t w = (e & 4) ? ((e & 2) ? q.w : q.z) : ((e & 2) ? q.y : q.x);
-    return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
-}
-
-// order-preserving 16-bit key of a bf16: -0 and +0 share a key; -Inf -> 0x80;
-// NaN (the mask value) -> 0, below every real key.
-__device__ __forceinline__ uint32_t order_key(uint32_t raw16)
-{
-    const uint32_t m = raw16 & 0x7FFFu;
-    if (m > 0x7F80u) return 0u;
-    return (raw16 & 0x8000u) ? (0x8000u - m) : (0x8000u + m);
-}
-
-__device__ __forceinline__ uint32_t key_to_raw(uint32_t key)
-{
-    const int s = (int)key - 0x8000;
-    return s >= 0 ? (uint32_t)s : (0x8000u | (uint32_t)(-s));
-}
-
-// larger packed value = better entry: (key desc, id asc); low 16 bits keep the
-// element's own bit pattern (so -0 survives); 0 = empty slot.
-__device__ __forceinline__ unsigned long long pack_entry(float v, uint32_t id)
-{
-    if (v != v) return 0ull;
-    const uint32_t raw = __float_as_uint(v) >> 16;
-    return ((unsigned long long)order_key(raw) << 48) | ((unsigned long long)(~id) << 16) | raw;
-}
-
-__device__ __forceinline__ uint32_t entry_key(unsigned long long e) { return (uint32_t)(e >> 48); }
-__device__ __forceinline__ uint32_t entry_id(unsigned long long e) { return ~(uint32_t)(e >> 16); }
-__device__ __forceinline__ uint16_t entry_raw(unsigned long long e) { return (uint16_t)(e & 0xFFFFu); }
-
-// bf16x2 max over one 16-byte vector
-__device__ __forceinline__ uint32_t vmax(const uint4 &q) { return bmax2(bmax2(q.x, q.y), bmax2(q.z, q.w)); }
-
-// both halves hold max(lo, hi)
-__device__ __forceinline__ uint32_t hmax_splat(uint32_t m2) { return bmax2(m2, __byte_perm(m2, 0, 0x1032)); }
-
-// Masked load of an edge vector: element by element, only inside [g0, g1).
-__device__ __forceinline__ uint4 load_edge(const uint16_t *buf, int64_t j, int mis, int64_t g0, int64_t g1)
-{
-    uint32_t w[4];
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-        uint32_t lo = 0x7FFFu, hi = 0x7FFFu;
-        const int64_t ga = 8 * j + 2 * h - mis, gb = ga + 1;
-        if (ga >= g0 && ga < g1) lo = __ldg(buf + ga);
-        if (gb >= g0 && gb < g1) hi = __ldg(buf + gb);
-        w[h] = lo | (hi << 16);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-__device__ __forceinline__ uint32_t lanemask_lt()
-{
-    uint32_t m;
-    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
-}
-
-// Exclusive prefix sum of v over the warp; also returns the warp total.
-__device__ __forceinline__ int warp_exclusive_sum(int v, int lane, int &total)
-{
-    int incl = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int y = __shfl_up_sync(kFull, incl, d);
-        if (lane >= d) incl += y;
-    }
-    total = __shfl_sync(kFull, incl, 31);
-    return incl - v;
-}
-
-// A 32-bit word other SMs update with atomics, read through L2.
-__device__ __forceinline__ uint32_t ld_relaxed(const unsigned int *p)
-{
-    uint32_t v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// ---- mbarrier / bulk-copy primitives (inline PTX, sm_90+) -------------------
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok)
-                 : "r"(smem_u32(bar)), "r"(parity)
-                 : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait for the phase with the given parity to complete, for at most
-// kWaitLimitNs of wall time; on giving up, flag the error and report false
-// (the data is then garbage, but the kernel still terminates).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (;;) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) {
-            atomicOr(&g_wait_timeouts, 1u);
-            return false;
-        }
-    }
-}
-
-// One bulk copy global -> shared, completing on `bar` with its byte count.
-// src, dst 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
-
-// ---- candidate buffers ------------------------------------------------------
-
-struct Pruned {
-    int n;       // entries kept (kk)
-    uint32_t t;  // their certificate: the kk-th largest key
-};
-
-// Prune the warp buffer wb[0..n) (n >= kk, any order) to its kk best
-// entries; returns kk and the kk-th largest key t (kk entries reach it: a
-// certificate).  Ties at t go to the smallest ids (token ids, or mapped
-// vocabulary ids for a shortlist), found by a bisection over the id bits only
-// when there are more ties than places.
-__device__ __noinline__ Pruned buf_prune(unsigned long long *wb, int n, int kk, int lane)
-{
-    constexpr int Q = kBufCap / 32;
-    unsigned long long e[Q];
-    uint32_t key[Q];
-#pragma unroll
-    for (int q = 0; q < Q; ++q) {
-        const int idx = q * 32 + lane;
-        e[q] = idx < n ? wb[idx] : 0ull;
-        key[q] = entry_key(e[q]);
-    }
-    uint32_t t = 0;   // kk-th largest key: bisection over the 16 key bits
-#pragma unroll 1
-    for (int bit = 15; bit >= 0; --bit) {
-        const uint32_t tr = t | (1u << bit);
-        int cnt = 0;
-#pragma unroll
-        for (int q = 0; q < Q; ++q) cnt += __popc(__ballot_sync(kFull, key[q] >= tr));
-        if (cnt >= kk) t = tr;
-    }
-    int cgt = 0, ceq = 0;
-#pragma unroll
-    for (int q = 0; q < Q; ++q) {
-        cgt += __popc(__ballot_sync(kFull, key[q] > t));
-        ceq += __popc(__ballot_sync(kFull, key[q] == t && e[q] != 0ull));
-    }
-    const int quota = kk - cgt;   // entries with key == t that survive
-    uint32_t tid[Q];
-#pragma unroll
-    for (int q = 0; q < Q; ++q) tid[q] = (key[q] == t && e[q] != 0ull) ? entry_id(e[q]) : 0xFFFFFFFFu;
-    uint32_t m = 0x7FFFFFFFu;     // ties kept: id <= m (ids < 2^31)
-    if (ceq > quota) {
-        m = 0;   // the quota-th smallest id among the ties
-#pragma unroll 1
-        for (int bit = 30; bit >= 0; --bit) {
-            const uint32_t tr = m | (1u << bit);
-            int cnt = 0;
-#pragma unroll
-            for (int q = 0; q < Q; ++q) cnt += __popc(__ballot_sync(kFull, tid[q] < tr));
-            if (cnt < quota) m = tr;
-        }
-    }
-    __syncwarp();
-    int out = 0;
-#pragma unroll
-    for (int q = 0; q < Q; ++q) {
-        const bool keep = key[q] > t || (tid[q] != 0xFFFFFFFFu && tid[q] <= m);
-        const uint32_t bal = __ballot_sync(kFull, keep);
-        if (keep) wb[out + __popc(bal & lanemask_lt())] = e[q];
-        out += __popc(bal);
-    }
-    __syncwarp();
-    return Pruned{out, t};
-}
-
-// Filter: candidates must be > thr (strict) or >= thr.
-struct Filter {
-    float thr;
-    uint32_t thr2;   // thr as a bf16 pair
-    bool strict;
-};
-
-// own_key: the warp's certified key for the column (0: none), strict unless
-// mapped; cert_key: another certificate for the column (inclusive).
-__device__ __forceinline__ Filter make_filter(uint32_t own_key, uint32_t cert_key, bool mapped)
-{
-    Filter f;
-    uint32_t key;
-    if (own_key != 0 && own_key >= cert_key) {
-        key = own_key;
-        f.strict = !mapped;
-    } else {
-        key = cert_key;
-        f.strict = false;
-    }
-    const uint32_t raw = key ? key_to_raw(key) : 0xFF80u;   // no certificate: >= -Inf
-    f.thr = bf16_as_float(raw);
-    f.thr2 = raw | (raw << 16);
-    return f;
-}
-
-__device__ __forceinline__ uint32_t elem_mask(const uint4 &q, const Filter &f)
-{
-    uint32_t cm = 0;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const float v = elem8(q, e);
-        cm |= (uint32_t)(f.strict ? (v > f.thr) : (v >= f.thr)) << e;
-    }
-    return cm;
-}
-
-struct ColState {
-    int n;          // entries in the buffer
-    uint32_t own;   // own certified key (last prune)
-    uint32_t cert;  // certificate from elsewhere (seed or merge), inclusive
-    bool open;      // the warp has started this column
-    int seen;       // elements of the column this warp has scanned (saturating)
-};
-
-// ---- the per-warp stream ------------------------------------------------------
-
-// Shared memory of one warp: its copy ring, candidate buffer and barriers.
-struct WarpSmem {
-    uint4 ring[kStages][kStageVec];
-    unsigned long long buf[kBufCap];
-    uint64_t full[kStages];
-};
-
-constexpr size_t kSmemBytes = (size_t)kWarpsPerCta * sizeof(WarpSmem);
-
-// One buffer (draft or target logits) seen as a flat run of N = cols * V
-// elements on the 16-byte vector grid: vector j holds elements
-// [8j - mis, 8j - mis + 8).  The run is cut into W slices of whole vectors;
-// slice w = vectors [start(w), start(w+1)), start(w) = floor(w * NV / W).
-struct Run {
-    const uint16_t *buf;
-    const uint4 *vb;          // 16-byte aligned base, at or just below buf
-    int64_t V, N, NV;
-    int64_t jlo, jhi;         // vectors [jlo, jhi) lie wholly inside the buffer
-    int W, gw0;               // warps on this run; global index of its slice 0
-    int kk;
-    int mis;
-    bool draft;
-};
-
-__device__ __forceinline__ int64_t slice_start(const Run &r, int64_t w) { return w * r.NV / r.W; }
-__device__ __forceinline__ int64_t owner(const Run &r, int64_t j) { return ((j + 1) * r.W - 1) / r.NV; }
-__device__ __forceinline__ int64_t first_elem(const Run &r, int64_t w)
-{
-    const int64_t g = 8 * slice_start(r, w) - r.mis;
-    return g > 0 ? g : 0;
-}
-
-// The list slot of warp w for column c: 0 if c is the first column of the
-// slice, else 1 (a slice holds part of at most two columns).
-__device__ __forceinline__ unsigned long long *list_slot(const RoundArgs &a, const Run &r, int64_t w, int64_t c)
-{
-    const int sl = (c == first_elem(r, w) / r.V) ? 0 : 1;
-    return a.partials + ((int64_t)(r.gw0 + w) * 2 + sl) * a.pstride;
-}
-
-// Write a finished column: its best entries (in the buffer, id order) are
-// ranked by value; top-k outputs, or for a target column the argmax and, for
-// the lane's last column, the prefix match (one lane per position).
-__device__ __noinline__ void emit_column(const RoundArgs &a, const Run &r, int64_t c,
-                                         const unsigned long long *wb, int n, int lane)
-{
-    const int kk = r.kk;
-    for (int i = lane; i < n; i += 32) {
-        const unsigned long long e = wb[i];
-        int rank = 0;
-        for (int j = 0; j < n; ++j) rank += wb[j] > e;
-        if (r.draft) {
-            a.out_vals[c * kk + rank] = entry_raw(e);
-            a.out_ids[c * kk + rank] = (int32_t)entry_id(e);
-        } else if (rank == 0) {
-            a.t_argmax[c] = (int32_t)entry_id(e);
-        }
-    }
-    if (r.draft) return;
-    const int gp1 = a.gamma + 1;
-    const int64_t ln = c / gp1;
-    __threadfence();
-    __syncwarp();
-    unsigned last = 0;
-    if (lane == 0) last = atomicAdd(a.lane_ticket + ln, 1u) == (unsigned)a.gamma;
-    if (!__shfl_sync(kFull, last, 0)) return;
-    __threadfence();
-    const int32_t tj = lane < gp1 ? __ldcg(a.t_argmax + ln * gp1 + lane) : 0;
-    const int32_t dj = lane < a.gamma ? __ldg(a.drafts + ln * a.gamma + lane) : 0;
-    const uint32_t miss = __ballot_sync(kFull, lane < a.gamma && dj != tj);
-    const int acc = miss ? __ffs(miss) - 1 : a.gamma;
-    if (lane < gp1) a.out_commit[ln * gp1 + lane] = lane <= acc ? tj : -1;
-    if (lane == 0) {
-        a.out_accept[ln] = acc;
-        a.lane_ticket[ln] = 0u;   // ready for the next launch
-    }
-}
-
-// Column c's segment in this warp is over.  If the warp saw the whole column,
-// emit it; otherwise publish the warp's list and take the column's ticket;
-// the warp that completes the column merges every warp's list (in slice
-// order, hence in id order) and emits it.
-template <bool MAPPED>
-__device__ __noinline__ void finish_column(const RoundArgs &a, const Run &r, int w, int64_t c,
-                                           unsigned long long *wb, int n_in, uint32_t own_in, int lane)
-{
-    ColState cs = {n_in, own_in, 0u, true, 0};
-    const int kk = r.kk;
-    if (cs.n > kk) { const Pruned pq = buf_prune(wb, cs.n, kk, lane); cs.n = pq.n; cs.own = pq.t; }
-    const int64_t wf = owner(r, (c * r.V + r.mis) >> 3);
-    const int64_t wl = owner(r, ((c + 1) * r.V - 1 + r.mis) >> 3);
-    if (wf == wl) {
-        emit_column(a, r, c, wb, cs.n, lane);
-        return;
-    }
-    // publish: the list (kk entries, id order, 0-padded), in slot kk its
-    // certificate -- the smallest key of a full list (kk entries reach it) --
-    // and in slot kk + 1 its length
-    uint32_t mk = 0xFFFFFFFFu;
-    for (int i = lane; i < cs.n; i += 32) {
-        const uint32_t ky = entry_key(wb[i]);
-        mk = ky < mk ? ky : mk;
-    }
-    mk = __reduce_min_sync(kFull, mk);
-    unsigned long long *mine = list_slot(a, r, w, c);
-    for (int i = lane; i < cs.n; i += 32) mine[i] = wb[i];
-    if (lane == 0) {
-        mine[kk] = cs.n == kk ? mk : 0u;
-        mine[kk + 1] = (unsigned long long)cs.n;
-    }
-    __threadfence();
-    __syncwarp();
-    const int64_t tix = r.draft ? c : a.d_cols + c;
-    unsigned last = 0;
-    if (lane == 0) last = atomicAdd(a.col_ticket + tix, 1u) == (unsigned)(wl - wf);
-    if (!__shfl_sync(kFull, last, 0)) return;
-    __threadfence();
-    // merge.  The best certificate (the column's shared one, or any full
-    // list's) bounds the column's kk-th key; only entries at or above it are
-    // gathered, list by list in slice order (hence id order), each lane
-    // loading one list, all lists in flight at once.
-    cs.n = 0;
-    cs.own = 0;
-    cs.cert = ld_relaxed(a.col_cert + tix);
-    const int64_t nparts = wl - wf + 1;
-    for (int64_t q0 = 0; q0 < nparts; q0 += 32) {
-        uint32_t key = 0;
-        if (q0 + lane < nparts) key = (uint32_t)__ldcg(list_slot(a, r, wf + q0 + lane, c) + kk);
-        key = __reduce_max_sync(kFull, key);
-        cs.cert = key > cs.cert ? key : cs.cert;
-    }
-    for (int64_t q0 = 0; q0 < nparts; q0 += 32) {
-        const bool mine_l = q0 + lane < nparts;
-        const unsigned long long *lst = mine_l ? list_slot(a, r, wf + q0 + lane, c) : nullptr;
-        const int len = mine_l ? (int)__ldcg(lst + kk + 1) : 0;
-        const int maxlen = __reduce_max_sync(kFull, len);
-        for (int i0 = 0; i0 < maxlen; i0 += 8) {
-            unsigned long long e8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) e8[i] = i0 + i < len ? __ldcg(lst + i0 + i) : 0ull;
-            uint32_t ok = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ok |= (uint32_t)(e8[i] != 0ull && entry_key(e8[i]) >= cs.cert) << i;
-            for (;;) {
-                int total;
-                const int excl = warp_exclusive_sum(__popc(ok), lane, total);
-                if (total == 0) break;
-                const int space = kBufCap - cs.n;
-                int pos = excl;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if ((ok >> i) & 1u) {
-                        if (pos < space) {
-                            wb[cs.n + pos] = e8[i];
-                            ok &= ~(1u << i);
-                        }
-                        ++pos;
-                    }
-                __syncwarp();
-                if (total <= space) {
-                    cs.n += total;
-                    break;
-                }
-                const Pruned pq = buf_prune(wb, kBufCap, kk, lane);
-                cs.n = pq.n;
-                cs.own = pq.t;
-                if (cs.own > cs.cert) cs.cert = cs.own;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (entry_key(e8[i]) < cs.cert) ok &= ~(1u << i);
-            }
-        }
-    }
-    if (cs.n > kk) { const Pruned pq = buf_prune(wb, cs.n, kk, lane); cs.n = pq.n; cs.own = pq.t; }
-    emit_column(a, r, c, wb, cs.n, lane);
-    if (lane == 0) {
-        a.col_ticket[tix] = 0u;   // ready for the next launch
-        a.col_cert[tix] = 0u;
-    }
-}
-
-// Issue the bulk copy of stage i of slice [J0, J1) into ring slot i % kStages.
-// Only vectors wholly inside the buffer are copied; the (at most two) edge
-// vectors of the buffer are read element by element by the consumer.
-__device__ __forceinline__ void issue_stage(const Run &r, WarpSmem &ws, int64_t J0, int64_t J1, int64_t i)
-{
-    const int st = (int)(i % kStages);
-    const int64_t vs = J0 + i * kStageVec;
-    const int64_t ve = vs + kStageVec < J1 ? vs + kStageVec : J1;
-    const int64_t is = vs > r.jlo ? vs : r.jlo;
-    const int64_t ie = ve < r.jhi ? ve : r.jhi;
-    const uint32_t bytes = ie > is ? (uint32_t)((ie - is) * 16) : 0u;
-    fence_proxy_async();
-    mbar_arrive_expect_tx(&ws.full[st], bytes);
-    if (bytes) bulk_g2s(&ws.ring[st][is - vs], r.vb + is, bytes, &ws.full[st]);
-}
-
-// One warp streams its slice w of run r: every column segment gets a
-// candidate buffer and a threshold; finished columns are emitted or merged.
-template <int SLOTS, bool MAPPED>
-__device__ __forceinline__ void stream_slice(const RoundArgs &a, const Run &r, int w,
-                                             const int32_t *__restrict__ id_map, WarpSmem &ws, int lane)
-{
-    const int64_t J0 = slice_start(r, w), J1 = slice_start(r, w + 1);
-    if (J1 <= J0) return;
-    const int64_t nst = (J1 - J0 + kStageVec - 1) / kStageVec;
-    const int kk = r.kk;
-    unsigned long long *wb = ws.buf;
-    if (lane == 0)
-        for (int64_t i = 0; i < nst && i < kStages; ++i) issue_stage(r, ws, J0, J1, i);
-
-    int64_t c = first_elem(r, w) / r.V;       // current column
-    ColState cs = {0, 0u, 0u, false, 0};
-    // a column split across warps has a shared certificate in global memory:
-    // every warp raises it with its own certified keys and filters against
-    // it (read one stage late, so the load latency hides behind the stream)
-    bool shared = false;
-    int64_t tix = 0;
-    uint32_t gcert = 0;
-
-    for (int64_t i = 0; i < nst; ++i) {
-        const int st = (int)(i % kStages);
-        mbar_wait(&ws.full[st], (uint32_t)(i / kStages) & 1u);
-        const int64_t vs = J0 + i * kStageVec;
-        const int64_t ve = vs + kStageVec < J1 ? vs + kStageVec : J1;
-        const int64_t g_first = 8 * vs - r.mis > 0 ? 8 * vs - r.mis : 0;
-        const int64_t g_end = 8 * ve - r.mis < r.N ? 8 * ve - r.mis : r.N;   // exclusive
-        for (;;) {
-            // the part of column c inside this stage, elements outside as NaN
-            const int64_t cb = c * r.V, ce = cb + r.V;
-            const bool whole = cb <= g_first && ce >= g_end;
-            uint4 y[kLaneVec];
-            if (whole && ve - vs == kStageVec && vs >= r.jlo && ve <= r.jhi) {
-                // the common case: a full stage, inside one column, no buffer edge
-                const uint4 *src = &ws.ring[st][lane];
-#pragma unroll
-                for (int u = 0; u < kLaneVec; ++u) y[u] = src[u * 32];
-            } else {
-#pragma unroll
-                for (int u = 0; u < kLaneVec; ++u) {
-                    const int64_t j = vs + u * 32 + lane;
-                    if (j >= ve) y[u] = make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
-                    else if (j < r.jlo || j >= r.jhi) {
-                        y[u] = load_edge(r.buf, j, r.mis, cb, ce < r.N ? ce : r.N);
-                        ws.ring[st][j - vs] = y[u];   // edge vectors are not copied in: keep them here
-                    }
-                    else y[u] = ws.ring[st][j - vs];
-                    if (!whole) {
-                        const int64_t g0 = 8 * j - r.mis;
-                        uint32_t wv[4] = {y[u].x, y[u].y, y[u].z, y[u].w};
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            const int64_t ga = g0 + 2 * h;
-                            if (ga < cb || ga >= ce) wv[h] = (wv[h] & 0xFFFF0000u) | 0x7FFFu;
-                            if (ga + 1 < cb || ga + 1 >= ce) wv[h] = (wv[h] & 0x0000FFFFu) | 0x7FFF0000u;
-                        }
-                        y[u] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                    }
-                }
-            }
-
-            if (!cs.open) {
-                cs.open = true;
-                shared = owner(r, (c * r.V + r.mis) >> 3) != owner(r, ((c + 1) * r.V - 1 + r.mis) >> 3);
-                tix = r.draft ? c : a.d_cols + c;
-                gcert = 0;
-            }
-            if (gcert > cs.cert) cs.cert = gcert;
-            if (cs.seen < 8 * kStageVec) {
-                // seed, until the warp has seen a full stage of the column: the
-                // kk-th largest of the group maxima certifies kk elements
-                constexpr int G = (SLOTS == 1) ? 1 : 4;
-                constexpr int PER = kLaneVec / G;
-                uint32_t key[G];
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    uint32_t m = vmax(y[g * PER]);
-#pragma unroll
-                    for (int u = 1; u < PER; ++u) m = bmax2(m, vmax(y[g * PER + u]));
-                    key[g] = order_key(hmax_splat(m) & 0xFFFFu);
-                }
-                uint32_t seed = 0;
-                if (kk == 1) {
-                    seed = __reduce_max_sync(kFull, key[0]);
-                } else {
-#pragma unroll 1
-                    for (int bit = 15; bit >= 0; --bit) {
-                        const uint32_t tr = seed | (1u << bit);
-                        int cnt = 0;
-#pragma unroll
-                        for (int g = 0; g < G; ++g) cnt += __popc(__ballot_sync(kFull, key[g] >= tr));
-                        if (cnt >= kk) seed = tr;
-                    }
-                }
-                cs.cert = seed > cs.cert ? seed : cs.cert;
-                if (shared && lane == 0 && seed > gcert) atomicMax(a.col_cert + tix, seed);
-                const int64_t lo = cb > g_first ? cb : g_first, hi = ce < g_end ? ce : g_end;
-                cs.seen += (int)(hi - lo);
-            }
-            Filter f = make_filter(cs.own, cs.cert, MAPPED);
-            uint32_t m = vmax(y[0]);
-#pragma unroll
-            for (int u = 1; u < kLaneVec; ++u) m = bmax2(m, vmax(y[u]));
-            const bool pass = f.strict ? any_gt(m, f.thr2) : any_ge(m, f.thr2);
-            if (__ballot_sync(kFull, pass)) {
-                // append the candidates: one warp prefix sum gives every lane
-                // its places, each lane writes its own (their order in the
-                // buffer does not matter, ties are settled by id when pruning)
-                const int64_t id_lane = 8 * (vs + lane) - r.mis - cb;   // id of element 0, vector 0
-                const uint16_t *sv = reinterpret_cast<const uint16_t *>(&ws.ring[st][0]);
-                uint64_t bits = 0;   // this lane's candidates: bit 8u+e = element e of vector u
-#pragma unroll
-                for (int u = 0; u < kLaneVec; ++u)
-                    if (pass && (f.strict ? any_gt(vmax(y[u]), f.thr2) : any_ge(vmax(y[u]), f.thr2)))
-                        bits |= (uint64_t)elem_mask(y[u], f) << (8 * u);
-                for (;;) {
-                    int total;
-                    const int excl = warp_exclusive_sum(__popcll(bits), lane, total);
-                    if (total == 0) break;
-                    const int space = kBufCap - cs.n;
-                    int pos = excl;
-                    uint64_t rest = bits;
-                    while (rest && pos < space) {
-                        const int b = __ffsll((long long)rest) - 1;
-                        rest &= rest - 1;
-                        const int u = b >> 3, e = b & 7;
-                        uint32_t cid = (uint32_t)(id_lane + 256 * u + e);
-                        if (MAPPED) cid = (uint32_t)__ldg(id_map + cid);
-                        wb[cs.n + pos] = pack_entry(bf16_as_float(sv[8 * (u * 32 + lane) + e]), cid);
-                        ++pos;
-                    }
-                    __syncwarp();
-                    if (total <= space) {
-                        cs.n += total;
-                        break;
-                    }
-                    // the buffer is full: prune it, then keep only what still
-                    // reaches the new key (inclusively: the rest of this
-                    // stage may hold smaller ids than entries just kept)
-                    const Pruned pq = buf_prune(wb, kBufCap, kk, lane);
-                    cs.n = pq.n;
-                    cs.own = pq.t;
-                    const float tv = bf16_as_float(key_to_raw(cs.own));
-                    uint64_t keep = 0;
-                    for (uint64_t q = rest; q; q &= q - 1) {
-                        const int b = __ffsll((long long)q) - 1;
-                        if (bf16_as_float(sv[8 * ((b >> 3) * 32 + lane) + (b & 7)]) >= tv) keep |= 1ull << b;
-                    }
-                    bits = keep;
-                }
-                __syncwarp();
-                // a first threshold as soon as kk candidates are in; after
-                // that, prune only when the buffer is three-quarters full (an
-                // append is cheap, a prune is a 16-step bisection)
-                if (cs.n >= kk && (cs.own == 0 || cs.n >= kBufCap * 3 / 4)) {
-                    const Pruned pq = buf_prune(wb, cs.n, kk, lane);
-                    cs.n = pq.n;
-                    cs.own = pq.t;
-                    if (shared && lane == 0 && cs.own > cs.cert) atomicMax(a.col_cert + tix, cs.own);
-                }
-            }
-
-            if (ce > g_end) break;                    // column c goes on past this stage
-            finish_column<MAPPED>(a, r, w, c, wb, cs.n, cs.own, lane);
-            cs = {0, 0u, 0u, false, 0};
-            ++c;
-            if (c * r.V >= g_end) break;              // next column starts in a later stage
-        }
-        __syncwarp();                                  // every lane is done with the slot
-        if (lane == 0 && i + kStages < nst) issue_stage(r, ws, J0, J1, i + kStages);
-        if (cs.open && shared) gcert = ld_relaxed(a.col_cert + tix);
-    }
-    // the slice ended inside column c: publish what this warp saw of it
-    if (cs.open) finish_column<MAPPED>(a, r, w, c, wb, cs.n, cs.own, lane);
-}
-
-template <int SLOTS, bool MAPPED>
-__global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_constant__ RoundArgs a)
-{
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int lane = threadIdx.x & 31;
-    const int gw = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-    WarpSmem &ws = reinterpret_cast<WarpSmem *>(smem)[threadIdx.x >> 5];
-    if (gw >= a.d_warps + a.t_warps) return;
-    if (lane == 0) {
-        for (int st = 0; st < kStages; ++st) mbar_init(&ws.full[st], 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
-
-    Run r;
-    const bool draft = gw < a.d_warps;
-    r.draft = draft;
-    r.buf = draft ? a.draft : a.target;
-    r.V = draft ? a.d_V : a.t_V;
-    r.N = (draft ? a.d_cols : a.t_cols) * r.V;
-    r.W = draft ? a.d_warps : a.t_warps;
-    r.gw0 = draft ? 0 : a.d_warps;
-    r.kk = draft ? a.k : 1;
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(r.buf);
-    r.mis = (int)((a0 >> 1) & 7);                       // element phase of buf in 16 B
-    r.vb = reinterpret_cast<const uint4 *>(a0 - 2 * (uintptr_t)r.mis);
-    r.NV = (r.N + r.mis + 7) >> 3;
-    r.jlo = r.mis ? 1 : 0;
-    r.jhi = ((r.N + r.mis) & 7) ? r.NV - 1 : r.NV;
-    if (r.jhi < r.jlo) r.jhi = r.jlo;
-    const int w = gw - r.gw0;
-    if (draft) stream_slice<SLOTS, MAPPED>(a, r, w, a.id_map, ws, lane);
-    else stream_slice<1, false>(a, r, w, nullptr, ws, lane);
-}
 
 // ---------------------------------------------------------------------------
 // host side
@@ -818,10 +38,19 @@ __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_co
 
 constexpr int kMaxDevices = 64;
 
+// Kernel choice.  The CTA-cooperative kernel keeps one threshold per column
+// per CTA and wins while an SM streams little of each column; the per-warp
+// kernel has no coordination inside the stream and wins once every warp sees
+// megabytes.  The crossover measured on GB300 lies between 0.1 and 3 MB of
+// logits per SM; the switch is at 1 MB.
+constexpr int64_t kCtaMaxBytesPerSm = 1 << 20;
+std::atomic<int> g_kernel_choice{SPEC_KERNEL_AUTO};
+
 struct DeviceState {
     bool init = false;
     int sms = 0;
-    int occ[2][2] = {{0, 0}, {0, 0}};   // resident CTAs per SM, [slots-1][mapped]
+    int occ_w[2][2] = {{0, 0}, {0, 0}};   // per-warp kernel: resident CTAs per SM, [slots-1][mapped]
+    int occ_c = 0;                        // CTA kernel: resident CTAs per SM
     // Scratch: [col tickets | lane tickets | target argmax | partial lists].
     // Each region keeps its place and capacity until the whole area is
     // reallocated (and zeroed), so a ticket is never laid over stale data.
@@ -855,8 +84,9 @@ spec_status cuda_fail(cudaError_t e, const char *what)
     return fail(SPEC_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
 }
 
+
 template <int S, bool M>
-void *kernel_ptr() { return reinterpret_cast<void *>(spec_round_kernel<S, M>); }
+void *kernel_ptr() { return reinterpret_cast<void *>(wrp::spec_round_kernel<S, M>); }
 
 spec_status device_state(DeviceState **out)
 {
@@ -868,16 +98,24 @@ spec_status device_state(DeviceState **out)
     if (!d.init) {
         e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-        void *kp[2][2] = {{kernel_ptr<1, false>(), kernel_ptr<1, true>()},
+        void *kw[2][2] = {{kernel_ptr<1, false>(), kernel_ptr<1, true>()},
                           {kernel_ptr<2, false>(), kernel_ptr<2, true>()}};
         for (int s = 0; s < 2; ++s)
             for (int m = 0; m < 2; ++m) {
-                e = cudaFuncSetAttribute(kp[s][m], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+                e = cudaFuncSetAttribute(kw[s][m], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wrp::kSmemBytes);
                 if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ[s][m], kp[s][m], kThreads, kSmemBytes);
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_w[s][m], kw[s][m], wrp::kThreads,
+                                                                  wrp::kSmemBytes);
                 if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-                if (d.occ[s][m] < 1) d.occ[s][m] = 1;
+                if (d.occ_w[s][m] < 1) d.occ_w[s][m] = 1;
             }
+        e = cudaFuncSetAttribute(cta::spec_round_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)cta::kSmemBytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_c, cta::spec_round_kernel, cta::kThreads,
+                                                          cta::kSmemBytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        if (d.occ_c < 1) d.occ_c = 1;
         d.init = true;
     }
     *out = &d;
@@ -972,19 +210,19 @@ int64_t vectors_of(const void *buf, int64_t n_elems)
     return (n_elems + mis + 7) >> 3;
 }
 
-// Split the warps of a full-GPU grid between the draft and the target logits
-// in proportion to their 16-byte vectors, so that every warp streams the same
-// number of bytes.  No slice is made smaller than kMinSliceVec vectors, and
-// the published lists (two per warp, kk_stride entries each) must fit in
-// max_partials entries.
-void split_warps(int64_t nv_d, int64_t nv_t, int64_t max_warps, int kk_stride, int64_t max_partials,
-                 int32_t *w_d, int32_t *w_t)
+// Split the streaming units (warps or CTAs) of a full-GPU grid between the
+// draft and the target logits in proportion to their 16-byte vectors, so
+// that every unit streams the same number of bytes.  No slice is made
+// smaller than min_slice vectors, and the published lists (two per unit,
+// kk_stride entries each) must fit in max_partials entries.
+void split_units(int64_t nv_d, int64_t nv_t, int64_t max_units, int64_t min_slice, int kk_stride,
+                 int64_t max_partials, int32_t *w_d, int32_t *w_t)
 {
-    int64_t total = max_warps;
+    int64_t total = max_units;
     const int64_t cap = max_partials / (2 * (int64_t)kk_stride);
     if (total > cap) total = cap;
     if (total < 2) total = 2;
-    auto limit = [](int64_t nv) { const int64_t m = nv / kMinSliceVec; return m < 1 ? (int64_t)1 : m; };
+    auto limit = [min_slice](int64_t nv) { const int64_t m = nv / min_slice; return m < 1 ? (int64_t)1 : m; };
     int64_t d = 0, t = 0;
     if (nv_d > 0 && nv_t > 0) {
         d = (int64_t)((double)total * (double)nv_d / (double)(nv_d + nv_t) + 0.5);
@@ -1000,6 +238,52 @@ void split_warps(int64_t nv_d, int64_t nv_t, int64_t max_warps, int kk_stride, i
     if (nv_t > 0 && t > limit(nv_t)) t = limit(nv_t);
     *w_d = (int32_t)d;
     *w_t = (int32_t)t;
+}
+
+// Which kernel runs a round, and on how many units (filled into a.d_units,
+// a.t_units; a.pstride is set too).
+struct Plan {
+    bool per_cta;
+    int slots;        // per-warp kernel: 2 for k > 32 (finer seed groups)
+    bool mapped;
+    int64_t grid;     // CTAs
+};
+
+Plan plan_round(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, bool mapped, int64_t max_partials)
+{
+    Plan p;
+    const int choice = g_kernel_choice.load(std::memory_order_relaxed);
+    p.per_cta = choice == SPEC_KERNEL_CTA ||
+                (choice == SPEC_KERNEL_AUTO && (nv_d + nv_t) * 16 <= kCtaMaxBytesPerSm * (int64_t)d.sms);
+    p.mapped = mapped;
+    p.slots = (a.d_cols > 0 && a.k > 32) ? 2 : 1;
+    a.pstride = a.k + 2;
+    if (p.per_cta) {
+        split_units(nv_d, nv_t, (int64_t)d.sms * d.occ_c, cta::kMinSliceVec, a.pstride, max_partials, &a.d_units,
+                    &a.t_units);
+        p.grid = (int64_t)a.d_units + a.t_units;
+    } else {
+        const int64_t max_warps = (int64_t)d.sms * d.occ_w[p.slots - 1][mapped ? 1 : 0] * wrp::kWarpsPerCta;
+        split_units(nv_d, nv_t, max_warps, wrp::kMinSliceVec, a.pstride, max_partials, &a.d_units, &a.t_units);
+        p.grid = ((int64_t)a.d_units + a.t_units + wrp::kWarpsPerCta - 1) / wrp::kWarpsPerCta;
+    }
+    return p;
+}
+
+// Partial-list entries a plan needs (two lists per unit).
+int64_t plan_partials(const RoundArgs &a) { return ((int64_t)a.d_units + a.t_units) * 2 * a.pstride; }
+
+void launch_plan(const Plan &p, const RoundArgs &a, cudaStream_t stream)
+{
+    if (p.per_cta) {
+        cta::spec_round_kernel<<<(unsigned)p.grid, cta::kThreads, cta::kSmemBytes, stream>>>(a);
+        return;
+    }
+    const dim3 grid((unsigned)p.grid), block(wrp::kThreads);
+    if (p.slots == 1 && !p.mapped) wrp::spec_round_kernel<1, false><<<grid, block, wrp::kSmemBytes, stream>>>(a);
+    else if (p.slots == 1) wrp::spec_round_kernel<1, true><<<grid, block, wrp::kSmemBytes, stream>>>(a);
+    else if (!p.mapped) wrp::spec_round_kernel<2, false><<<grid, block, wrp::kSmemBytes, stream>>>(a);
+    else wrp::spec_round_kernel<2, true><<<grid, block, wrp::kSmemBytes, stream>>>(a);
 }
 
 bool misaligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
@@ -1044,9 +328,7 @@ spec_status launch_round(const uint16_t *draft, int64_t cols, int64_t V, int32_t
     DeviceState *d = nullptr;
     spec_status st = device_state(&d);
     if (st != SPEC_OK) return st;
-    const int slots = (cols > 0 && k > 32) ? 2 : 1;
     const bool mapped = cols > 0 && id_map != nullptr;
-    const int64_t max_ctas = (int64_t)d->sms * d->occ[slots - 1][mapped ? 1 : 0];
     const int64_t t_cols = lanes * (gamma + 1);
 
     RoundArgs a;
@@ -1055,12 +337,10 @@ spec_status launch_round(const uint16_t *draft, int64_t cols, int64_t V, int32_t
     a.id_map = id_map; a.out_vals = vals; a.out_ids = ids;
     a.target = target; a.t_cols = t_cols; a.t_V = lanes ? tV : 1; a.gamma = gamma;
     a.drafts = drafts; a.out_accept = acc; a.out_commit = com;
-    a.pstride = a.k + 2;
-    split_warps(cols ? vectors_of(draft, cols * V) : 0, lanes ? vectors_of(target, t_cols * tV) : 0,
-                max_ctas * kWarpsPerCta, a.pstride, INT64_MAX / 4, &a.d_warps, &a.t_warps);
+    const Plan plan = plan_round(*d, a, cols ? vectors_of(draft, cols * V) : 0,
+                                 lanes ? vectors_of(target, t_cols * tV) : 0, mapped, INT64_MAX / 4);
     cudaStream_t stream = t_stream;
-    const int64_t nwarps = (int64_t)a.d_warps + a.t_warps;
-    const ScratchCaps need = {2 * (cols + t_cols), lanes, t_cols, nwarps * 2 * a.pstride};
+    const ScratchCaps need = {2 * (cols + t_cols), lanes, t_cols, plan_partials(a)};
     st = ensure_scratch(*d, need, stream);
     if (st != SPEC_OK) return st;
     const ScratchPtrs sp = scratch_ptrs(*d);
@@ -1069,12 +349,7 @@ spec_status launch_round(const uint16_t *draft, int64_t cols, int64_t V, int32_t
     a.col_cert = sp.col_ticket + (cols + t_cols);
     a.lane_ticket = sp.lane_ticket;
     a.t_argmax = sp.t_argmax;
-
-    const dim3 grid((unsigned)((nwarps + kWarpsPerCta - 1) / kWarpsPerCta)), block(kThreads);
-    if (slots == 1 && !mapped) spec_round_kernel<1, false><<<grid, block, kSmemBytes, stream>>>(a);
-    else if (slots == 1) spec_round_kernel<1, true><<<grid, block, kSmemBytes, stream>>>(a);
-    else if (!mapped) spec_round_kernel<2, false><<<grid, block, kSmemBytes, stream>>>(a);
-    else spec_round_kernel<2, true><<<grid, block, kSmemBytes, stream>>>(a);
+    launch_plan(plan, a, stream);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -1209,6 +484,17 @@ spec_status spec_round_host(const uint16_t *draft_logits, int64_t cols, int64_t 
     return SPEC_OK;
 }
 
+spec_status spec_set_kernel(int32_t which)
+{
+    t_err.clear();
+    if (which != SPEC_KERNEL_AUTO && which != SPEC_KERNEL_WARP && which != SPEC_KERNEL_CTA)
+        return fail(SPEC_ERR_ARG, "spec_set_kernel: unknown kernel %d", which);
+    g_kernel_choice.store(which, std::memory_order_relaxed);
+    return SPEC_OK;
+}
+
+int32_t spec_get_kernel(void) { return g_kernel_choice.load(std::memory_order_relaxed); }
+
 spec_status spec_set_stream(void *stream)
 {
     t_stream = static_cast<cudaStream_t>(stream);
@@ -1228,8 +514,11 @@ spec_status spec_reserve(int64_t max_cols, int32_t max_k, int64_t max_lanes, int
     spec_status st = device_state(&d);
     if (st != SPEC_OK) return st;
     const int64_t t_cols = max_lanes * (max_gamma + 1);
-    const ScratchCaps need = {2 * (max_cols + t_cols), max_lanes, t_cols,
-                              (int64_t)d->sms * d->occ[max_k > 32 ? 1 : 0][0] * kWarpsPerCta * 2 * (max_k + 2)};
+    int occ = d->occ_w[0][0];
+    for (int s = 0; s < 2; ++s)
+        for (int m = 0; m < 2; ++m) occ = d->occ_w[s][m] > occ ? d->occ_w[s][m] : occ;
+    const int64_t units = (int64_t)d->sms * occ * wrp::kWarpsPerCta;   // the per-warp kernel has the most units
+    const ScratchCaps need = {2 * (max_cols + t_cols), max_lanes, t_cols, units * 2 * (max_k + 2)};
     return ensure_scratch(*d, need, t_stream);
 }
 
@@ -1351,19 +640,15 @@ extern "C" spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t 
     st = noalloc_scratch(&base);
     if (st != SPEC_OK) return st;
 
-    const int slots = (cols > 0 && k > 32) ? 2 : 1;
-    const int64_t max_ctas = (int64_t)d->sms * d->occ[slots - 1][0];
     RoundArgs a;
     memset(&a, 0, sizeof a);
     a.draft = draft_logits; a.d_cols = cols; a.d_V = cols ? V : 1; a.k = cols ? k : 1;
     a.out_vals = out_vals; a.out_ids = out_ids;
     a.target = target_logits; a.t_cols = t_cols; a.t_V = lanes ? V : 1; a.gamma = gamma;
     a.drafts = drafts; a.out_accept = out_accept_len; a.out_commit = out_commit_ids;
-    a.pstride = a.k + 2;
-    // warps as in spec_round, fewer if their published lists would not fit
-    split_warps(cols ? vectors_of(draft_logits, cols * V) : 0, lanes ? vectors_of(target_logits, t_cols * V) : 0,
-                max_ctas * kWarpsPerCta, a.pstride, kNoAllocPartials, &a.d_warps, &a.t_warps);
-    const int64_t nwarps = (int64_t)a.d_warps + a.t_warps;
+    // units as in spec_round, fewer if their published lists would not fit
+    const Plan plan = plan_round(*d, a, cols ? vectors_of(draft_logits, cols * V) : 0,
+                                 lanes ? vectors_of(target_logits, t_cols * V) : 0, false, kNoAllocPartials);
     char *p = static_cast<char *>(base);
     a.col_ticket = reinterpret_cast<unsigned int *>(p + kNoAllocColTicket);
     a.col_cert = a.col_ticket + (cols + t_cols);
@@ -1375,9 +660,7 @@ extern "C" spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t 
     // the array keeps whatever the last call left: start every ticket at zero
     cudaError_t e = cudaMemsetAsync(base, 0, kNoAllocTicketBytes, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch tickets)");
-    const dim3 grid((unsigned)((nwarps + kWarpsPerCta - 1) / kWarpsPerCta)), block(kThreads);
-    if (slots == 1) spec_round_kernel<1, false><<<grid, block, kSmemBytes, stream>>>(a);
-    else spec_round_kernel<2, false><<<grid, block, kSmemBytes, stream>>>(a);
+    launch_plan(plan, a, stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);

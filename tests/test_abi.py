@@ -79,3 +79,14 @@ def test_stream_is_thread_local(sd):
     t.start(); t.join()
     assert sd.lib.spec_get_stream() == 0x1234 and seen == [None]
     sd.lib.spec_set_stream(None)
+
+
+def test_kernel_choice(sd):
+    assert sd.spec_get_kernel() == sd.SPEC_KERNEL_AUTO
+    for which in (sd.SPEC_KERNEL_WARP, sd.SPEC_KERNEL_CTA, sd.SPEC_KERNEL_AUTO):
+        assert sd.lib.spec_set_kernel(which) == sd.SPEC_OK
+        assert sd.spec_get_kernel() == which
+    for bad in (-1, 3, 99):
+        assert sd.lib.spec_set_kernel(bad) == sd.SPEC_ERR_ARG
+        assert "unknown kernel" in sd.spec_last_error()
+    assert sd.spec_get_kernel() == sd.SPEC_KERNEL_AUTO

@@ -1,6 +1,6 @@
 """CUDA path vs the CPU oracle, element by element and bit-exact: top-k ids and
 bf16 bits, accept lengths and committed ids.  Every call goes through the C
-ABI (via the thin binding).  Needs a GPU."""
+ABI (via the thin binding), once on each streaming kernel.  Needs a GPU."""
 from __future__ import annotations
 
 import numpy as np
@@ -23,6 +23,15 @@ def _lib():
     oracle.load()
     import speculative_decoding_draft_column_gb300 as sd
     return sd
+
+
+@pytest.fixture(autouse=True, params=[1, 2], ids=["warp", "cta"])
+def kernel(request, _lib):
+    """Every parity case runs on both streaming kernels (forced), whatever the
+    automatic choice would be for its size."""
+    _lib.spec_set_kernel(request.param)
+    yield request.param
+    _lib.spec_set_kernel(_lib.SPEC_KERNEL_AUTO)
 
 
 # ---------------------------------------------------------------------------
