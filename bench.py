@@ -39,7 +39,7 @@ if ROOT not in sys.path:
 
 METRIC = "µs per round and logit GB/s (% of GB300 HBM peak), top-k + greedy verify"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_draft_column_gb300", "csrc", "specsel.cu")
+KERNEL_DIR = os.path.join(ROOT, "speculative_decoding_draft_column_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 WORKLOADS = {
@@ -82,8 +82,23 @@ def hbm_peak():
 
 
 def source_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256 (first 16 hex digits) over the kernel sources, in name order."""
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(KERNEL_DIR)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(KERNEL_DIR, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+# The library runs a round on its CTA-cooperative kernel while the round's
+# logits are at most 1 MiB per SM and on its per-warp kernel above (the
+# automatic choice of spec_set_kernel); the bench only names the one that ran.
+CTA_MAX_BYTES_PER_SM = 1 << 20
+
+
+def kernel_name(bytes_round: int, sms: int) -> str:
+    return "cta::spec_round_kernel" if bytes_round <= CTA_MAX_BYTES_PER_SM * sms else "wrp::spec_round_kernel"
 
 
 def recorded_traffic(config: str):
@@ -429,7 +444,8 @@ def run_ours(args):
         "pct_of_hbm_peak": round(100 * gbs / world / peak, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; see synth/)",
         "config": workload_config(args, r, (R, R * bytes_round, l2)),
-        "roofline": {"bound": "hbm", "kernel": "spec_round_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": kernel_name(bytes_round, torch.cuda.get_device_properties(dev).multi_processor_count),
+                     "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "traffic": recorded_traffic(args.config), "algorithmic_bytes_per_launch": bytes_round,
                      "launch_us": round(per_launch_us, 3),

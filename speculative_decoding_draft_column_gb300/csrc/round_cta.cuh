@@ -27,6 +27,7 @@ constexpr int kQuarterVec = kQuarterWarps * kWarpVec;
 constexpr int kQuarters = (kWarpsPerCta + kQuarterWarps - 1) / kQuarterWarps;
 constexpr int kSlots = 3;                          // ring depth (180 KiB per SM)
 constexpr int kBufCap = 96;                        // candidate buffer (entries)
+constexpr int kSegSlots = 3;                       // segments the streaming warps may run ahead of the merge
 constexpr int kMinSliceVec = 1024;                 // smallest slice a CTA is given
 constexpr int64_t kSeedElems = 8 * kChunkVec / 2;  // seed a column until the CTA has seen this many elements
 
@@ -42,27 +43,63 @@ __device__ __forceinline__ int list_merge32(unsigned long long *lst, int L, unsi
 {
     const uint32_t has = __ballot_sync(kFull, e != 0ull);
     if (!has) return L;
+    const int b = __popc(has);
     const unsigned long long l0 = lane < L ? lst[lane] : 0ull;
     const unsigned long long l1 = lane + 32 < L ? lst[lane + 32] : 0ull;
-    // one pass over the candidates: each one, broadcast, moves the list
-    // entries below it down one place; the list entries above it (two
-    // ballots) and the candidates above it give its own place
     int p0 = lane, p1 = lane + 32, pc = 0;
-    for (uint32_t mm = has; mm; mm &= mm - 1) {
-        const int src = __ffs(mm) - 1;
-        const unsigned long long o = __shfl_sync(kFull, e, src);
-        pc += o > e;
-        p0 += o > l0;
-        p1 += o > l1;
-        const int above = __popc(__ballot_sync(kFull, l0 > o)) + __popc(__ballot_sync(kFull, l1 > o));
-        if (lane == src) pc += above;
+    if (b <= 8) {
+        // few: one pass over the candidates; each one, broadcast, moves the
+        // list entries below it down one place; the list entries above it
+        // (two ballots) and the candidates above it give its own place
+        for (uint32_t mm = has; mm; mm &= mm - 1) {
+            const int src = __ffs(mm) - 1;
+            const unsigned long long o = __shfl_sync(kFull, e, src);
+            pc += o > e;
+            p0 += o > l0;
+            p1 += o > l1;
+            const int above = __popc(__ballot_sync(kFull, l0 > o)) + __popc(__ballot_sync(kFull, l1 > o));
+            if (lane == src) pc += above;
+        }
+    } else {
+        // many: sort the batch across the warp (bitonic, best first); a
+        // candidate's place is its index plus the list entries above it, a
+        // list entry's its index plus the candidates above it (two searches)
+#pragma unroll
+        for (int k2 = 2; k2 <= 32; k2 <<= 1)
+#pragma unroll
+            for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
+                const unsigned long long o = __shfl_xor_sync(kFull, e, j2);
+                const bool first = (lane & j2) == 0, desc = (lane & k2) == 0;
+                e = (first == desc) ? (e > o ? e : o) : (e < o ? e : o);
+            }
+        int lo = 0, hi = L;   // list entries above e
+        if (e != 0ull)
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (lst[mid] > e) lo = mid + 1;
+                else hi = mid;
+            }
+        pc = lane + lo;
+        int c0 = 0, c1 = 0;   // batch entries above l0, l1: the first index whose entry is below
+#pragma unroll
+        for (int step = 16; step >= 1; step >>= 1) {
+            const unsigned long long v0 = __shfl_sync(kFull, e, c0 + step - 1);
+            const unsigned long long v1 = __shfl_sync(kFull, e, c1 + step - 1);
+            if (v0 > l0) c0 += step;
+            if (v1 > l1) c1 += step;
+        }
+        const unsigned long long e31 = __shfl_sync(kFull, e, 31);   // every lane takes part
+        if (c0 == 31 && e31 > l0) c0 = 32;
+        if (c1 == 31 && e31 > l1) c1 = 32;
+        p0 += c0;
+        p1 += c1;
     }
     __syncwarp();         // every read of the list is done
     if (lane < L && p0 < kk) lst[p0] = l0;
     if (lane + 32 < L && p1 < kk) lst[p1] = l1;
     if (e != 0ull && pc < kk) lst[pc] = e;
     __syncwarp();
-    const int nl = L + __popc(has);
+    const int nl = L + b;
     return nl < kk ? nl : kk;
 }
 
@@ -85,21 +122,20 @@ __device__ __forceinline__ int batch_source(int pre, int g, int &off)
 // ---- the per-CTA stream ---------------------------------------------------------
 
 // Shared memory of one CTA: its copy ring, the warps' candidate buffers (two
-// halves, alternating by segment), the CTA's list for the current column and
+// slots, rotating by segment), the CTA's list for the current column and
 // the copy barriers.
 struct CtaSmem {
     uint4 ring[kSlots][kChunkVec];
-    unsigned long long wbuf[kWarpsPerCta][2][kBufCap];
+    unsigned long long wbuf[kWarpsPerCta][kSegSlots][kBufCap];
     unsigned long long cbuf[SPEC_MAX_K];    // the CTA's list for its current column, best first
     unsigned long long tcert;               // ((column + 1) << 16) | certified key of cbuf
     uint64_t full[kSlots][kQuarters];       // a quarter chunk has landed
-    uint64_t seg_full[2];                   // every streaming warp is done with a segment (per half)
-    uint64_t seg_empty[2];                  // the merging warp is done with a half
-    uint32_t cnt[2][kWarpsPerCta];          // entries each warp appended in a segment
+    uint64_t seg_full[kSegSlots];           // every streaming warp is done with a segment (per slot)
+    uint64_t seg_empty[kSegSlots];          // the merging warp is done with a slot
+    uint32_t cnt[kSegSlots][kWarpsPerCta];  // entries each warp appended in a segment
     uint32_t done[kSlots];                  // streaming warps done with a slot's chunk
     uint32_t seedmax[2][kWarpsPerCta];
     __align__(16) uint32_t hist[2][2][128]; // seed histograms [parity][pass]: 256 16-bit counts
-    unsigned long long pool[kBufCap + 32];  // merging warp's scratch for large batches
 };
 
 constexpr size_t kSmemBytes = sizeof(CtaSmem);
@@ -167,18 +203,25 @@ __device__ __noinline__ int finish_column(const RoundArgs &a, const Run &r, int 
     if (lane == 0) last = atomicAdd(a.col_ticket + tix, 1u) == (unsigned)(wl - wf);
     if (!__shfl_sync(kFull, last, 0)) return 0;
     __threadfence();
-    // merge every slice's list, 32 lists at a time, 32 entries per step
+    // merge every slice's list, 32 lists at a time, 32 entries per step.  The
+    // best certificate of a full list (its kk-th key) bounds the column's
+    // kk-th key: entries below it are left out.
     n = 0;
     const int64_t nparts = wl - wf + 1;
     for (int64_t q0 = 0; q0 < nparts; q0 += 32) {
-        const int len = q0 + lane < nparts ? (int)__ldcg(list_slot(a, r, wf + q0 + lane, c) + kk) : 0;
+        const unsigned long long *mylist = q0 + lane < nparts ? list_slot(a, r, wf + q0 + lane, c) : nullptr;
+        const int len = mylist ? (int)__ldcg(mylist + kk) : 0;
+        const unsigned long long last = mylist ? __ldcg(mylist + kk - 1) : 0ull;
+        const uint32_t cert = __reduce_max_sync(kFull, len == kk ? entry_key(last) : 0u);
         int total;
         const int pre = warp_exclusive_sum(len, lane, total);
         for (int base = 0; base < total; base += 32) {
             int off;
             const int q = batch_source(pre, base + lane, off);
-            const unsigned long long e =
-                base + lane < total ? __ldcg(list_slot(a, r, wf + q0 + q, c) + off) : 0ull;
+            const unsigned long long *src = reinterpret_cast<const unsigned long long *>(
+                __shfl_sync(kFull, reinterpret_cast<uintptr_t>(mylist), q));
+            unsigned long long e = base + lane < total ? __ldcg(src + off) : 0ull;
+            if (entry_key(e) < cert || (n == kk && e < lst[kk - 1])) e = 0ull;
             n = list_merge32(lst, n, e, kk, lane);
         }
     }
@@ -297,7 +340,7 @@ __device__ __forceinline__ uint32_t seed_kth(uint32_t key, int kk, CtaSmem &s, i
     return ((uint32_t)b1 << 8) | (uint32_t)b2;
 }
 
-// Fold every streaming warp's candidates of a segment (half h of the warp
+// Fold every streaming warp's candidates of a segment (slot h of the warp
 // buffers) into the CTA's sorted list lst[0..n) for column c; publish the
 // list's certificate (the key of its kk-th entry).  Returns the new length.
 __device__ __forceinline__ int merge_segment(const Run &r, int64_t c, CtaSmem &s, int h, int n, int lane)
@@ -311,16 +354,6 @@ __device__ __forceinline__ int merge_segment(const Run &r, int64_t c, CtaSmem &s
         total += (int)cw[q];
     }
     if (total == 0) return n;
-    // a full list's kk-th entry: candidates below it cannot enter
-    const unsigned long long floor_e = n == kk ? s.cbuf[kk - 1] : 0ull;
-    const bool large = total > 16;   // many candidates: select, then sort
-    int pn = 0;
-    uint32_t pt = 0;                 // key certified by the pool once pruned
-    if (large) {
-        for (int i = lane; i < n; i += 32) s.pool[i] = s.cbuf[i];
-        pn = n;
-        __syncwarp();
-    }
     for (int base = 0; base < total; base += 32) {
         // candidate g = base + lane: find its warp by scanning the counts
         const int g = base + lane;
@@ -334,32 +367,8 @@ __device__ __forceinline__ int merge_segment(const Run &r, int64_t c, CtaSmem &s
             acc += (int)cw[w2];
         }
         unsigned long long e = q >= 0 ? s.wbuf[q][h][off] : 0ull;
-        if (e < floor_e || entry_key(e) < pt) e = 0ull;
-        if (!large) {
-            n = list_merge32(s.cbuf, n, e, kk, lane);
-            continue;
-        }
-        const uint32_t bal = __ballot_sync(kFull, e != 0ull);
-        if (e != 0ull) s.pool[pn + __popc(bal & lanemask_lt())] = e;
-        pn += __popc(bal);
-        __syncwarp();
-        if (pn > kBufCap) {   // at most kBufCap + 32 entries: prune to kk
-            const Pruned pq = buf_prune<kBufCap / 32 + 1>(s.pool, pn, kk, lane);
-            pn = pq.n;
-            pt = pq.t;
-        }
-    }
-    if (large) {
-        if (pn > kk) pn = buf_prune<kBufCap / 32 + 1>(s.pool, pn, kk, lane).n;
-        // sort the survivors into the list: each entry's place is its rank
-        for (int i = lane; i < pn; i += 32) {
-            const unsigned long long e = s.pool[i];
-            int rank = 0;
-            for (int j = 0; j < pn; ++j) rank += s.pool[j] > e;
-            s.cbuf[rank] = e;
-        }
-        __syncwarp();
-        n = pn;
+        if (n == kk && e < s.cbuf[kk - 1]) e = 0ull;   // below a full list's kk-th: cannot enter
+        n = list_merge32(s.cbuf, n, e, kk, lane);
     }
     if (n == kk && lane == 0)
         *reinterpret_cast<volatile unsigned long long *>(&s.tcert) =
@@ -398,8 +407,8 @@ __device__ __noinline__ void merge_slice(const RoundArgs &a, const Run &r, int64
         for (;;) {
             const int64_t ce = (c + 1) * r.V;
             const bool col_ends = ce <= k.g_end;
-            const int h = sg & 1;
-            mbar_wait(&s.seg_full[h], (uint32_t)(sg >> 1) & 1u);
+            const int h = sg % kSegSlots;
+            mbar_wait(&s.seg_full[h], (uint32_t)(sg / kSegSlots) & 1u);
             n = merge_segment(r, c, s, h, n, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.seg_empty[h]);
@@ -501,8 +510,8 @@ __device__ __forceinline__ int append_share(const Run &r, const uint4 (&y)[kLane
 
 // A streaming warp w of slice bi takes vectors [w * kWarpVec, (w + 1) *
 // kWarpVec) of every chunk.  Per segment it filters its share against the
-// column's certificate and appends its candidates to buffer half sg % 2, then
-// hands the half to the merging warp.  id_map is null for token ids.
+// column's certificate and appends its candidates to buffer slot sg % kSegSlots,
+// then hands the slot to the merging warp.  id_map is null for token ids.
 __device__ __forceinline__ void stream_slice(const RoundArgs &a, const Run &r, int bi, int64_t J0, int64_t J1,
                                              const int32_t *__restrict__ id_map, CtaSmem &s, int lane, int w)
 {
@@ -555,9 +564,9 @@ __device__ __forceinline__ void stream_slice(const RoundArgs &a, const Run &r, i
             tcta = tprev > tcta ? tprev : tcta;
             const Filter f = make_filter(tcta, tseed, id_map != nullptr);
 
-            const int h = sg & 1;
-            // buffer half h is free once the merge of segment sg - 2 is done
-            if (sg >= 2) mbar_wait(&s.seg_empty[h], (uint32_t)((sg - 2) >> 1) & 1u);
+            const int h = sg % kSegSlots;
+            // buffer slot h is free once the merge of segment sg - kSegSlots is done
+            if (sg >= kSegSlots) mbar_wait(&s.seg_empty[h], (uint32_t)((sg - kSegSlots) / kSegSlots) & 1u);
             int n = 0;
             if (__ballot_sync(kFull, f.strict ? any_gt(m, f.thr2) : any_ge(m, f.thr2)))
                 n = append_share(r, y, reinterpret_cast<const uint16_t *>(&s.ring[sl][wvs - k.vs]),
@@ -621,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_co
     if (threadIdx.x == 0) {
         for (int sl = 0; sl < kSlots; ++sl)
             for (int q = 0; q < kQuarters; ++q) mbar_init(&s.full[sl][q], 1);
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < kSegSlots; ++h) {
             mbar_init(&s.seg_full[h], kWarpsPerCta);
             mbar_init(&s.seg_empty[h], 1);
         }
