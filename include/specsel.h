@@ -122,6 +122,33 @@ spec_status spec_round(const uint16_t *draft_logits, int64_t cols, int64_t V, in
                        const uint16_t *target_logits, const int32_t *drafts, int64_t lanes,
                        int32_t gamma, int32_t *out_accept_len, int32_t *out_commit_ids);
 
+/* Speculative-decoding counters ("A drafter inside the artifact", Ignis
+ * DFlash2 page, section "See it, control it", Metrics: rounds, drafted and
+ * accepted tokens, and the per-position drafted/accepted pair), kept in
+ * DEVICE memory and only ever added to.  Per verified lane of a round:
+ *   rounds += 1;  drafted_tokens += gamma;  accepted_tokens += a;
+ *   position_drafted[i] += 1 and position_accepted[i] += (a > i)
+ * for i < gamma, where a is the lane's accept length.  So the per-position
+ * counts sum to the totals, and tokens committed per round are
+ * (accepted_tokens + rounds) / rounds (the bonus token is not a draft). */
+typedef struct {
+    uint64_t rounds;
+    uint64_t drafted_tokens;
+    uint64_t accepted_tokens;
+    uint64_t position_drafted[SPEC_MAX_GAMMA];
+    uint64_t position_accepted[SPEC_MAX_GAMMA];
+} spec_counters;
+
+/* spec_round, also adding the round's verify outcome to *counters (a device
+ * pointer to a zero-initialised or earlier-used spec_counters, 8-byte
+ * aligned; NULL: no counting, exactly spec_round).  The counts are device
+ * atomics in the same launch; concurrent calls may share one block. */
+spec_status spec_round_counted(const uint16_t *draft_logits, int64_t cols, int64_t V, int32_t k,
+                               uint16_t *out_vals, int32_t *out_ids,
+                               const uint16_t *target_logits, const int32_t *drafts, int64_t lanes,
+                               int32_t gamma, int32_t *out_accept_len, int32_t *out_commit_ids,
+                               spec_counters *counters);
+
 /* spec_round for callers holding HOST buffers: every pointer is a host
  * pointer (pinned memory copies fastest).  The call copies the inputs to
  * library-owned device staging memory, runs spec_round, copies the outputs

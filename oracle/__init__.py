@@ -129,3 +129,26 @@ def verify(target: np.ndarray, drafts: np.ndarray, threads: int | None = None, l
     _check(lib.oracle_verify(_ptr(t), _ptr(d), lanes, gamma, V, _ptr(acc), _ptr(com),
                              threads or default_threads()))
     return acc, com
+
+
+def counters(accept_len: np.ndarray, gamma: int) -> dict:
+    """The round counters of one verify round ("A drafter inside the
+    artifact", Ignis DFlash2 page, section "See it, control it", Metrics):
+    per lane one round, gamma drafted tokens and its accept length a of
+    accepted tokens; per position i < gamma one drafted token, and one
+    accepted token when a > i.  Written out lane by lane, position by
+    position (small inputs only)."""
+    acc = [int(a) for a in np.asarray(accept_len).reshape(-1)]
+    out = {"rounds": 0, "drafted_tokens": 0, "accepted_tokens": 0,
+           "position_drafted": [0] * gamma, "position_accepted": [0] * gamma}
+    for a in acc:
+        if not 0 <= a <= gamma:
+            raise ValueError(f"accept length {a} outside [0, {gamma}]")
+        out["rounds"] += 1
+        out["drafted_tokens"] += gamma
+        out["accepted_tokens"] += a
+        for i in range(gamma):
+            out["position_drafted"][i] += 1
+            if a > i:
+                out["position_accepted"][i] += 1
+    return out

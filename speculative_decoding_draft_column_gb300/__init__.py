@@ -21,7 +21,7 @@ __all__ = [
     "SPEC_OK", "SPEC_ERR_ARG", "SPEC_ERR_ALLOC", "SPEC_ERR_CUDA", "SPEC_VOCAB", "SPEC_MAX_K",
     "SPEC_MAX_GAMMA", "SpecError", "LIB_PATH", "lib",
     "spec_topk", "spec_topk_mapped", "spec_verify", "spec_verify_v", "spec_round", "spec_round_host",
-    "spec_round_noalloc",
+    "spec_round_noalloc", "spec_round_counted", "new_counters", "read_counters", "COUNTER_WORDS",
     "spec_set_kernel", "spec_get_kernel", "SPEC_KERNEL_AUTO", "SPEC_KERNEL_WARP", "SPEC_KERNEL_CTA",
     "spec_set_stream", "spec_get_stream", "spec_reserve", "spec_release", "spec_last_error",
     "spec_launch_count", "spec_device_status", "topk", "topk_mapped", "verify", "round_step", "EXPORTS",
@@ -47,6 +47,7 @@ _SIGS = {
     "spec_round": [_p, _i64, _i64, _i32, _p, _p, _p, _p, _i64, _i32, _p, _p],
     "spec_round_host": [_p, _i64, _i64, _i32, _p, _p, _p, _p, _i64, _i32, _p, _p],
     "spec_round_noalloc": [_p, _i64, _i64, _i32, _p, _p, _p, _p, _i64, _i32, _p, _p],
+    "spec_round_counted": [_p, _i64, _i64, _i32, _p, _p, _p, _p, _i64, _i32, _p, _p, _p],
     "spec_set_kernel": [_i32],
     "spec_get_kernel": [],
     "spec_set_stream": [_p],
@@ -132,6 +133,34 @@ def spec_round_noalloc(draft_logits, cols, V, k, out_vals, out_ids, target_logit
     _check(lib.spec_round_noalloc(_ptr(draft_logits), cols, V, k, _ptr(out_vals), _ptr(out_ids),
                                   _ptr(target_logits), _ptr(drafts), lanes, gamma, _ptr(out_accept_len),
                                   _ptr(out_commit_ids)))
+
+
+COUNTER_WORDS = 3 + 2 * SPEC_MAX_GAMMA   # uint64 words of a spec_counters block
+
+
+def spec_round_counted(draft_logits, cols, V, k, out_vals, out_ids, target_logits, drafts, lanes, gamma,
+                       out_accept_len, out_commit_ids, counters):
+    """spec_round that also adds the round to ``counters`` (an int64 CUDA
+    tensor of COUNTER_WORDS, see ``new_counters``; None: no counting)."""
+    _use_torch_stream()
+    _check(lib.spec_round_counted(_ptr(draft_logits), cols, V, k, _ptr(out_vals), _ptr(out_ids),
+                                  _ptr(target_logits), _ptr(drafts), lanes, gamma, _ptr(out_accept_len),
+                                  _ptr(out_commit_ids), _ptr(counters)))
+
+
+def new_counters(device="cuda"):
+    """A zeroed spec_counters block on the device (int64 tensor)."""
+    import torch
+    return torch.zeros(COUNTER_WORDS, dtype=torch.int64, device=device)
+
+
+def read_counters(counters) -> dict:
+    """The block as a dict: rounds, drafted_tokens, accepted_tokens,
+    position_drafted[15], position_accepted[15]."""
+    v = [int(x) for x in counters.cpu().tolist()]
+    g = SPEC_MAX_GAMMA
+    return {"rounds": v[0], "drafted_tokens": v[1], "accepted_tokens": v[2],
+            "position_drafted": v[3:3 + g], "position_accepted": v[3 + g:3 + 2 * g]}
 
 
 def spec_round_host(draft_logits, cols, V, k, out_vals, out_ids, target_logits, drafts, lanes, gamma,

@@ -45,7 +45,24 @@ struct RoundArgs {
     unsigned int *lane_ticket;      // [lanes]
     int32_t *t_argmax;              // [t_cols]
     int32_t pstride;
+    spec_counters *counters;        // null: no counting
 };
+
+// Add one verified lane's outcome (accept length acc of gamma drafts) to the
+// round counters: one lane per position (device atomics).
+__device__ __forceinline__ void count_lane(spec_counters *cnt, int gamma, int acc, int lane)
+{
+    if (!cnt) return;
+    if (lane == 0) {
+        atomicAdd(reinterpret_cast<unsigned long long *>(&cnt->rounds), 1ull);
+        atomicAdd(reinterpret_cast<unsigned long long *>(&cnt->drafted_tokens), (unsigned long long)gamma);
+        atomicAdd(reinterpret_cast<unsigned long long *>(&cnt->accepted_tokens), (unsigned long long)acc);
+    }
+    if (lane < gamma) {
+        atomicAdd(reinterpret_cast<unsigned long long *>(&cnt->position_drafted[lane]), 1ull);
+        if (lane < acc) atomicAdd(reinterpret_cast<unsigned long long *>(&cnt->position_accepted[lane]), 1ull);
+    }
+}
 
 // Set (bit 0) when a bounded wait gave up; read and cleared by spec_device_status.
 __device__ unsigned int g_wait_timeouts;

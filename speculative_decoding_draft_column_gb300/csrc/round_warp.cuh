@@ -74,6 +74,7 @@ __device__ __noinline__ void emit_column(const RoundArgs &a, const Run &r, int64
     const uint32_t miss = __ballot_sync(kFull, lane < a.gamma && dj != tj);
     const int acc = miss ? __ffs(miss) - 1 : a.gamma;
     if (lane < gp1) a.out_commit[ln * gp1 + lane] = lane <= acc ? tj : -1;
+    count_lane(a.counters, a.gamma, acc, lane);
     if (lane == 0) {
         a.out_accept[ln] = acc;
         a.lane_ticket[ln] = 0u;   // ready for the next launch

@@ -321,7 +321,8 @@ spec_status check_verify_args(const uint16_t *tl, const int32_t *drafts, int64_t
 // Plan and launch one kernel covering a top-k part and/or a verify part.
 spec_status launch_round(const uint16_t *draft, int64_t cols, int64_t V, int32_t k, const int32_t *id_map,
                          uint16_t *vals, int32_t *ids, const uint16_t *target, const int32_t *drafts,
-                         int64_t lanes, int32_t gamma, int64_t tV, int32_t *acc, int32_t *com)
+                         int64_t lanes, int32_t gamma, int64_t tV, int32_t *acc, int32_t *com,
+                         spec_counters *counters = nullptr)
 {
     if (cols == 0 && lanes == 0) return SPEC_OK;
     std::lock_guard<std::mutex> lock(g_mu);
@@ -337,6 +338,7 @@ spec_status launch_round(const uint16_t *draft, int64_t cols, int64_t V, int32_t
     a.id_map = id_map; a.out_vals = vals; a.out_ids = ids;
     a.target = target; a.t_cols = t_cols; a.t_V = lanes ? tV : 1; a.gamma = gamma;
     a.drafts = drafts; a.out_accept = acc; a.out_commit = com;
+    a.counters = lanes ? counters : nullptr;
     const Plan plan = plan_round(*d, a, cols ? vectors_of(draft, cols * V) : 0,
                                  lanes ? vectors_of(target, t_cols * tV) : 0, mapped, INT64_MAX / 4);
     cudaStream_t stream = t_stream;
@@ -433,6 +435,21 @@ spec_status spec_round(const uint16_t *draft_logits, int64_t cols, int64_t V, in
     if (st != SPEC_OK) return st;
     return launch_round(draft_logits, cols, V, k, nullptr, out_vals, out_ids, target_logits, drafts, lanes,
                         gamma, V, out_accept_len, out_commit_ids);
+}
+
+spec_status spec_round_counted(const uint16_t *draft_logits, int64_t cols, int64_t V, int32_t k,
+                               uint16_t *out_vals, int32_t *out_ids, const uint16_t *target_logits,
+                               const int32_t *drafts, int64_t lanes, int32_t gamma, int32_t *out_accept_len,
+                               int32_t *out_commit_ids, spec_counters *counters)
+{
+    t_err.clear();
+    spec_status st = check_topk_args(draft_logits, cols, V, k, out_vals, out_ids);
+    if (st != SPEC_OK) return st;
+    st = check_verify_args(target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids);
+    if (st != SPEC_OK) return st;
+    if (counters && misaligned(counters, 8)) return fail(SPEC_ERR_ARG, "counters misaligned (8 bytes needed)");
+    return launch_round(draft_logits, cols, V, k, nullptr, out_vals, out_ids, target_logits, drafts, lanes,
+                        gamma, V, out_accept_len, out_commit_ids, counters);
 }
 
 spec_status spec_round_host(const uint16_t *draft_logits, int64_t cols, int64_t V, int32_t k, uint16_t *out_vals,

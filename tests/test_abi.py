@@ -90,3 +90,11 @@ def test_kernel_choice(sd):
         assert sd.lib.spec_set_kernel(bad) == sd.SPEC_ERR_ARG
         assert "unknown kernel" in sd.spec_last_error()
     assert sd.spec_get_kernel() == sd.SPEC_KERNEL_AUTO
+
+
+def test_counted_round_checks_counters_alignment(sd):
+    lib = sd.lib
+    P = 0x10000   # never dereferenced: the call fails its argument checks first
+    st = lib.spec_round_counted(P, 2, 100, 3, P, P, P, P, 1, 2, P, P, P + 4)
+    assert st == sd.SPEC_ERR_ARG and "counters misaligned" in sd.spec_last_error()
+    assert sd.COUNTER_WORDS == 3 + 2 * sd.SPEC_MAX_GAMMA

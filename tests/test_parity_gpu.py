@@ -237,6 +237,49 @@ def test_round_matches_separate_calls_and_repeats():
         gu.assert_verify_equal((a, c), oracle.verify(r.target, r.drafts), f"repeat {rep}")
 
 
+def test_round_counters_accumulate():
+    """spec_round_counted: the same outputs as spec_round, and the counter
+    block gains exactly the oracle's counts of each round (accumulated over
+    rounds of different gamma; NULL counters count nothing)."""
+    import torch
+    sd = gu.sd_module()
+    cnt = sd.new_counters()
+    want = {"rounds": 0, "drafted_tokens": 0, "accepted_tokens": 0,
+            "position_drafted": [0] * sd.SPEC_MAX_GAMMA, "position_accepted": [0] * sd.SPEC_MAX_GAMMA}
+    cases = [synth.make_c2(seed=41, V=40_000), synth.make_c3(seed=42, V=30_001), synth.make_c1(seed=43, V=20_000)]
+    for r in cases:
+        x, t = gu.dev_u16(r.draft), gu.dev_u16(r.target)
+        vals = torch.empty((r.cols, r.k), dtype=torch.int16, device="cuda")
+        ids = torch.empty((r.cols, r.k), dtype=torch.int32, device="cuda")
+        acc = torch.empty(r.lanes, dtype=torch.int32, device="cuda")
+        com = torch.empty((r.lanes, r.gamma + 1), dtype=torch.int32, device="cuda")
+        sd.spec_round_counted(x, r.cols, r.V, r.k, vals, ids, t, gu.dev_i32(r.drafts), r.lanes, r.gamma, acc, com,
+                              cnt)
+        torch.cuda.synchronize()
+        sd.spec_device_status()
+        wa, wc = oracle.verify(r.target, r.drafts)
+        gu.assert_verify_equal((acc.cpu().numpy(), com.cpu().numpy()), (wa, wc), "counted round")
+        gu.assert_topk_equal((vals.cpu().numpy().view(np.uint16), ids.cpu().numpy()), oracle.topk(r.draft, r.k),
+                             "counted round")
+        c = oracle.counters(wa, r.gamma)
+        for key in ("rounds", "drafted_tokens", "accepted_tokens"):
+            want[key] += c[key]
+        for i in range(r.gamma):
+            want["position_drafted"][i] += c["position_drafted"][i]
+            want["position_accepted"][i] += c["position_accepted"][i]
+        assert sd.read_counters(cnt) == want
+    # NULL: no counting
+    r = cases[0]
+    x, t = gu.dev_u16(r.draft), gu.dev_u16(r.target)
+    vals = torch.empty((r.cols, r.k), dtype=torch.int16, device="cuda")
+    ids = torch.empty((r.cols, r.k), dtype=torch.int32, device="cuda")
+    acc = torch.empty(r.lanes, dtype=torch.int32, device="cuda")
+    com = torch.empty((r.lanes, r.gamma + 1), dtype=torch.int32, device="cuda")
+    sd.spec_round_counted(x, r.cols, r.V, r.k, vals, ids, t, gu.dev_i32(r.drafts), r.lanes, r.gamma, acc, com, None)
+    torch.cuda.synchronize()
+    assert sd.read_counters(cnt) == want
+
+
 def test_empty_and_rejected_calls_write_nothing():
     import torch
     sd = gu.sd_module()
