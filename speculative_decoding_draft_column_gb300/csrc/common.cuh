@@ -42,11 +42,18 @@ struct RoundArgs {
     unsigned long long *partials;   // [(d_units + t_units) * 2][pstride]: published lists
     unsigned int *col_ticket;       // [d_cols + t_cols]
     unsigned int *col_cert;         // [d_cols + t_cols]: best certified key published for a split column
-    unsigned int *lane_ticket;      // [lanes]
-    int32_t *t_argmax;              // [t_cols]
+    unsigned int *lane_ticket;      // [lanes]: the lane's finished columns (per-warp kernel); with, from
+                                    // bit 8 on, a bit per matching draft (CTA kernel)
     int32_t pstride;
     spec_counters *counters;        // null: no counting
 };
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel(unsigned int *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 
 // Add one verified lane's outcome (accept length acc of gamma drafts) to the
 // round counters: one lane per position (device atomics).
@@ -401,6 +408,37 @@ __device__ __forceinline__ unsigned long long *list_slot(const RoundArgs &a, con
 {
     const int sl = (c == first_elem(r, w) / r.V) ? 0 : 1;
     return a.partials + ((int64_t)(r.gw0 + w) * 2 + sl) * a.pstride;
+}
+
+// Target column c (position j = c mod (gamma+1) of lane ln) is done and
+// its argmax is `arg` (the warp's lane 0 holds it).  Lane 0 writes the
+// column's commit id and adds to the lane's ticket word, in one acq_rel
+// atomic, 1 (bits 0-7: columns done) plus, for j < gamma, bit 8+j if
+// draft j equals the argmax.  The completing column's warp reads every
+// match bit from the word: the accept length is the run of set bits from
+// bit 8, and it pads the commit ids after it with -1.
+__device__ __noinline__ void verify_column_done(const RoundArgs &a, int64_t c, int32_t arg, int lane)
+{
+    const int gamma = a.gamma, gp1 = gamma + 1;
+    const int64_t ln = c / gp1;
+    const int j = (int)(c - ln * gp1);
+    uint32_t word = 0;
+    if (lane == 0) {
+        const bool match = j < gamma && __ldg(a.drafts + ln * gamma + j) == arg;
+        a.out_commit[ln * gp1 + j] = arg;
+        const uint32_t add = 1u + ((match ? 1u : 0u) << (8 + j));
+        word = atom_add_acq_rel(a.lane_ticket + ln, add) + add;
+    }
+    word = __shfl_sync(kFull, word, 0);
+    if ((word & 0xFFu) != (uint32_t)gp1) return;
+    const uint32_t flags = (word >> 8) & ((1u << gamma) - 1u);
+    const int acc = __ffs(~flags) - 1 < gamma ? __ffs(~flags) - 1 : gamma;
+    if (lane < gp1 && lane > acc) a.out_commit[ln * gp1 + lane] = -1;
+    count_lane(a.counters, gamma, acc, lane);
+    if (lane == 0) {
+        a.out_accept[ln] = acc;
+        a.lane_ticket[ln] = 0u;   // ready for the next launch
+    }
 }
 
 }  // namespace

@@ -157,25 +157,7 @@ __device__ __noinline__ void emit_column(const RoundArgs &a, const Run &r, int64
         }
         return;
     }
-    if (lane == 0 && n > 0) a.t_argmax[c] = (int32_t)entry_id(lst[0]);
-    const int gp1 = a.gamma + 1;
-    const int64_t ln = c / gp1;
-    __threadfence();
-    __syncwarp();
-    unsigned last = 0;
-    if (lane == 0) last = atomicAdd(a.lane_ticket + ln, 1u) == (unsigned)a.gamma;
-    if (!__shfl_sync(kFull, last, 0)) return;
-    __threadfence();
-    const int32_t tj = lane < gp1 ? __ldcg(a.t_argmax + ln * gp1 + lane) : 0;
-    const int32_t dj = lane < a.gamma ? __ldg(a.drafts + ln * a.gamma + lane) : 0;
-    const uint32_t miss = __ballot_sync(kFull, lane < a.gamma && dj != tj);
-    const int acc = miss ? __ffs(miss) - 1 : a.gamma;
-    if (lane < gp1) a.out_commit[ln * gp1 + lane] = lane <= acc ? tj : -1;
-    count_lane(a.counters, a.gamma, acc, lane);
-    if (lane == 0) {
-        a.out_accept[ln] = acc;
-        a.lane_ticket[ln] = 0u;   // ready for the next launch
-    }
+    verify_column_done(a, c, n > 0 ? (int32_t)entry_id(lst[0]) : 0, lane);
 }
 
 // Column c's part in slice w is over and its best entries are the sorted

@@ -57,10 +57,12 @@ __device__ __noinline__ void emit_column(const RoundArgs &a, const Run &r, int64
             a.out_vals[c * kk + rank] = entry_raw(e);
             a.out_ids[c * kk + rank] = (int32_t)entry_id(e);
         } else if (rank == 0) {
-            a.t_argmax[c] = (int32_t)entry_id(e);
+            a.out_commit[c] = (int32_t)entry_id(e);   // column c is position c mod (gamma+1) of its lane
         }
     }
     if (r.draft) return;
+    // the lane's ticket counts its finished columns; the warp that finishes
+    // the last one reads the argmaxes back and runs the prefix match
     const int gp1 = a.gamma + 1;
     const int64_t ln = c / gp1;
     __threadfence();
@@ -69,11 +71,11 @@ __device__ __noinline__ void emit_column(const RoundArgs &a, const Run &r, int64
     if (lane == 0) last = atomicAdd(a.lane_ticket + ln, 1u) == (unsigned)a.gamma;
     if (!__shfl_sync(kFull, last, 0)) return;
     __threadfence();
-    const int32_t tj = lane < gp1 ? __ldcg(a.t_argmax + ln * gp1 + lane) : 0;
+    const int32_t tj = lane < gp1 ? __ldcg(a.out_commit + ln * gp1 + lane) : 0;
     const int32_t dj = lane < a.gamma ? __ldg(a.drafts + ln * a.gamma + lane) : 0;
     const uint32_t miss = __ballot_sync(kFull, lane < a.gamma && dj != tj);
     const int acc = miss ? __ffs(miss) - 1 : a.gamma;
-    if (lane < gp1) a.out_commit[ln * gp1 + lane] = lane <= acc ? tj : -1;
+    if (lane < gp1 && lane > acc) a.out_commit[ln * gp1 + lane] = -1;
     count_lane(a.counters, a.gamma, acc, lane);
     if (lane == 0) {
         a.out_accept[ln] = acc;

@@ -51,12 +51,12 @@ struct DeviceState {
     int sms = 0;
     int occ_w[2][2] = {{0, 0}, {0, 0}};   // per-warp kernel: resident CTAs per SM, [slots-1][mapped]
     int occ_c = 0;                        // CTA kernel: resident CTAs per SM
-    // Scratch: [col tickets | lane tickets | target argmax | partial lists].
+    // Scratch: [col tickets and certificates | lane tickets | partial lists].
     // Each region keeps its place and capacity until the whole area is
     // reallocated (and zeroed), so a ticket is never laid over stale data.
     void *scratch = nullptr;
     size_t scratch_bytes = 0;
-    int64_t cap_cols = 0, cap_lanes = 0, cap_tcols = 0, cap_part = 0;
+    int64_t cap_cols = 0, cap_lanes = 0, cap_part = 0;
     void *staging = nullptr;
     size_t staging_bytes = 0;
 };
@@ -127,18 +127,16 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct ScratchPtrs {
     unsigned int *col_ticket;
     unsigned int *lane_ticket;
-    int32_t *t_argmax;
     unsigned long long *partials;
 };
 
 struct ScratchCaps {
-    int64_t cols, lanes, tcols, part;   // part = partial-list entries (u64)
+    int64_t cols, lanes, part;   // cols = ticket/certificate words; part = partial-list entries (u64)
 };
 
 size_t scratch_bytes(const ScratchCaps &c)
 {
-    return align256((size_t)c.cols * 4) + align256((size_t)c.lanes * 4) + align256((size_t)c.tcols * 4) +
-           align256((size_t)c.part * 8);
+    return align256((size_t)c.cols * 4) + align256((size_t)c.lanes * 4) + align256((size_t)c.part * 8);
 }
 
 ScratchPtrs scratch_ptrs(const DeviceState &d)
@@ -149,8 +147,6 @@ ScratchPtrs scratch_ptrs(const DeviceState &d)
     p += align256((size_t)d.cap_cols * 4);
     s.lane_ticket = reinterpret_cast<unsigned int *>(p);
     p += align256((size_t)d.cap_lanes * 4);
-    s.t_argmax = reinterpret_cast<int32_t *>(p);
-    p += align256((size_t)d.cap_tcols * 4);
     s.partials = reinterpret_cast<unsigned long long *>(p);
     return s;
 }
@@ -167,8 +163,7 @@ bool stream_capturing(cudaStream_t st)
 // when they finish.
 spec_status ensure_scratch(DeviceState &d, const ScratchCaps &need, cudaStream_t st)
 {
-    if (d.scratch && need.cols <= d.cap_cols && need.lanes <= d.cap_lanes && need.tcols <= d.cap_tcols &&
-        need.part <= d.cap_part)
+    if (d.scratch && need.cols <= d.cap_cols && need.lanes <= d.cap_lanes && need.part <= d.cap_part)
         return SPEC_OK;
     if (stream_capturing(st))
         return fail(SPEC_ERR_ALLOC, "scratch must grow during stream capture; call spec_reserve before capturing");
@@ -176,7 +171,6 @@ spec_status ensure_scratch(DeviceState &d, const ScratchCaps &need, cudaStream_t
     ScratchCaps c;
     c.cols = grow(d.cap_cols, need.cols);
     c.lanes = grow(d.cap_lanes, need.lanes);
-    c.tcols = grow(d.cap_tcols, need.tcols);
     c.part = grow(d.cap_part, need.part);
     const size_t bytes = scratch_bytes(c);
     cudaError_t e;
@@ -186,7 +180,7 @@ spec_status ensure_scratch(DeviceState &d, const ScratchCaps &need, cudaStream_t
         cudaFree(d.scratch);
         d.scratch = nullptr;
         d.scratch_bytes = 0;
-        d.cap_cols = d.cap_lanes = d.cap_tcols = d.cap_part = 0;
+        d.cap_cols = d.cap_lanes = d.cap_part = 0;
     }
     e = cudaMalloc(&d.scratch, bytes);
     if (e != cudaSuccess) {
@@ -199,7 +193,6 @@ spec_status ensure_scratch(DeviceState &d, const ScratchCaps &need, cudaStream_t
     d.scratch_bytes = bytes;
     d.cap_cols = c.cols;
     d.cap_lanes = c.lanes;
-    d.cap_tcols = c.tcols;
     d.cap_part = c.part;
     return SPEC_OK;
 }
@@ -342,7 +335,7 @@ spec_status launch_round(const uint16_t *draft, int64_t cols, int64_t V, int32_t
     const Plan plan = plan_round(*d, a, cols ? vectors_of(draft, cols * V) : 0,
                                  lanes ? vectors_of(target, t_cols * tV) : 0, mapped, INT64_MAX / 4);
     cudaStream_t stream = t_stream;
-    const ScratchCaps need = {2 * (cols + t_cols), lanes, t_cols, plan_partials(a)};
+    const ScratchCaps need = {2 * (cols + t_cols), lanes, plan_partials(a)};
     st = ensure_scratch(*d, need, stream);
     if (st != SPEC_OK) return st;
     const ScratchPtrs sp = scratch_ptrs(*d);
@@ -350,7 +343,6 @@ spec_status launch_round(const uint16_t *draft, int64_t cols, int64_t V, int32_t
     a.col_ticket = sp.col_ticket;
     a.col_cert = sp.col_ticket + (cols + t_cols);
     a.lane_ticket = sp.lane_ticket;
-    a.t_argmax = sp.t_argmax;
     launch_plan(plan, a, stream);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
@@ -535,7 +527,7 @@ spec_status spec_reserve(int64_t max_cols, int32_t max_k, int64_t max_lanes, int
     for (int s = 0; s < 2; ++s)
         for (int m = 0; m < 2; ++m) occ = d->occ_w[s][m] > occ ? d->occ_w[s][m] : occ;
     const int64_t units = (int64_t)d->sms * occ * wrp::kWarpsPerCta;   // the per-warp kernel has the most units
-    const ScratchCaps need = {2 * (max_cols + t_cols), max_lanes, t_cols, units * 2 * (max_k + 2)};
+    const ScratchCaps need = {2 * (max_cols + t_cols), max_lanes, units * 2 * (max_k + 2)};
     return ensure_scratch(*d, need, t_stream);
 }
 
@@ -555,7 +547,7 @@ spec_status spec_release(void)
     if (d.staging) cudaFree(d.staging);
     d.scratch = d.staging = nullptr;
     d.scratch_bytes = d.staging_bytes = 0;
-    d.cap_cols = d.cap_lanes = d.cap_tcols = d.cap_part = 0;
+    d.cap_cols = d.cap_lanes = d.cap_part = 0;
     return SPEC_OK;
 }
 
@@ -589,7 +581,7 @@ spec_status spec_device_status(void)
 // free memory), a serving loop that must never pay the device-wide
 // synchronisation that cudaFree implies, or a C host that runs under a fixed
 // memory budget.  For them this entry point keeps its scratch (column and lane
-// tickets, target argmaxes, partial lists) in one statically sized device
+// tickets, column certificates, partial lists) in one statically sized device
 // array, so it allocates nothing, ever.  The array costs every GPU that loads
 // the library its size until the process exits.
 
@@ -600,10 +592,9 @@ constexpr int64_t kNoAllocMaxLanes = SPEC_NOALLOC_MAX_LANES;
 constexpr int64_t kNoAllocPartials = 131072;                    // partial-list entries (1 MiB)
 constexpr size_t kNoAllocColTicket = 0;
 constexpr size_t kNoAllocLaneTicket = kNoAllocColTicket + ((2 * kNoAllocMaxCols * 4 + 255) & ~int64_t(255));
-constexpr size_t kNoAllocArgmax = kNoAllocLaneTicket + ((kNoAllocMaxLanes * 4 + 255) & ~int64_t(255));
-constexpr size_t kNoAllocPart = kNoAllocArgmax + ((kNoAllocMaxCols * 4 + 255) & ~int64_t(255));
+constexpr size_t kNoAllocPart = kNoAllocLaneTicket + ((kNoAllocMaxLanes * 4 + 255) & ~int64_t(255));
 constexpr size_t kNoAllocBytes = kNoAllocPart + kNoAllocPartials * 8;
-constexpr size_t kNoAllocTicketBytes = kNoAllocArgmax;         // tickets and column certificates, cleared per call
+constexpr size_t kNoAllocTicketBytes = kNoAllocPart;           // tickets and column certificates, cleared per call
 
 // Device scratch of spec_round_noalloc.  In host code this name only stands
 // for the symbol; the device address comes from cudaGetSymbolAddress.
@@ -670,7 +661,6 @@ extern "C" spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t 
     a.col_ticket = reinterpret_cast<unsigned int *>(p + kNoAllocColTicket);
     a.col_cert = a.col_ticket + (cols + t_cols);
     a.lane_ticket = reinterpret_cast<unsigned int *>(p + kNoAllocLaneTicket);
-    a.t_argmax = reinterpret_cast<int32_t *>(p + kNoAllocArgmax);
     a.partials = reinterpret_cast<unsigned long long *>(p + kNoAllocPart);
 
     cudaStream_t stream = t_stream;
