@@ -113,6 +113,31 @@ spec_status spec_verify_v(const uint16_t *target_logits, const int32_t *drafts, 
                           int32_t gamma, int64_t V, int32_t *out_accept_len,
                           int32_t *out_commit_ids);
 
+/* Sampled verify with one-hot drafts (speculative sampling; "A drafter
+ * inside the artifact", Ignis DFlash2 page, "The numbers": sampled
+ * acceptance at T = 1.0, top_p 0.95, top_k 20).  Per target column the
+ * target's distribution q is computed in float64 from the column's top_k
+ * logits (largest first, ties to the smaller id), in this order:
+ * z_t = v_t / temperature; e_t = exp(z_t - z_0); p_t = e_t / sum(e);
+ * the nucleus is the shortest prefix whose running sum of p reaches top_p;
+ * q_t = p_t / (that sum).  Position j < gamma accepts draft j when
+ * uniforms[l][j][0] < q_j(draft j) (0 outside the nucleus).  The first
+ * rejected position commits a draw from q_j without the draft: the first
+ * nucleus token (draft skipped, list order) whose running q exceeds
+ * uniforms[l][j][1] times the total q without the draft.  A lane that accepts
+ * all gamma drafts commits a draw from q_gamma with uniforms[l][gamma][1].
+ *   uniforms  double [lanes][gamma+1][2], each in [0, 1), caller-owned device
+ *             memory (random numbers are inputs: no generator inside).
+ *   temperature > 0, 0 < top_p <= 1, 1 <= top_k <= min(V, 64).
+ *   out_accept_len, out_commit_ids as for spec_verify: the accepted drafts,
+ *   then the draw, then -1.
+ * With top_k = 1 this is exactly spec_verify_v.  One launch; target logits
+ * are read once. */
+spec_status spec_verify_sampled(const uint16_t *target_logits, const int32_t *drafts, int64_t lanes,
+                                int32_t gamma, int64_t V, double temperature, double top_p,
+                                int32_t top_k, const double *uniforms, int32_t *out_accept_len,
+                                int32_t *out_commit_ids);
+
 /* One whole selection step in ONE kernel launch: spec_topk over the draft
  * columns and spec_verify_v over the target columns, same vocabulary V.
  * Results are identical to the two separate calls.  Either part may be

@@ -152,3 +152,98 @@ def counters(accept_len: np.ndarray, gamma: int) -> dict:
             if a > i:
                 out["position_accepted"][i] += 1
     return out
+
+
+def sampled_column(values: np.ndarray, ids: np.ndarray, temperature: float, top_p: float):
+    """The target's sampling distribution over one column's top-k set
+    ("A drafter inside the artifact", Ignis DFlash2 page, "The numbers":
+    sampled acceptance at T, top_p, top_k).  values: the top-k bf16 bits,
+    best first (ties by smaller id), ids: their token ids.  Steps, each in
+    float64 and in this order: z_t = v_t / T; e_t = exp(z_t - z_0); S = sum of
+    e_t in list order; p_t = e_t / S; the nucleus is the shortest prefix whose
+    running sum c_t (list order) reaches top_p; q_t = p_t / c_last on it.
+    Returns (kept ids, q)."""
+    vals = np.asarray(values, dtype=np.uint16).astype(np.uint32) << 16
+    x = vals.view(np.float32).astype(np.float64)
+    z = [float(xi) / temperature for xi in x]
+    e = [np.exp(zi - z[0]) for zi in z]
+    S = 0.0
+    for ei in e:
+        S += ei
+    p = [ei / S for ei in e]
+    c, last = 0.0, len(p) - 1
+    for t, pt in enumerate(p):
+        c += pt
+        if c >= top_p:
+            last = t
+            break
+    kept = [int(i) for i in ids[:last + 1]]
+    q = [p[t] / c for t in range(last + 1)]
+    return kept, q
+
+
+def sampled_decision(kept, q, draft: int | None, u: float, u2: float):
+    """One position of sampled verify with a one-hot draft: accept the draft
+    when u < q(draft) (q = 0 outside the nucleus); otherwise (or with no
+    draft, the bonus position) draw from q with the draft's mass removed:
+    the first kept token (list order, the draft skipped) whose running weight
+    exceeds u2 times the total weight.  Returns (accepted, token, margin):
+    token is the draft when accepted, else the draw; margin is the smallest
+    distance of u or u2 (scaled) to a decision boundary."""
+    qd = 0.0
+    if draft is not None:
+        for t, tok in enumerate(kept):
+            if tok == draft:
+                qd = q[t]
+        if u < qd:
+            return True, int(draft), abs(u - qd)
+    margin = abs(u - qd) if draft is not None else float("inf")
+    W = 0.0
+    for t, tok in enumerate(kept):
+        if draft is None or tok != draft:
+            W += q[t]
+    target = u2 * W
+    run, pick = 0.0, None
+    for t, tok in enumerate(kept):
+        if draft is not None and tok == draft:
+            continue
+        prev = run
+        run += q[t]
+        if pick is None and run > target:
+            pick = tok
+            margin = min(margin, abs(target - prev), abs(run - target))
+    if pick is None:   # rounding left the target at the very end: the last kept token
+        pick = [tok for tok in kept if draft is None or tok != draft][-1]
+        margin = 0.0
+    return False, int(pick), margin
+
+
+def sampled_verify(target: np.ndarray, drafts: np.ndarray, temperature: float, top_p: float, top_k: int,
+                   uniforms: np.ndarray, threads: int | None = None):
+    """Sampled verify with one-hot drafts (speculative sampling): target
+    [lanes*(gamma+1), V] bf16 bits, drafts [lanes, gamma], uniforms
+    [lanes, gamma+1, 2] in [0, 1).  Position j < gamma accepts draft j with
+    probability q_j(draft j); the first rejection commits a draw from q_j
+    without the draft, and a lane that accepts all gamma drafts commits a
+    bonus draw from q_gamma.  Returns (accept_len, commit_ids, min margin)."""
+    d = np.ascontiguousarray(drafts, dtype=np.int32)
+    lanes, gamma = d.shape
+    t = np.ascontiguousarray(target, dtype=np.uint16).reshape(lanes * (gamma + 1), -1)
+    u = np.asarray(uniforms, dtype=np.float64).reshape(lanes, gamma + 1, 2)
+    vals, ids = topk(t, top_k, threads=threads)
+    acc = np.zeros(lanes, dtype=np.int32)
+    com = np.full((lanes, gamma + 1), -1, dtype=np.int32)
+    margin = float("inf")
+    for ln in range(lanes):
+        a = gamma
+        for j in range(gamma + 1):
+            kept, q = sampled_column(vals[ln * (gamma + 1) + j], ids[ln * (gamma + 1) + j], temperature, top_p)
+            draft = int(d[ln, j]) if j < gamma else None
+            ok, tok, m = sampled_decision(kept, q, draft, float(u[ln, j, 0]), float(u[ln, j, 1]))
+            margin = min(margin, m)
+            com[ln, j] = tok
+            if not ok:
+                a = j
+                break
+        acc[ln] = a
+    return acc, com, margin

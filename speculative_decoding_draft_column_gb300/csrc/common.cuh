@@ -46,6 +46,11 @@ struct RoundArgs {
                                     // bit 8 on, a bit per matching draft (CTA kernel)
     int32_t pstride;
     spec_counters *counters;        // null: no counting
+    // sampled verify (uniforms non-null): the target columns keep their
+    // top t_k (else t_k = 1, the argmax)
+    int32_t t_k;
+    double temperature, top_p;
+    const double *uniforms;         // [lanes][gamma+1][2]
 };
 
 __device__ __forceinline__ uint32_t atom_add_acq_rel(unsigned int *p, uint32_t v)
@@ -427,6 +432,103 @@ __device__ __noinline__ void verify_column_done(const RoundArgs &a, int64_t c, i
         const bool match = j < gamma && __ldg(a.drafts + ln * gamma + j) == arg;
         a.out_commit[ln * gp1 + j] = arg;
         const uint32_t add = 1u + ((match ? 1u : 0u) << (8 + j));
+        word = atom_add_acq_rel(a.lane_ticket + ln, add) + add;
+    }
+    word = __shfl_sync(kFull, word, 0);
+    if ((word & 0xFFu) != (uint32_t)gp1) return;
+    const uint32_t flags = (word >> 8) & ((1u << gamma) - 1u);
+    const int acc = __ffs(~flags) - 1 < gamma ? __ffs(~flags) - 1 : gamma;
+    if (lane < gp1 && lane > acc) a.out_commit[ln * gp1 + lane] = -1;
+    count_lane(a.counters, gamma, acc, lane);
+    if (lane == 0) {
+        a.out_accept[ln] = acc;
+        a.lane_ticket[ln] = 0u;   // ready for the next launch
+    }
+}
+
+// Sampled verify of target column c (position j = c mod (gamma+1) of lane
+// ln) from its top-t_k list lst[0..n), best first -- speculative sampling
+// with a one-hot draft ("A drafter inside the artifact", Ignis DFlash2
+// page, "The numbers": sampled acceptance at T, top_p, top_k).  In float64
+// and in list order: z_t = v_t / T; e_t = exp(z_t - z_0); S = sum e_t;
+// p_t = e_t / S; the nucleus is the shortest prefix whose running sum of p
+// reaches top_p; q_t = p_t / (that sum).  Draft j is accepted when u < q(draft)
+// (u = uniforms[ln][j][0]); otherwise -- and always at position gamma, the
+// bonus -- the token drawn is the first nucleus token (draft skipped) whose
+// running q exceeds uniforms[ln][j][1] times the total q without the draft.
+// The position's token (the draft, or the draw) goes to its commit id and
+// its acceptance bit to the lane's ticket word, as in verify_column_done.
+// Every lane computes the same sums (broadcast terms, same order).
+__device__ __noinline__ void sampled_column_done(const RoundArgs &a, int64_t c, const unsigned long long *lst, int n,
+                                                 int lane)
+{
+    const int gamma = a.gamma, gp1 = gamma + 1;
+    const int64_t ln = c / gp1;
+    const int j = (int)(c - ln * gp1);
+    const double T = a.temperature;
+    const unsigned long long ea_ = lane < n ? lst[lane] : 0ull, eb_ = lane + 32 < n ? lst[lane + 32] : 0ull;
+    const double z0 = (double)bf16_as_float(entry_raw(lst[0])) / T;
+    const double ea = lane < n ? exp((double)bf16_as_float(entry_raw(ea_)) / T - z0) : 0.0;
+    const double eb = lane + 32 < n ? exp((double)bf16_as_float(entry_raw(eb_)) / T - z0) : 0.0;
+    const int32_t ida = lane < n ? (int32_t)entry_id(ea_) : -1, idb = lane + 32 < n ? (int32_t)entry_id(eb_) : -1;
+    double S = 0.0;
+    for (int t = 0; t < n; ++t) {
+        const double va = __shfl_sync(kFull, ea, t & 31), vb = __shfl_sync(kFull, eb, t & 31);
+        S += t < 32 ? va : vb;
+    }
+    const double pa = ea / S, pb = eb / S;
+    double cum = 0.0, C = 0.0;
+    int last = n - 1;
+    bool found = false;
+    for (int t = 0; t < n; ++t) {
+        const double va = __shfl_sync(kFull, pa, t & 31), vb = __shfl_sync(kFull, pb, t & 31);
+        cum += t < 32 ? va : vb;
+        if (!found && cum >= a.top_p) {
+            found = true;
+            last = t;
+            C = cum;
+        }
+    }
+    if (!found) C = cum;
+    const double qa = lane <= last ? pa / C : 0.0, qb = lane + 32 <= last ? pb / C : 0.0;
+    const int32_t draft = j < gamma ? __ldg(a.drafts + ln * gamma + j) : -1;
+    const double u = a.uniforms[(ln * gp1 + j) * 2], u2 = a.uniforms[(ln * gp1 + j) * 2 + 1];
+    // q of the draft (0 outside the nucleus)
+    const uint32_t ha = __ballot_sync(kFull, lane <= last && ida == draft && draft >= 0);
+    const uint32_t hb = __ballot_sync(kFull, lane + 32 <= last && idb == draft && draft >= 0);
+    double qd = 0.0;
+    {
+        const double xa = __shfl_sync(kFull, qa, ha ? __ffs(ha) - 1 : 0);
+        const double xb = __shfl_sync(kFull, qb, hb ? __ffs(hb) - 1 : 0);
+        qd = ha ? xa : (hb ? xb : 0.0);
+    }
+    const bool accepted = j < gamma && u < qd;
+    int32_t token = draft;
+    if (!accepted) {
+        double W = 0.0;
+        for (int t = 0; t <= last; ++t) {
+            const double va = __shfl_sync(kFull, qa, t & 31), vb = __shfl_sync(kFull, qb, t & 31);
+            const int32_t ia = __shfl_sync(kFull, ida, t & 31), ib = __shfl_sync(kFull, idb, t & 31);
+            if ((t < 32 ? ia : ib) != draft) W += t < 32 ? va : vb;
+        }
+        const double target = u2 * W;
+        double run = 0.0;
+        int32_t pick = -1, last_tok = -1;
+        for (int t = 0; t <= last; ++t) {
+            const double va = __shfl_sync(kFull, qa, t & 31), vb = __shfl_sync(kFull, qb, t & 31);
+            const int32_t ia = __shfl_sync(kFull, ida, t & 31), ib = __shfl_sync(kFull, idb, t & 31);
+            const int32_t tok = t < 32 ? ia : ib;
+            if (tok == draft) continue;
+            last_tok = tok;
+            run += t < 32 ? va : vb;
+            if (pick < 0 && run > target) pick = tok;
+        }
+        token = pick >= 0 ? pick : last_tok;
+    }
+    uint32_t word = 0;
+    if (lane == 0) {
+        a.out_commit[ln * gp1 + j] = token;
+        const uint32_t add = 1u + ((accepted ? 1u : 0u) << (8 + j));
         word = atom_add_acq_rel(a.lane_ticket + ln, add) + add;
     }
     word = __shfl_sync(kFull, word, 0);

@@ -157,7 +157,8 @@ __device__ __noinline__ void emit_column(const RoundArgs &a, const Run &r, int64
         }
         return;
     }
-    verify_column_done(a, c, n > 0 ? (int32_t)entry_id(lst[0]) : 0, lane);
+    if (a.uniforms) sampled_column_done(a, c, lst, n, lane);
+    else verify_column_done(a, c, n > 0 ? (int32_t)entry_id(lst[0]) : 0, lane);
 }
 
 // Column c's part in slice w is over and its best entries are the sorted
@@ -598,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_co
     r.N = (draft ? a.d_cols : a.t_cols) * r.V;
     r.W = draft ? a.d_units : a.t_units;
     r.gw0 = draft ? 0 : a.d_units;
-    r.kk = draft ? a.k : 1;
+    r.kk = draft ? a.k : a.t_k;
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(r.buf);
     r.mis = (int)((a0 >> 1) & 7);                       // element phase of buf in 16 B
     r.vb = reinterpret_cast<const uint4 *>(a0 - 2 * (uintptr_t)r.mis);

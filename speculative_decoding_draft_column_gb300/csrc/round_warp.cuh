@@ -46,7 +46,7 @@ constexpr size_t kSmemBytes = (size_t)kWarpsPerCta * sizeof(WarpSmem);
 // ranked by value; top-k outputs, or for a target column the argmax and, for
 // the lane's last column, the prefix match (one lane per position).
 __device__ __noinline__ void emit_column(const RoundArgs &a, const Run &r, int64_t c,
-                                         const unsigned long long *wb, int n, int lane)
+                                         unsigned long long *wb, int n, int lane)
 {
     const int kk = r.kk;
     for (int i = lane; i < n; i += 32) {
@@ -56,11 +56,26 @@ __device__ __noinline__ void emit_column(const RoundArgs &a, const Run &r, int64
         if (r.draft) {
             a.out_vals[c * kk + rank] = entry_raw(e);
             a.out_ids[c * kk + rank] = (int32_t)entry_id(e);
-        } else if (rank == 0) {
+        } else if (rank == 0 && !a.uniforms) {
             a.out_commit[c] = (int32_t)entry_id(e);   // column c is position c mod (gamma+1) of its lane
         }
     }
     if (r.draft) return;
+    if (a.uniforms) {
+        // sampled verify needs the list best first: place every entry at its rank
+        const unsigned long long e0 = lane < n ? wb[lane] : 0ull, e1 = lane + 32 < n ? wb[lane + 32] : 0ull;
+        int r0 = 0, r1 = 0;
+        for (int j = 0; j < n; ++j) {
+            r0 += wb[j] > e0;
+            r1 += wb[j] > e1;
+        }
+        __syncwarp();
+        if (lane < n) wb[r0] = e0;
+        if (lane + 32 < n) wb[r1] = e1;
+        __syncwarp();
+        sampled_column_done(a, c, wb, n, lane);
+        return;
+    }
     // the lane's ticket counts its finished columns; the warp that finishes
     // the last one reads the argmaxes back and runs the prefix match
     const int gp1 = a.gamma + 1;
@@ -288,7 +303,10 @@ __device__ __forceinline__ void stream_slice(const RoundArgs &a, const Run &r, i
                 }
                 uint32_t seed = 0;
                 if (kk == 1) {
-                    seed = __reduce_max_sync(kFull, key[0]);
+                    uint32_t km = key[0];
+#pragma unroll
+                    for (int g = 1; g < G; ++g) km = key[g] > km ? key[g] : km;
+                    seed = __reduce_max_sync(kFull, km);
                 } else {
 #pragma unroll 1
                     for (int bit = 15; bit >= 0; --bit) {
@@ -405,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_co
     r.N = (draft ? a.d_cols : a.t_cols) * r.V;
     r.W = draft ? a.d_units : a.t_units;
     r.gw0 = draft ? 0 : a.d_units;
-    r.kk = draft ? a.k : 1;
+    r.kk = draft ? a.k : a.t_k;
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(r.buf);
     r.mis = (int)((a0 >> 1) & 7);                       // element phase of buf in 16 B
     r.vb = reinterpret_cast<const uint4 *>(a0 - 2 * (uintptr_t)r.mis);
@@ -415,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_co
     if (r.jhi < r.jlo) r.jhi = r.jlo;
     const int w = gw - r.gw0;
     if (draft) stream_slice<SLOTS, MAPPED>(a, r, w, a.id_map, ws, lane);
-    else stream_slice<1, false>(a, r, w, nullptr, ws, lane);
+    else stream_slice<SLOTS, false>(a, r, w, nullptr, ws, lane);
 }
 
 }  // namespace wrp

@@ -249,8 +249,9 @@ Plan plan_round(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, 
     p.per_cta = choice == SPEC_KERNEL_CTA ||
                 (choice == SPEC_KERNEL_AUTO && (nv_d + nv_t) * 16 <= kCtaMaxBytesPerSm * (int64_t)d.sms);
     p.mapped = mapped;
-    p.slots = (a.d_cols > 0 && a.k > 32) ? 2 : 1;
-    a.pstride = a.k + 2;
+    const int kmax = a.k > a.t_k ? a.k : a.t_k;   // the larger list of the two runs
+    p.slots = kmax > 32 ? 2 : 1;
+    a.pstride = kmax + 2;
     if (p.per_cta) {
         split_units(nv_d, nv_t, (int64_t)d.sms * d.occ_c, cta::kMinSliceVec, a.pstride, max_partials, &a.d_units,
                     &a.t_units);
@@ -312,10 +313,17 @@ spec_status check_verify_args(const uint16_t *tl, const int32_t *drafts, int64_t
 }
 
 // Plan and launch one kernel covering a top-k part and/or a verify part.
+// Sampled verify parameters (uniforms == nullptr: greedy verify).
+struct Sampling {
+    int32_t top_k = 1;
+    double temperature = 1.0, top_p = 1.0;
+    const double *uniforms = nullptr;
+};
+
 spec_status launch_round(const uint16_t *draft, int64_t cols, int64_t V, int32_t k, const int32_t *id_map,
                          uint16_t *vals, int32_t *ids, const uint16_t *target, const int32_t *drafts,
                          int64_t lanes, int32_t gamma, int64_t tV, int32_t *acc, int32_t *com,
-                         spec_counters *counters = nullptr)
+                         spec_counters *counters = nullptr, const Sampling &smp = Sampling())
 {
     if (cols == 0 && lanes == 0) return SPEC_OK;
     std::lock_guard<std::mutex> lock(g_mu);
@@ -332,6 +340,10 @@ spec_status launch_round(const uint16_t *draft, int64_t cols, int64_t V, int32_t
     a.target = target; a.t_cols = t_cols; a.t_V = lanes ? tV : 1; a.gamma = gamma;
     a.drafts = drafts; a.out_accept = acc; a.out_commit = com;
     a.counters = lanes ? counters : nullptr;
+    a.t_k = lanes && smp.uniforms ? smp.top_k : 1;
+    a.temperature = smp.temperature;
+    a.top_p = smp.top_p;
+    a.uniforms = lanes ? smp.uniforms : nullptr;
     const Plan plan = plan_round(*d, a, cols ? vectors_of(draft, cols * V) : 0,
                                  lanes ? vectors_of(target, t_cols * tV) : 0, mapped, INT64_MAX / 4);
     cudaStream_t stream = t_stream;
@@ -408,6 +420,29 @@ spec_status spec_verify_v(const uint16_t *target_logits, const int32_t *drafts, 
     if (st != SPEC_OK) return st;
     return launch_round(nullptr, 0, 1, 1, nullptr, nullptr, nullptr, target_logits, drafts, lanes, gamma, V,
                         out_accept_len, out_commit_ids);
+}
+
+spec_status spec_verify_sampled(const uint16_t *target_logits, const int32_t *drafts, int64_t lanes, int32_t gamma,
+                                int64_t V, double temperature, double top_p, int32_t top_k, const double *uniforms,
+                                int32_t *out_accept_len, int32_t *out_commit_ids)
+{
+    t_err.clear();
+    spec_status st = check_verify_args(target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids);
+    if (st != SPEC_OK) return st;
+    if (!(temperature > 0.0) || temperature > 1e30)
+        return fail(SPEC_ERR_ARG, "temperature = %g: must be positive and finite", temperature);
+    if (!(top_p > 0.0 && top_p <= 1.0)) return fail(SPEC_ERR_ARG, "top_p = %g outside (0, 1]", top_p);
+    if (top_k < 1 || top_k > SPEC_MAX_K || (int64_t)top_k > V)
+        return fail(SPEC_ERR_ARG, "top_k = %d outside [1, min(V, %d)]", top_k, SPEC_MAX_K);
+    if (lanes == 0) return SPEC_OK;
+    if (!uniforms || misaligned(uniforms, 8)) return fail(SPEC_ERR_ARG, "uniforms null or misaligned");
+    Sampling smp;
+    smp.top_k = top_k;
+    smp.temperature = temperature;
+    smp.top_p = top_p;
+    smp.uniforms = uniforms;
+    return launch_round(nullptr, 0, 1, 1, nullptr, nullptr, nullptr, target_logits, drafts, lanes, gamma, V,
+                        out_accept_len, out_commit_ids, nullptr, smp);
 }
 
 spec_status spec_verify(const uint16_t *target_logits, const int32_t *drafts, int64_t lanes, int32_t gamma,
@@ -654,6 +689,7 @@ extern "C" spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t 
     a.out_vals = out_vals; a.out_ids = out_ids;
     a.target = target_logits; a.t_cols = t_cols; a.t_V = lanes ? V : 1; a.gamma = gamma;
     a.drafts = drafts; a.out_accept = out_accept_len; a.out_commit = out_commit_ids;
+    a.t_k = 1;   // greedy verify
     // units as in spec_round, fewer if their published lists would not fit
     const Plan plan = plan_round(*d, a, cols ? vectors_of(draft_logits, cols * V) : 0,
                                  lanes ? vectors_of(target_logits, t_cols * V) : 0, false, kNoAllocPartials);

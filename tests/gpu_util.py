@@ -128,3 +128,21 @@ def oracle_topk(x, k, id_map=None):
     if id_map is None:
         return oracle.topk(x, k)
     return oracle.topk_mapped(x, k, id_map)
+
+
+def run_verify_sampled(t_host: np.ndarray, drafts: np.ndarray, temperature: float, top_p: float, top_k: int,
+                       uniforms: np.ndarray, offset: int = 0):
+    import torch
+    sd = sd_module()
+    lanes, gamma = drafts.shape
+    V = t_host.shape[-1]
+    t = dev_u16(t_host, offset)
+    u = torch.from_numpy(np.ascontiguousarray(uniforms, dtype=np.float64)).cuda()
+    acc = Guarded(lanes, torch.int32)
+    com = Guarded(lanes * (gamma + 1), torch.int32)
+    sd.spec_verify_sampled(t, dev_i32(drafts), lanes, gamma, V, temperature, top_p, top_k, u, acc.view, com.view)
+    torch.cuda.synchronize()
+    sd.spec_device_status()
+    acc.check_guards()
+    com.check_guards()
+    return acc.host(), com.host().reshape(lanes, gamma + 1)

@@ -98,3 +98,16 @@ def test_counted_round_checks_counters_alignment(sd):
     st = lib.spec_round_counted(P, 2, 100, 3, P, P, P, P, 1, 2, P, P, P + 4)
     assert st == sd.SPEC_ERR_ARG and "counters misaligned" in sd.spec_last_error()
     assert sd.COUNTER_WORDS == 3 + 2 * sd.SPEC_MAX_GAMMA
+
+
+def test_sampled_verify_argument_checks(sd):
+    lib = sd.lib
+    P = 0x10000   # never dereferenced: every call below fails its checks first
+    for T, p, k, msg in [(0.0, 0.95, 20, "temperature"), (-1.0, 0.95, 20, "temperature"),
+                         (1.0, 0.0, 20, "top_p"), (1.0, 1.5, 20, "top_p"), (1.0, 0.95, 0, "top_k"),
+                         (1.0, 0.95, 65, "top_k"), (1.0, 0.95, 11, "top_k")]:
+        st = lib.spec_verify_sampled(P, P, 1, 2, 10, T, p, k, P, P, P)
+        assert st == sd.SPEC_ERR_ARG and msg in sd.spec_last_error(), (T, p, k)
+    assert lib.spec_verify_sampled(P, P, 1, 2, 100, 1.0, 0.95, 20, None, P, P) == sd.SPEC_ERR_ARG
+    assert lib.spec_verify_sampled(P, P, 1, 2, 100, 1.0, 0.95, 20, P + 4, P, P) == sd.SPEC_ERR_ARG
+    assert lib.spec_verify_sampled(None, None, 0, 2, 100, 1.0, 0.95, 20, None, None, None) == sd.SPEC_OK

@@ -280,6 +280,50 @@ def test_round_counters_accumulate():
     assert sd.read_counters(cnt) == want
 
 
+def _flat_sampled_round(seed: int, lanes: int, gamma: int, V: int):
+    """Target columns of plain N(0,1) noise, each draft one of its column's
+    five best tokens: acceptance is a real coin flip at every position."""
+    from types import SimpleNamespace
+    t = synth._draft_block(seed, lanes * (gamma + 1), V, 1.0)
+    _, ids = oracle.topk(t, 5)
+    pick = synth.rng(seed, 1).integers(0, 5, size=(lanes, gamma))
+    drafts = np.array([[ids[l * (gamma + 1) + j, pick[l, j]] for j in range(gamma)] for l in range(lanes)],
+                      dtype=np.int32)
+    return SimpleNamespace(target=t.reshape(lanes, gamma + 1, V), drafts=drafts, lanes=lanes, gamma=gamma)
+
+
+@pytest.mark.parametrize("temperature,top_p,top_k", [(1.0, 0.95, 20), (0.7, 0.9, 8), (1.5, 1.0, 64), (2.0, 0.5, 33)])
+def test_sampled_verify(temperature, top_p, top_k):
+    """spec_verify_sampled against the oracle, bit-exact, on seeded rounds
+    whose accept/draw decisions all lie well clear of a boundary (both sides
+    compute in float64; exp may differ in the last place)."""
+    cases = [(synth.make_c1(seed=51, V=30_000), 0), (synth.make_c2(seed=52, V=20_003), 3),
+             (synth.make_c3(seed=53, V=10_001), 5), (_flat_sampled_round(55, 12, 5, 40_000), 1)]
+    for i, (r, off) in enumerate(cases):
+        u = synth.rng(900 + i, int(top_k)).random((r.lanes, r.gamma + 1, 2))
+        wa, wc, margin = oracle.sampled_verify(r.target, r.drafts, temperature, top_p, top_k, u)
+        assert margin > 1e-9, margin
+        got = gu.run_verify_sampled(r.target, r.drafts, temperature, top_p, top_k, u, offset=off)
+        gu.assert_verify_equal(got, (wa, wc), f"sampled T={temperature} top_p={top_p} top_k={top_k} case {i}")
+
+
+def test_sampled_verify_full_vocabulary():
+    """The pages' sampled setting (T 1.0, top_p 0.95, top_k 20) on the C2
+    verify part at V = 248,046."""
+    r = synth.make_c2()
+    u = synth.rng(950, 0).random((r.lanes, r.gamma + 1, 2))
+    wa, wc, margin = oracle.sampled_verify(r.target, r.drafts, 1.0, 0.95, 20, u)
+    assert margin > 1e-9
+    gu.assert_verify_equal(gu.run_verify_sampled(r.target, r.drafts, 1.0, 0.95, 20, u), (wa, wc), "sampled C2")
+
+
+def test_sampled_top_k_one_is_greedy():
+    r = synth.make_c3(seed=54, V=7_777)
+    u = synth.rng(960, 0).random((r.lanes, r.gamma + 1, 2))
+    gu.assert_verify_equal(gu.run_verify_sampled(r.target, r.drafts, 0.8, 0.95, 1, u),
+                           oracle.verify(r.target, r.drafts), "sampled top_k=1")
+
+
 def test_empty_and_rejected_calls_write_nothing():
     import torch
     sd = gu.sd_module()
