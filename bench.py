@@ -65,6 +65,9 @@ def parse_args(argv=None):
     p.add_argument("--k", type=int, default=None, help="k for C5 (1, 8, 20 or 64)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--sampled", action="store_true",
+                   help="verify by speculative sampling (T 1.0, top_p 0.95, top_k 20, one-hot drafts; "
+                        "spec_round_sampled) instead of greedy; measures the kernel line only (no e2e, no CPU arm)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args(argv)
 
@@ -315,7 +318,10 @@ def workload_config(args, r, ring):
     if ring is not None:
         c["l2"] = (f"inputs rotated through a ring of {ring[0]} copies ({ring[1] / 1e6:.0f} MB, > 4x the "
                    f"{ring[2] / 1e6:.0f} MB L2): every round reads its logits from HBM")
-        c["launch"] = "spec_round: one kernel per round; K rounds replayed as CUDA graphs"
+        c["launch"] = ("spec_round_sampled" if args.sampled else "spec_round") + \
+            ": one kernel per round; K rounds replayed as CUDA graphs"
+    if args.sampled:
+        c["verify"] = "sampled: T 1.0, top_p 0.95, top_k 20, one-hot drafts, seeded uniforms"
     return c
 
 
@@ -349,8 +355,15 @@ def run_ours(args):
     sd.spec_reserve(cols, k, lanes, gamma)
     stream = torch.cuda.Stream(device=dev)
 
-    def one(i):
-        sd.spec_round(xs[i % R], cols, V, k, vals, ids, ts[i % R], drafts, lanes, gamma, acc, com)
+    if args.sampled:
+        uni = torch.from_numpy(np.random.default_rng(12345 + rank).random((max(lanes, 1), gamma + 1, 2))).to(dev)
+
+        def one(i):
+            sd.spec_round_sampled(xs[i % R], cols, V, k, vals, ids, ts[i % R], drafts, lanes, gamma,
+                                  1.0, 0.95, 20, uni, acc, com)
+    else:
+        def one(i):
+            sd.spec_round(xs[i % R], cols, V, k, vals, ids, ts[i % R], drafts, lanes, gamma, acc, com)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -398,7 +411,7 @@ def run_ours(args):
 
     # end to end through the host-buffer entry point
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.sampled:
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
         hd = pin(r.draft.view(np.int16))
         ht = pin(r.target.view(np.int16)) if lanes else None
@@ -456,7 +469,7 @@ def run_ours(args):
     }
     if e2e:
         line["e2e"] = e2e
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not args.sampled:
         line["cpu_baseline"] = cpu_baseline(r)
     print(json.dumps(line), flush=True)
     return 0

@@ -6,11 +6,11 @@
  *
  *   top-k   section "How it works", third paragraph: for each draft column,
  *           keep the k largest bf16 logits, largest first, ties going to
- *           the smaller row (token) id.  The kernel splits the vocabulary
- *           axis of every column across CTAs, filters 16-byte vectors
- *           against a running k-th value held in registers, and merges the
- *           per-CTA lists in the last CTA to finish a column -- the logits
- *           are read from HBM exactly once.
+ *           the smaller row (token) id.  One launch streams the logits
+ *           once: every CTA (or warp) of a full-GPU grid takes an equal
+ *           slice of the flat run of columns, filters 16-byte vectors against
+ *           a certified running k-th value, and the unit that completes a
+ *           split column merges the published lists (spec_set_kernel).
  *
  *   verify  section "How it works", first paragraph: a verify round runs
  *           every lane's anchor plus its drafts through the target model
@@ -137,6 +137,15 @@ spec_status spec_verify_sampled(const uint16_t *target_logits, const int32_t *dr
                                 int32_t gamma, int64_t V, double temperature, double top_p,
                                 int32_t top_k, const double *uniforms, int32_t *out_accept_len,
                                 int32_t *out_commit_ids);
+
+/* spec_round with sampled verify: spec_topk over the draft columns and
+ * spec_verify_sampled over the target columns in ONE launch, same V. */
+spec_status spec_round_sampled(const uint16_t *draft_logits, int64_t cols, int64_t V, int32_t k,
+                               uint16_t *out_vals, int32_t *out_ids,
+                               const uint16_t *target_logits, const int32_t *drafts, int64_t lanes,
+                               int32_t gamma, double temperature, double top_p, int32_t top_k,
+                               const double *uniforms, int32_t *out_accept_len,
+                               int32_t *out_commit_ids);
 
 /* One whole selection step in ONE kernel launch: spec_topk over the draft
  * columns and spec_verify_v over the target columns, same vocabulary V.

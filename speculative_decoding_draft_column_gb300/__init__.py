@@ -21,7 +21,7 @@ __all__ = [
     "SPEC_OK", "SPEC_ERR_ARG", "SPEC_ERR_ALLOC", "SPEC_ERR_CUDA", "SPEC_VOCAB", "SPEC_MAX_K",
     "SPEC_MAX_GAMMA", "SpecError", "LIB_PATH", "lib",
     "spec_topk", "spec_topk_mapped", "spec_verify", "spec_verify_v", "spec_round", "spec_round_host",
-    "spec_round_noalloc", "spec_round_counted", "spec_verify_sampled", "new_counters", "read_counters", "COUNTER_WORDS",
+    "spec_round_noalloc", "spec_round_counted", "spec_verify_sampled", "spec_round_sampled", "new_counters", "read_counters", "COUNTER_WORDS",
     "spec_set_kernel", "spec_get_kernel", "SPEC_KERNEL_AUTO", "SPEC_KERNEL_WARP", "SPEC_KERNEL_CTA",
     "spec_set_stream", "spec_get_stream", "spec_reserve", "spec_release", "spec_last_error",
     "spec_launch_count", "spec_device_status", "topk", "topk_mapped", "verify", "round_step", "EXPORTS",
@@ -49,6 +49,8 @@ _SIGS = {
     "spec_round_noalloc": [_p, _i64, _i64, _i32, _p, _p, _p, _p, _i64, _i32, _p, _p],
     "spec_round_counted": [_p, _i64, _i64, _i32, _p, _p, _p, _p, _i64, _i32, _p, _p, _p],
     "spec_verify_sampled": [_p, _p, _i64, _i32, _i64, ctypes.c_double, ctypes.c_double, _i32, _p, _p, _p],
+    "spec_round_sampled": [_p, _i64, _i64, _i32, _p, _p, _p, _p, _i64, _i32, ctypes.c_double, ctypes.c_double, _i32,
+                           _p, _p, _p],
     "spec_set_kernel": [_i32],
     "spec_get_kernel": [],
     "spec_set_stream": [_p],
@@ -143,6 +145,15 @@ def spec_verify_sampled(target_logits, drafts, lanes, gamma, V, temperature, top
     _use_torch_stream()
     _check(lib.spec_verify_sampled(_ptr(target_logits), _ptr(drafts), lanes, gamma, V, float(temperature),
                                    float(top_p), top_k, _ptr(uniforms), _ptr(out_accept_len), _ptr(out_commit_ids)))
+
+
+def spec_round_sampled(draft_logits, cols, V, k, out_vals, out_ids, target_logits, drafts, lanes, gamma,
+                       temperature, top_p, top_k, uniforms, out_accept_len, out_commit_ids):
+    """spec_round with sampled verify, one launch."""
+    _use_torch_stream()
+    _check(lib.spec_round_sampled(_ptr(draft_logits), cols, V, k, _ptr(out_vals), _ptr(out_ids),
+                                  _ptr(target_logits), _ptr(drafts), lanes, gamma, float(temperature), float(top_p),
+                                  top_k, _ptr(uniforms), _ptr(out_accept_len), _ptr(out_commit_ids)))
 
 
 COUNTER_WORDS = 3 + 2 * SPEC_MAX_GAMMA   # uint64 words of a spec_counters block

@@ -422,6 +422,39 @@ spec_status spec_verify_v(const uint16_t *target_logits, const int32_t *drafts, 
                         out_accept_len, out_commit_ids);
 }
 
+spec_status check_sampling(double temperature, double top_p, int32_t top_k, int64_t V, int64_t lanes,
+                           const double *uniforms)
+{
+    if (!(temperature > 0.0) || temperature > 1e30)
+        return fail(SPEC_ERR_ARG, "temperature = %g: must be positive and finite", temperature);
+    if (!(top_p > 0.0 && top_p <= 1.0)) return fail(SPEC_ERR_ARG, "top_p = %g outside (0, 1]", top_p);
+    if (top_k < 1 || top_k > SPEC_MAX_K || (int64_t)top_k > V)
+        return fail(SPEC_ERR_ARG, "top_k = %d outside [1, min(V, %d)]", top_k, SPEC_MAX_K);
+    if (lanes > 0 && (!uniforms || misaligned(uniforms, 8))) return fail(SPEC_ERR_ARG, "uniforms null or misaligned");
+    return SPEC_OK;
+}
+
+spec_status spec_round_sampled(const uint16_t *draft_logits, int64_t cols, int64_t V, int32_t k, uint16_t *out_vals,
+                               int32_t *out_ids, const uint16_t *target_logits, const int32_t *drafts, int64_t lanes,
+                               int32_t gamma, double temperature, double top_p, int32_t top_k,
+                               const double *uniforms, int32_t *out_accept_len, int32_t *out_commit_ids)
+{
+    t_err.clear();
+    spec_status st = check_topk_args(draft_logits, cols, V, k, out_vals, out_ids);
+    if (st != SPEC_OK) return st;
+    st = check_verify_args(target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids);
+    if (st != SPEC_OK) return st;
+    st = check_sampling(temperature, top_p, top_k, V, lanes, uniforms);
+    if (st != SPEC_OK) return st;
+    Sampling smp;
+    smp.top_k = top_k;
+    smp.temperature = temperature;
+    smp.top_p = top_p;
+    smp.uniforms = uniforms;
+    return launch_round(draft_logits, cols, V, k, nullptr, out_vals, out_ids, target_logits, drafts, lanes, gamma,
+                        V, out_accept_len, out_commit_ids, nullptr, smp);
+}
+
 spec_status spec_verify_sampled(const uint16_t *target_logits, const int32_t *drafts, int64_t lanes, int32_t gamma,
                                 int64_t V, double temperature, double top_p, int32_t top_k, const double *uniforms,
                                 int32_t *out_accept_len, int32_t *out_commit_ids)
@@ -429,13 +462,9 @@ spec_status spec_verify_sampled(const uint16_t *target_logits, const int32_t *dr
     t_err.clear();
     spec_status st = check_verify_args(target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids);
     if (st != SPEC_OK) return st;
-    if (!(temperature > 0.0) || temperature > 1e30)
-        return fail(SPEC_ERR_ARG, "temperature = %g: must be positive and finite", temperature);
-    if (!(top_p > 0.0 && top_p <= 1.0)) return fail(SPEC_ERR_ARG, "top_p = %g outside (0, 1]", top_p);
-    if (top_k < 1 || top_k > SPEC_MAX_K || (int64_t)top_k > V)
-        return fail(SPEC_ERR_ARG, "top_k = %d outside [1, min(V, %d)]", top_k, SPEC_MAX_K);
+    st = check_sampling(temperature, top_p, top_k, V, lanes, uniforms);
+    if (st != SPEC_OK) return st;
     if (lanes == 0) return SPEC_OK;
-    if (!uniforms || misaligned(uniforms, 8)) return fail(SPEC_ERR_ARG, "uniforms null or misaligned");
     Sampling smp;
     smp.top_k = top_k;
     smp.temperature = temperature;

@@ -317,6 +317,28 @@ def test_sampled_verify_full_vocabulary():
     gu.assert_verify_equal(gu.run_verify_sampled(r.target, r.drafts, 1.0, 0.95, 20, u), (wa, wc), "sampled C2")
 
 
+def test_round_sampled_is_topk_plus_sampled_verify():
+    import torch
+    sd = gu.sd_module()
+    r = synth.make_c2(seed=56, V=30_011)
+    u = synth.rng(970, 0).random((r.lanes, r.gamma + 1, 2))
+    x, t = gu.dev_u16(r.draft), gu.dev_u16(r.target, 2)
+    vals = torch.empty((r.cols, r.k), dtype=torch.int16, device="cuda")
+    ids = torch.empty((r.cols, r.k), dtype=torch.int32, device="cuda")
+    acc = torch.empty(r.lanes, dtype=torch.int32, device="cuda")
+    com = torch.empty((r.lanes, r.gamma + 1), dtype=torch.int32, device="cuda")
+    ut = torch.from_numpy(u).cuda()
+    sd.spec_round_sampled(x, r.cols, r.V, r.k, vals, ids, t, gu.dev_i32(r.drafts), r.lanes, r.gamma, 1.0, 0.95, 20,
+                          ut, acc, com)
+    torch.cuda.synchronize()
+    sd.spec_device_status()
+    gu.assert_topk_equal((vals.cpu().numpy().view(np.uint16), ids.cpu().numpy()), oracle.topk(r.draft, r.k),
+                         "round_sampled top-k")
+    wa, wc, margin = oracle.sampled_verify(r.target, r.drafts, 1.0, 0.95, 20, u)
+    assert margin > 1e-9
+    gu.assert_verify_equal((acc.cpu().numpy(), com.cpu().numpy()), (wa, wc), "round_sampled verify")
+
+
 def test_sampled_top_k_one_is_greedy():
     r = synth.make_c3(seed=54, V=7_777)
     u = synth.rng(960, 0).random((r.lanes, r.gamma + 1, 2))
