@@ -132,7 +132,8 @@ spec_status spec_verify_v(const uint16_t *target_logits, const int32_t *drafts, 
  *   out_accept_len, out_commit_ids as for spec_verify: the accepted drafts,
  *   then the draw, then -1.
  * With top_k = 1 this is exactly spec_verify_v.  One launch; target logits
- * are read once. */
+ * are read once.  A column whose best value is +-Inf has no softmax: such
+ * columns (like NaN) are outside this call's contract. */
 spec_status spec_verify_sampled(const uint16_t *target_logits, const int32_t *drafts, int64_t lanes,
                                 int32_t gamma, int64_t V, double temperature, double top_p,
                                 int32_t top_k, const double *uniforms, int32_t *out_accept_len,

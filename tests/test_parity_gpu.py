@@ -339,6 +339,23 @@ def test_round_sampled_is_topk_plus_sampled_verify():
     gu.assert_verify_equal((acc.cpu().numpy(), com.cpu().numpy()), (wa, wc), "round_sampled verify")
 
 
+def test_sampled_verify_small_and_tied():
+    """Tiny vocabularies (top_k = V), all-tied columns (a uniform q: every
+    draw walks the id order) and ragged phases."""
+    for V, gamma, lanes in ((1, 1, 3), (2, 3, 5), (5, 4, 7), (17, 15, 2)):
+        t = synth._draft_block(70 + V, lanes * (gamma + 1), V, 1.0)
+        t[::3] = synth.bf16_bits(0.5)                           # every third column all tied
+        drafts = synth.rng(71 + V, 0).integers(-1, V + 1, size=(lanes, gamma)).astype(np.int32)
+        u = synth.rng(72 + V, 0).random((lanes, gamma + 1, 2))
+        for top_k, top_p in ((V, 1.0), (max(1, V // 2), 0.8), (1, 0.95)):
+            wa, wc, margin = oracle.sampled_verify(t, drafts, 1.0, top_p, top_k, u)
+            if margin <= 1e-9:
+                continue   # a decision on a boundary: float64 exp may round either way
+            got = gu.run_verify_sampled(t.reshape(lanes, gamma + 1, V), drafts, 1.0, top_p, top_k, u,
+                                        offset=(V + gamma) % 8)
+            gu.assert_verify_equal(got, (wa, wc), f"sampled V={V} gamma={gamma} top_k={top_k} top_p={top_p}")
+
+
 def test_sampled_top_k_one_is_greedy():
     r = synth.make_c3(seed=54, V=7_777)
     u = synth.rng(960, 0).random((r.lanes, r.gamma + 1, 2))
