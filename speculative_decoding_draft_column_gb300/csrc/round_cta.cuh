@@ -180,18 +180,48 @@ __device__ __noinline__ int finish_column(const RoundArgs &a, const Run &r, int 
     unsigned long long *mine = list_slot(a, r, w, c);
     for (int i = lane; i < n; i += 32) mine[i] = lst[i];
     if (lane == 0) mine[kk] = (unsigned long long)n;
-    __threadfence();
     __syncwarp();
+    // the ticket: release (the list above is visible first) and acquire
+    // (every earlier list is visible to the last) in one atomic
     const int64_t tix = r.draft ? c : a.d_cols + c;
     unsigned last = 0;
-    if (lane == 0) last = atomicAdd(a.col_ticket + tix, 1u) == (unsigned)(wl - wf);
+    if (lane == 0) last = atom_add_acq_rel(a.col_ticket + tix, 1u) == (unsigned)(wl - wf);
     if (!__shfl_sync(kFull, last, 0)) return 0;
-    __threadfence();
-    // merge every slice's list, 32 lists at a time, 32 entries per step.  The
-    // best certificate of a full list (its kk-th key) bounds the column's
-    // kk-th key: entries below it are left out.
+    __syncwarp();
+    // merge every slice's list.  The best certificate of a full list (its
+    // kk-th key) bounds the column's kk-th key: entries below it are left
+    // out.
     n = 0;
     const int64_t nparts = wl - wf + 1;
+    if (nparts <= 32 && nparts * kk <= 128) {
+        // few short lists: lengths, certificates and every list slot in one
+        // round of loads, four slots a lane
+        const unsigned long long *mylist = lane < nparts ? list_slot(a, r, wf + lane, c) : nullptr;
+        const int len = mylist ? (int)__ldcg(mylist + kk) : 0;
+        const unsigned long long lastv = mylist ? __ldcg(mylist + kk - 1) : 0ull;
+        unsigned long long ent[4];
+        int slot[4], from[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int g = lane + 32 * i;
+            from[i] = g < nparts * kk ? g / kk : 0;
+            slot[i] = g - from[i] * kk;
+            const unsigned long long *src = reinterpret_cast<const unsigned long long *>(
+                __shfl_sync(kFull, reinterpret_cast<uintptr_t>(mylist), from[i]));
+            ent[i] = g < nparts * kk ? __ldcg(src + slot[i]) : 0ull;
+        }
+        const uint32_t cert = __reduce_max_sync(kFull, len == kk ? entry_key(lastv) : 0u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int lq = __shfl_sync(kFull, len, from[i]);
+            unsigned long long e = slot[i] < lq ? ent[i] : 0ull;   // slots past a list's length are stale
+            if (entry_key(e) < cert || (n == kk && e < lst[kk - 1])) e = 0ull;
+            n = list_merge32(lst, n, e, kk, lane);
+        }
+        emit_column(a, r, c, lst, n, lane);
+        if (lane == 0) a.col_ticket[tix] = 0u;   // ready for the next launch
+        return 0;
+    }
     for (int64_t q0 = 0; q0 < nparts; q0 += 32) {
         const unsigned long long *mylist = q0 + lane < nparts ? list_slot(a, r, wf + q0 + lane, c) : nullptr;
         const int len = mylist ? (int)__ldcg(mylist + kk) : 0;
