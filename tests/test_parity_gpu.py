@@ -363,6 +363,31 @@ def test_sampled_top_k_one_is_greedy():
                            oracle.verify(r.target, r.drafts), "sampled top_k=1")
 
 
+@pytest.mark.parametrize("k", [1, 8, 64])
+def test_column_over_many_units(k):
+    """One column of a million logits: about 120 CTAs (or 240 warps) share
+    it, so the completing unit merges lists more than 32 at a time."""
+    V = 1_000_000
+    x = synth._draft_block(80 + k, 1, V, 3.0)
+    gu.assert_topk_equal(gu.run_topk(x, k, offset=3), oracle.topk(x, k), f"one column V={V} k={k}")
+
+
+def test_verify_columns_over_many_units():
+    """A lane of four target columns of a million logits each (greedy and
+    sampled): every column is shared by dozens of units."""
+    V, gamma = 1_000_000, 3
+    t = synth._draft_block(90, gamma + 1, V, 1.0)
+    _, ids = oracle.topk(t, 3)
+    drafts = np.array([[ids[0, 0], ids[1, 0], ids[2, 1]]], dtype=np.int32)
+    gu.assert_verify_equal(gu.run_verify(t.reshape(1, gamma + 1, V), drafts), oracle.verify(t, drafts),
+                           "verify V=1e6")
+    u = synth.rng(91, 0).random((1, gamma + 1, 2))
+    wa, wc, margin = oracle.sampled_verify(t, drafts, 1.0, 0.95, 20, u)
+    assert margin > 1e-9
+    gu.assert_verify_equal(gu.run_verify_sampled(t.reshape(1, gamma + 1, V), drafts, 1.0, 0.95, 20, u),
+                           (wa, wc), "sampled V=1e6")
+
+
 def test_empty_and_rejected_calls_write_nothing():
     import torch
     sd = gu.sd_module()
