@@ -247,7 +247,8 @@ void *spec_get_stream(void);
 /* Make sure the current device's scratch covers calls up to these sizes
  * (so that later calls need no allocation, e.g. inside a CUDA graph
  * capture).  max_cols counts draft columns, max_lanes/max_gamma the verify
- * part.  Synchronises the device if it has to reallocate. */
+ * part; max_k is the largest k -- or sampled-verify top_k -- to come.
+ * Synchronises the device if it has to reallocate. */
 spec_status spec_reserve(int64_t max_cols, int32_t max_k, int64_t max_lanes, int32_t max_gamma);
 
 /* Free the scratch and staging of the current device (after synchronising
