@@ -202,6 +202,12 @@ __device__ __forceinline__ uint32_t ld_relaxed(const unsigned int *p)
     return v;
 }
 
+// Programmatic dependent launch: let the next launch on the stream be
+// scheduled now (its CTAs still wait below for this grid to finish), and
+// wait for the previous launch to finish and flush before touching memory.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- mbarrier / bulk-copy primitives (inline PTX, sm_90+) -------------------
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }

@@ -615,6 +615,8 @@ __device__ __forceinline__ void stream_slice(const RoundArgs &a, const Run &r, i
 
 __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_constant__ RoundArgs a)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     extern __shared__ __align__(128) unsigned char smem[];
     CtaSmem &s = *reinterpret_cast<CtaSmem *>(smem);
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;

@@ -267,17 +267,42 @@ Plan plan_round(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, 
 // Partial-list entries a plan needs (two lists per unit).
 int64_t plan_partials(const RoundArgs &a) { return ((int64_t)a.d_units + a.t_units) * 2 * a.pstride; }
 
-void launch_plan(const Plan &p, const RoundArgs &a, cudaStream_t stream)
+// Launch, with programmatic stream serialization when pdl: the kernel
+// signals its dependents at entry and waits for its predecessor before any
+// memory access, so the stream order holds while the next launch's setup
+// overlaps the current launch's tail.
+template <typename K>
+cudaError_t launch_pdl(K kernel, unsigned grid, unsigned block, size_t smem, cudaStream_t stream, const RoundArgs &a,
+                       bool pdl)
 {
-    if (p.per_cta) {
-        cta::spec_round_kernel<<<(unsigned)p.grid, cta::kThreads, cta::kSmemBytes, stream>>>(a);
-        return;
-    }
-    const dim3 grid((unsigned)p.grid), block(wrp::kThreads);
-    if (p.slots == 1 && !p.mapped) wrp::spec_round_kernel<1, false><<<grid, block, wrp::kSmemBytes, stream>>>(a);
-    else if (p.slots == 1) wrp::spec_round_kernel<1, true><<<grid, block, wrp::kSmemBytes, stream>>>(a);
-    else if (!p.mapped) wrp::spec_round_kernel<2, false><<<grid, block, wrp::kSmemBytes, stream>>>(a);
-    else wrp::spec_round_kernel<2, true><<<grid, block, wrp::kSmemBytes, stream>>>(a);
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+// pdl: whether a CTA-kernel launch may overlap the stream's previous kernel
+// (off when a non-kernel operation the kernel depends on comes right before
+// it).  Only the CTA kernel -- small, launch-bound rounds -- uses it; it
+// measured slower for the per-warp kernel's large rounds.
+cudaError_t launch_plan(const Plan &p, const RoundArgs &a, cudaStream_t stream, bool pdl = true)
+{
+    const unsigned g = (unsigned)p.grid;
+    if (p.per_cta) return launch_pdl(cta::spec_round_kernel, g, cta::kThreads, cta::kSmemBytes, stream, a, pdl);
+    const unsigned b = wrp::kThreads;
+    const size_t m = wrp::kSmemBytes;
+    if (p.slots == 1 && !p.mapped) return launch_pdl(wrp::spec_round_kernel<1, false>, g, b, m, stream, a, false);
+    if (p.slots == 1) return launch_pdl(wrp::spec_round_kernel<1, true>, g, b, m, stream, a, false);
+    if (!p.mapped) return launch_pdl(wrp::spec_round_kernel<2, false>, g, b, m, stream, a, false);
+    return launch_pdl(wrp::spec_round_kernel<2, true>, g, b, m, stream, a, false);
 }
 
 bool misaligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
@@ -355,8 +380,7 @@ spec_status launch_round(const uint16_t *draft, int64_t cols, int64_t V, int32_t
     a.col_ticket = sp.col_ticket;
     a.col_cert = sp.col_ticket + (cols + t_cols);
     a.lane_ticket = sp.lane_ticket;
-    launch_plan(plan, a, stream);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_plan(plan, a, stream);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return SPEC_OK;
@@ -732,8 +756,7 @@ extern "C" spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t 
     // the array keeps whatever the last call left: start every ticket at zero
     cudaError_t e = cudaMemsetAsync(base, 0, kNoAllocTicketBytes, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch tickets)");
-    launch_plan(plan, a, stream);
-    e = cudaGetLastError();
+    e = launch_plan(plan, a, stream, false);   // right after the ticket clear
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return SPEC_OK;
