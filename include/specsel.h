@@ -255,6 +255,15 @@ spec_status spec_reserve(int64_t max_cols, int32_t max_k, int64_t max_lanes, int
  * it).  Later calls allocate again. */
 spec_status spec_release(void);
 
+/* Diagnostic of the bounded waits every kernel uses on its copy pipeline:
+ * launches (on the calling thread's stream) one thread that waits on an
+ * mbarrier nothing arrives on, for at most limit_ns (1 us .. 1 s), then
+ * waits on it once more.  The first wait gives up and raises the flag that
+ * spec_device_status reports; the second returns at once (a CTA whose wait
+ * gave up waits no more).  out4: device uint64[4] = {first wait succeeded
+ * (0), its ns, second wait succeeded (0), its ns}.  No fault, no hang. */
+spec_status spec_selftest_wait_timeout(int64_t limit_ns, uint64_t *out4);
+
 /* Text of the last error raised on the calling thread ("" if none). */
 const char *spec_last_error(void);
 

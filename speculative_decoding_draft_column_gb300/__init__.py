@@ -60,6 +60,7 @@ _SIGS = {
     "spec_last_error": [],
     "spec_launch_count": [],
     "spec_device_status": [],
+    "spec_selftest_wait_timeout": [_i64, _p],
 }
 EXPORTS = tuple(_SIGS)
 for _name, _args in _SIGS.items():

@@ -250,22 +250,23 @@ __device__ __forceinline__ uint64_t global_ns()
 __shared__ unsigned int s_gave_up;
 
 // Wait for the phase with the given parity to complete, for at most
-// kWaitLimitNs of wall time; on giving up, flag the error and report false
-// (the data is then garbage, but the kernel still terminates).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+// limit_ns of wall time; on giving up, flag the error and report false (the
+// data is then garbage, but the kernel still terminates).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*reinterpret_cast<volatile unsigned int *>(&s_gave_up)) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             s_gave_up = 1u;
             atomicOr(&g_wait_timeouts, 1u);
             return false;
         }
     }
 }
+
 
 // One bulk copy global -> shared, completing on `bar` with its byte count.
 // src, dst 16-byte aligned, bytes a multiple of 16.
@@ -547,6 +548,28 @@ __device__ __noinline__ void sampled_column_done(const RoundArgs &a, int64_t c, 
         a.out_accept[ln] = acc;
         a.lane_ticket[ln] = 0u;   // ready for the next launch
     }
+}
+
+// Diagnostic of the bounded waits: one thread waits on an mbarrier that
+// nothing arrives on (limit limit_ns), then once more on the same phase; the
+// first wait must give up and flag, the second return at once.  Writes the
+// two results and their durations to out[0..3].
+__global__ void wait_timeout_probe(uint64_t limit_ns, unsigned long long *out)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    s_gave_up = 0u;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    const uint64_t t0 = global_ns();
+    const bool first = mbar_wait(&bar, 0, limit_ns);
+    const uint64_t t1 = global_ns();
+    const bool second = mbar_wait(&bar, 0, limit_ns);
+    const uint64_t t2 = global_ns();
+    out[0] = first;
+    out[1] = t1 - t0;
+    out[2] = second;
+    out[3] = t2 - t1;
 }
 
 }  // namespace

@@ -643,6 +643,17 @@ const char *spec_last_error(void) { return t_err.c_str(); }
 
 int64_t spec_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+spec_status spec_selftest_wait_timeout(int64_t limit_ns, uint64_t *out4)
+{
+    t_err.clear();
+    if (limit_ns < 1000 || limit_ns > 1000000000) return fail(SPEC_ERR_ARG, "limit_ns outside [1 us, 1 s]");
+    if (!out4 || misaligned(out4, 8)) return fail(SPEC_ERR_ARG, "out4 null or misaligned");
+    wait_timeout_probe<<<1, 32, 0, t_stream>>>((uint64_t)limit_ns, reinterpret_cast<unsigned long long *>(out4));
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return SPEC_OK;
+}
+
 spec_status spec_device_status(void)
 {
     t_err.clear();

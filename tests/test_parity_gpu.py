@@ -448,3 +448,22 @@ def test_round_host_buffers():
     sd.spec_round_host(r.draft, r.cols, r.V, r.k, vals, ids, r.target, r.drafts, r.lanes, r.gamma, acc, com)
     gu.assert_topk_equal((vals, ids), oracle.topk(r.draft, r.k), "host buffers")
     gu.assert_verify_equal((acc, com), oracle.verify(r.target, r.drafts), "host buffers")
+
+
+def test_bounded_wait_gives_up_and_is_reported(kernel):
+    """Failure detection without a fault: a wait on a barrier nothing
+    arrives on gives up after its limit, the device flag is reported once
+    by spec_device_status, and the CTA's next wait returns at once."""
+    import torch
+    sd = gu.sd_module()
+    sd.spec_device_status()                        # nothing pending
+    out = torch.zeros(4, dtype=torch.int64, device="cuda")
+    sd._check(sd.lib.spec_selftest_wait_timeout(2_000_000, out.data_ptr()))   # 2 ms
+    torch.cuda.synchronize()
+    first_ok, first_ns, second_ok, second_ns = (int(v) for v in out.cpu())
+    assert first_ok == 0 and first_ns >= 2_000_000
+    assert second_ok == 0 and second_ns < 1_000_000
+    with pytest.raises(sd.SpecError) as ei:
+        sd.spec_device_status()
+    assert "gave up a bounded wait" in str(ei.value)
+    sd.spec_device_status()                        # cleared by the report
