@@ -65,6 +65,8 @@ def parse_args(argv=None):
     p.add_argument("--k", type=int, default=None, help="k for C5 (1, 8, 20 or 64)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--kernel", default="auto", choices=["auto", "warp", "cta"],
+                   help="streaming kernel (spec_set_kernel); auto picks by round size")
     p.add_argument("--sampled", action="store_true",
                    help="verify by speculative sampling (T 1.0, top_p 0.95, top_k 20, one-hot drafts; "
                         "spec_round_sampled) instead of greedy; measures the kernel line only (no e2e, no CPU arm)")
@@ -95,12 +97,14 @@ def source_hash() -> str:
 
 
 # The library runs a round on its CTA-cooperative kernel while the round's
-# logits are at most 1 MiB per SM and on its per-warp kernel above (the
-# automatic choice of spec_set_kernel); the bench only names the one that ran.
-CTA_MAX_BYTES_PER_SM = 1 << 20
+# logits are at most 6 MiB per SM and on its per-warp kernel above (the
+# automatic choice of spec_set_kernel); the bench names the one that ran.
+CTA_MAX_BYTES_PER_SM = 6 << 20
 
 
-def kernel_name(bytes_round: int, sms: int) -> str:
+def kernel_name(bytes_round: int, sms: int, forced: str = "auto") -> str:
+    if forced != "auto":
+        return "cta::spec_round_kernel" if forced == "cta" else "wrp::spec_round_kernel"
     return "cta::spec_round_kernel" if bytes_round <= CTA_MAX_BYTES_PER_SM * sms else "wrp::spec_round_kernel"
 
 
@@ -352,6 +356,7 @@ def run_ours(args):
     ids = torch.empty((cols, k), dtype=torch.int32, device=dev)
     acc = torch.empty(max(lanes, 1), dtype=torch.int32, device=dev)
     com = torch.empty((max(lanes, 1), gamma + 1), dtype=torch.int32, device=dev)
+    sd.spec_set_kernel({"auto": sd.SPEC_KERNEL_AUTO, "warp": sd.SPEC_KERNEL_WARP, "cta": sd.SPEC_KERNEL_CTA}[args.kernel])
     sd.spec_reserve(cols, k, lanes, gamma)
     stream = torch.cuda.Stream(device=dev)
 
@@ -457,7 +462,8 @@ def run_ours(args):
         "pct_of_hbm_peak": round(100 * gbs / world / peak, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; see synth/)",
         "config": workload_config(args, r, (R, R * bytes_round, l2)),
-        "roofline": {"bound": "hbm", "kernel": kernel_name(bytes_round, torch.cuda.get_device_properties(dev).multi_processor_count),
+        "roofline": {"bound": "hbm", "kernel": kernel_name(bytes_round, torch.cuda.get_device_properties(dev).multi_processor_count,
+                                                        args.kernel),
                      "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "traffic": recorded_traffic(args.config), "algorithmic_bytes_per_launch": bytes_round,

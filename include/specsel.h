@@ -225,13 +225,13 @@ spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t cols, int64
  *   SPEC_KERNEL_CTA  -- the CTAs of a full-GPU grid each stream a contiguous
  *                       slice in 60 KiB chunks; per column one threshold per
  *                       CTA (the k-th best the CTA has seen), kept by a
- *                       merging warp.  Fastest while each SM streams little
- *                       (rounds of up to ~150 MB of logits).
+ *                       merging warp.  Fastest while each SM streams a few
+ *                       columns at most (rounds of up to ~950 MB of logits).
  *   SPEC_KERNEL_WARP -- every warp streams its own slice with its own ring,
  *                       buffer and threshold; no coordination inside the
  *                       stream.  Fastest for large rounds.
  *   SPEC_KERNEL_AUTO -- (default) CTA while the round's logits are at most
- *                       1 MiB per SM, WARP above.
+ *                       6 MiB per SM, WARP above.
  * The choice is process-wide; SPEC_ERR_ARG for any other value. */
 #define SPEC_KERNEL_AUTO 0
 #define SPEC_KERNEL_WARP 1

@@ -39,11 +39,12 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 // Kernel choice.  The CTA-cooperative kernel keeps one threshold per column
-// per CTA and wins while an SM streams little of each column; the per-warp
+// per CTA and wins while an SM streams a few columns at most; the per-warp
 // kernel has no coordination inside the stream and wins once every warp sees
-// megabytes.  The crossover measured on GB300 lies between 0.1 and 3 MB of
-// logits per SM; the switch is at 1 MB.
-constexpr int64_t kCtaMaxBytesPerSm = 1 << 20;
+// megabytes.  Measured on GB300 (graph-replayed rounds, k = 8 and 20): the
+// CTA kernel is ahead up to 6.3 MB of logits per SM (219 against 225 us),
+// behind at 26 MB per SM (850 against 696 us); the switch is at 6 MiB.
+constexpr int64_t kCtaMaxBytesPerSm = 6ll << 20;
 std::atomic<int> g_kernel_choice{SPEC_KERNEL_AUTO};
 
 struct DeviceState {
