@@ -53,6 +53,8 @@ WORKLOADS = {
           "verify 64 lanes x 8 target columns",
     "C5": "256 lanes x 15 drafts = 3,840 draft columns x V=248,046 bf16 ~N(0,3), k={k}; verify 256 lanes x 16 "
           "target columns",
+    "C5s": "shortlist: 3,840 draft columns x 131,072 bf16 ~N(0,3) whose local ids map to vocabulary ids through "
+           "a seeded 131,072-entry id map (spec_topk_mapped), k={k}; no verify",
 }
 
 
@@ -62,7 +64,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=100_000)
     p.add_argument("--warmup", type=int, default=200)
     p.add_argument("--config", default="C2", choices=sorted(WORKLOADS))
-    p.add_argument("--k", type=int, default=None, help="k for C5 (1, 8, 20 or 64)")
+    p.add_argument("--k", type=int, default=None, help="k for C5 and C5s (1, 8, 20 or 64)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--kernel", default="auto", choices=["auto", "warp", "cta"],
@@ -126,7 +128,7 @@ def make_workload(config: str, k: int | None, seed_offset: int = 0):
     import synth
     fn = synth.CONFIGS[config]
     kw = {}
-    if config == "C5" and k is not None:
+    if config in ("C5", "C5s") and k is not None:
         kw["k"] = k
     if seed_offset:
         import inspect
@@ -233,7 +235,10 @@ def oracle_round(r, threads: int, cols=None, n: int | None = None):
     elements); returns the logit bytes it read."""
     import oracle
     if cols is None:
-        oracle.topk(r.draft, r.k, threads=threads)
+        if r.id_map is not None:
+            oracle.topk_mapped(r.draft, r.k, r.id_map, threads=threads)
+        else:
+            oracle.topk(r.draft, r.k, threads=threads)
         if r.target is not None:
             oracle.verify(r.target, r.drafts, threads=threads)
         return r.logit_bytes()
@@ -241,7 +246,10 @@ def oracle_round(r, threads: int, cols=None, n: int | None = None):
     nb = 0
     if len(dc):
         x = r.draft[dc, :n]
-        oracle.topk(x, min(r.k, x.shape[1]), threads=threads)
+        if r.id_map is not None:
+            oracle.topk_mapped(x, min(r.k, x.shape[1]), r.id_map[:x.shape[1]], threads=threads)
+        else:
+            oracle.topk(x, min(r.k, x.shape[1]), threads=threads)
         nb += x.size * 2
     if len(tc):
         t = r.target[tc, :n]
@@ -322,8 +330,8 @@ def workload_config(args, r, ring):
     if ring is not None:
         c["l2"] = (f"inputs rotated through a ring of {ring[0]} copies ({ring[1] / 1e6:.0f} MB, > 4x the "
                    f"{ring[2] / 1e6:.0f} MB L2): every round reads its logits from HBM")
-        c["launch"] = ("spec_round_sampled" if args.sampled else "spec_round") + \
-            ": one kernel per round; K rounds replayed as CUDA graphs"
+        c["launch"] = ("spec_round_sampled" if args.sampled else "spec_topk_mapped" if r.id_map is not None
+                       else "spec_round") + ": one kernel per round; K rounds replayed as CUDA graphs"
     if args.sampled:
         c["verify"] = "sampled: T 1.0, top_p 0.95, top_k 20, one-hot drafts, seeded uniforms"
     return c
@@ -345,6 +353,8 @@ def run_ours(args):
     import speculative_decoding_draft_column_gb300 as sd
 
     r = make_workload(args.config, args.k, seed_offset=rank)   # independent lanes per GPU
+    if args.sampled and r.id_map is not None:
+        raise SystemExit("--sampled needs target columns; the shortlist workload has none")
     cols, V, k, lanes, gamma = r.cols, r.V, r.k, r.lanes, max(r.gamma, 1)
     bytes_round = r.logit_bytes()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -352,6 +362,7 @@ def run_ours(args):
     xs = [torch.from_numpy(r.draft.view(np.int16)).to(dev) for _ in range(R)]
     ts = [torch.from_numpy(r.target.view(np.int16)).to(dev) if lanes else None for _ in range(R)]
     drafts = torch.from_numpy(r.drafts).to(dev) if lanes else None
+    id_map = torch.from_numpy(r.id_map).to(dev) if r.id_map is not None else None
     vals = torch.empty((cols, k), dtype=torch.int16, device=dev)
     ids = torch.empty((cols, k), dtype=torch.int32, device=dev)
     acc = torch.empty(max(lanes, 1), dtype=torch.int32, device=dev)
@@ -366,6 +377,9 @@ def run_ours(args):
         def one(i):
             sd.spec_round_sampled(xs[i % R], cols, V, k, vals, ids, ts[i % R], drafts, lanes, gamma,
                                   1.0, 0.95, 20, uni, acc, com)
+    elif id_map is not None:
+        def one(i):
+            sd.spec_topk_mapped(xs[i % R], cols, V, k, id_map, vals, ids)
     else:
         def one(i):
             sd.spec_round(xs[i % R], cols, V, k, vals, ids, ts[i % R], drafts, lanes, gamma, acc, com)
@@ -426,11 +440,27 @@ def run_ours(args):
         ha = torch.empty(max(lanes, 1), dtype=torch.int32).pin_memory()
         hc = torch.empty((max(lanes, 1), gamma + 1), dtype=torch.int32).pin_memory()
         sd.spec_set_stream(stream)
+        api = "spec_round_host (pinned host buffers; H2D, kernel, D2H, stream sync per step)"
 
         def host_step():
             sd.lib.spec_round_host(hd.data_ptr(), cols, V, k, hv.data_ptr(), hi.data_ptr(),
                                    ht.data_ptr() if lanes else None, hdr.data_ptr() if lanes else None, lanes,
                                    gamma, ha.data_ptr() if lanes else None, hc.data_ptr() if lanes else None)
+
+        if id_map is not None:
+            # the shortlist has no host-buffer entry point: the caller's own
+            # copies around spec_topk_mapped (the map stays on the device)
+            api = ("torch copies from pinned host buffers on the library stream + spec_topk_mapped + "
+                   "copies back, stream sync per step")
+            xd = xs[0]
+
+            def host_step():
+                with torch.cuda.stream(stream):
+                    xd.copy_(hd, non_blocking=True)
+                    sd.spec_topk_mapped(xd, cols, V, k, id_map, vals, ids)
+                    hv.copy_(vals, non_blocking=True)
+                    hi.copy_(ids, non_blocking=True)
+                stream.synchronize()
 
         for _ in range(5):
             host_step()
@@ -447,7 +477,7 @@ def run_ours(args):
         e2e = {"value": round(world * bytes_round * n_e2e / dt / 1e9, 2), "unit": "GB/s",
                "us_per_round": round(dt / n_e2e * 1e6, 2), "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
-               "api": "spec_round_host (pinned host buffers; H2D, kernel, D2H, stream sync per step)"}
+               "api": api}
 
     if rank != 0:
         return 0

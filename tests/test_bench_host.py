@@ -69,3 +69,15 @@ def test_reference_arm_other_ranks_exit_quietly():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2"],
                          capture_output=True, text=True, env=env, timeout=120)
     assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+def test_shortlist_oracle_round_small():
+    """The CPU legs of the shortlist workload go through the mapped oracle,
+    whole and cut to a prefix of each column (the map cut with it)."""
+    import synth
+    r = synth.make_c5s(cols=4, V_local=4096, k=8)
+    assert r.target is None and r.id_map.shape == (4096,)
+    assert bench.oracle_round(r, 2) == r.logit_bytes()
+    assert bench.oracle_round(r, 2, cols=([0, 3], []), n=1000) == 2 * 1000 * 2
+    c = bench.workload_config(bench.parse_args(["--config", "C5s"]), r, None)
+    assert c["workload"].startswith("C5s: shortlist") and c["lanes"] == 0
