@@ -37,7 +37,9 @@
  *  - Scratch: the library owns one scratch area per device (per-column
  *    tickets and partial lists, a few MB at most).  It grows on demand with
  *    cudaMalloc outside stream capture; inside a capture a call that needs
- *    more than spec_reserve set aside fails with SPEC_ERR_ALLOC.  Calls that
+ *    more than spec_reserve set aside fails with SPEC_ERR_ALLOC.  An area
+ *    that a larger one replaces stays allocated until spec_release, so
+ *    launches in flight and CUDA graphs captured earlier keep valid scratch.  Calls that
  *    may run concurrently on the GPU (different streams, or different host
  *    threads) share this scratch and race: issue them on one stream.
  *  - Outputs must not alias inputs.
@@ -248,11 +250,13 @@ void *spec_get_stream(void);
  * (so that later calls need no allocation, e.g. inside a CUDA graph
  * capture).  max_cols counts draft columns, max_lanes/max_gamma the verify
  * part; max_k is the largest k -- or sampled-verify top_k -- to come.
- * Synchronises the device if it has to reallocate. */
+ * Growing allocates a new area (cudaMalloc + cudaMemset); the old one is
+ * kept for what already uses it. */
 spec_status spec_reserve(int64_t max_cols, int32_t max_k, int64_t max_lanes, int32_t max_gamma);
 
-/* Free the scratch and staging of the current device (after synchronising
- * it).  Later calls allocate again. */
+/* Free the scratch (current and replaced areas) and staging of the current
+ * device, after synchronising it.  CUDA graphs that captured calls of this
+ * library must not be replayed afterwards.  Later calls allocate again. */
 spec_status spec_release(void);
 
 /* Diagnostic of the bounded waits every kernel uses on its copy pipeline:

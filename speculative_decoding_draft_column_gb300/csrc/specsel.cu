@@ -24,6 +24,7 @@
 #include <atomic>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "specsel.h"
 #include "common.cuh"
@@ -58,6 +59,10 @@ struct DeviceState {
     void *scratch = nullptr;
     size_t scratch_bytes = 0;
     int64_t cap_cols = 0, cap_lanes = 0, cap_part = 0;
+    // Areas a larger one has replaced.  Launches already enqueued, and CUDA
+    // graphs captured earlier, still hold their addresses (and leave their
+    // tickets at zero), so they stay allocated until spec_release.
+    std::vector<void *> retired;
     void *staging = nullptr;
     size_t staging_bytes = 0;
 };
@@ -161,7 +166,7 @@ bool stream_capturing(cudaStream_t st)
 
 // Grow (never shrink) the device's scratch so that every region covers
 // `need`; fresh scratch is zeroed, and the kernels leave every ticket at zero
-// when they finish.
+// when they finish.  The area it replaces is retired, not freed.
 spec_status ensure_scratch(DeviceState &d, const ScratchCaps &need, cudaStream_t st)
 {
     if (d.scratch && need.cols <= d.cap_cols && need.lanes <= d.cap_lanes && need.part <= d.cap_part)
@@ -174,23 +179,19 @@ spec_status ensure_scratch(DeviceState &d, const ScratchCaps &need, cudaStream_t
     c.lanes = grow(d.cap_lanes, need.lanes);
     c.part = grow(d.cap_part, need.part);
     const size_t bytes = scratch_bytes(c);
-    cudaError_t e;
-    if (d.scratch) {
-        e = cudaDeviceSynchronize();
-        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-        cudaFree(d.scratch);
-        d.scratch = nullptr;
-        d.scratch_bytes = 0;
-        d.cap_cols = d.cap_lanes = d.cap_part = 0;
-    }
-    e = cudaMalloc(&d.scratch, bytes);
+    void *fresh = nullptr;
+    cudaError_t e = cudaMalloc(&fresh, bytes);
     if (e != cudaSuccess) {
-        d.scratch = nullptr;
         cudaGetLastError();
         return fail(SPEC_ERR_ALLOC, "cudaMalloc(%zu) for scratch: %s", bytes, cudaGetErrorString(e));
     }
-    e = cudaMemset(d.scratch, 0, bytes);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset scratch");
+    e = cudaMemset(fresh, 0, bytes);   // synchronous: zero before any launch can see it
+    if (e != cudaSuccess) {
+        cudaFree(fresh);
+        return cuda_fail(e, "cudaMemset scratch");
+    }
+    if (d.scratch) d.retired.push_back(d.scratch);
+    d.scratch = fresh;
     d.scratch_bytes = bytes;
     d.cap_cols = c.cols;
     d.cap_lanes = c.lanes;
@@ -629,11 +630,13 @@ spec_status spec_release(void)
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return SPEC_OK;
     DeviceState &d = g_dev[dev];
-    if (!d.scratch && !d.staging) return SPEC_OK;
+    if (!d.scratch && !d.staging && d.retired.empty()) return SPEC_OK;
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
     if (d.scratch) cudaFree(d.scratch);
     if (d.staging) cudaFree(d.staging);
+    for (void *p : d.retired) cudaFree(p);
+    d.retired.clear();
     d.scratch = d.staging = nullptr;
     d.scratch_bytes = d.staging_bytes = 0;
     d.cap_cols = d.cap_lanes = d.cap_part = 0;

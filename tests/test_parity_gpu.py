@@ -438,6 +438,50 @@ def test_side_stream_and_graph_capture():
     sd.spec_set_stream(None)
 
 
+def test_graph_survives_scratch_growth():
+    """A graph captured before the scratch grows replays correctly after it:
+    the area it captured stays allocated (retired, not freed) while a larger
+    one serves new calls."""
+    import torch
+    sd = gu.sd_module()
+    r = synth.make_c1(seed=6, V=50_001)
+    x, t, d = gu.dev_u16(r.draft), gu.dev_u16(r.target), gu.dev_i32(r.drafts)
+    cols, V, k, lanes, gamma = r.cols, r.V, r.k, r.lanes, r.gamma
+    vals = torch.empty((cols, k), dtype=torch.int16, device="cuda")
+    ids = torch.empty((cols, k), dtype=torch.int32, device="cuda")
+    acc = torch.empty(lanes, dtype=torch.int32, device="cuda")
+    com = torch.empty((lanes, gamma + 1), dtype=torch.int32, device="cuda")
+    sd.spec_reserve(cols, k, lanes, gamma)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        sd.spec_round(x, cols, V, k, vals, ids, t, d, lanes, gamma, acc, com)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        sd.spec_round(x, cols, V, k, vals, ids, t, d, lanes, gamma, acc, com)
+    sd.spec_set_stream(None)
+    # larger than any round of the suite: every region moves to a new area
+    sd.spec_reserve(3_000_000, 64, 8192, 15)
+    big = synth.make_c2(seed=7, V=20_011)
+    got = gu.run_round(big.draft, big.k, big.target, big.drafts)
+    gu.assert_topk_equal(got[:2], oracle.topk(big.draft, big.k), "after growth")
+    gu.assert_verify_equal(got[2:], oracle.verify(big.target, big.drafts), "after growth verify")
+    torch.cuda.synchronize()
+    for _ in range(2):
+        with torch.cuda.stream(s):
+            vals.zero_()
+            acc.fill_(-7)
+            g.replay()
+        s.synchronize()
+        sd.spec_device_status()
+        gu.assert_topk_equal((vals.cpu().numpy().view(np.uint16), ids.cpu().numpy()), oracle.topk(r.draft, k),
+                             "old graph after growth")
+        gu.assert_verify_equal((acc.cpu().numpy(), com.cpu().numpy()), oracle.verify(r.target, r.drafts),
+                               "old graph after growth verify")
+    del g
+    sd.spec_release()
+
+
 def test_round_host_buffers():
     sd = gu.sd_module()
     r = synth.make_c2(seed=9, V=30_000)
