@@ -8,7 +8,11 @@ is no CPU or PyTorch fallback.  If the shared library has not been built
 (``__graft_entry__.build()``), importing this package raises ImportError.
 
 Tensor conventions: bf16 logits may be ``torch.bfloat16`` or a 16-bit
-integer view of the same bits; ids and lengths are ``torch.int32``.
+integer view of the same bits; ids and lengths are ``torch.int32``.  A
+tensor argument must be contiguous, on the current CUDA device (host memory
+for ``spec_round_host``) and hold at least what the call reads or writes;
+otherwise ``SpecError`` (``SPEC_ERR_ARG``) is raised before the library is
+called.  Raw integer pointers are passed on unchecked, as in the C ABI.
 """
 from __future__ import annotations
 
@@ -92,6 +96,70 @@ def _ptr(x):
     return x.data_ptr()
 
 
+def _n(x) -> int:
+    """A count as a Python int, negatives as 0 (the C checks reject them)."""
+    try:
+        return max(0, int(x))
+    except (TypeError, ValueError):
+        return 0
+
+
+def _dev(x, count, elem_bytes: int, name: str):
+    """Pointer of a device buffer that must hold `count` elements of
+    `elem_bytes` bytes.  A tensor must be a contiguous CUDA tensor on the
+    current device and large enough; otherwise SpecError(SPEC_ERR_ARG) is
+    raised before anything is enqueued (a wrong buffer would make a kernel
+    read or write outside it).  None and raw integer pointers are passed on
+    unchecked, like the C ABI."""
+    if x is None or isinstance(x, int):
+        return x
+    if not (getattr(x, "is_cuda", False) and hasattr(x, "data_ptr")):
+        raise SpecError(SPEC_ERR_ARG, f"{name}: need a CUDA tensor (or a raw device pointer)")
+    import torch
+    if torch.cuda.is_available() and x.device.index != torch.cuda.current_device():
+        raise SpecError(SPEC_ERR_ARG, f"{name}: tensor on {x.device}, the current device is "
+                                      f"cuda:{torch.cuda.current_device()}")
+    if not x.is_contiguous():
+        raise SpecError(SPEC_ERR_ARG, f"{name}: tensor must be contiguous")
+    need, have = _n(count) * elem_bytes, x.numel() * x.element_size()
+    if have < need:
+        raise SpecError(SPEC_ERR_ARG, f"{name}: {have} bytes, the call needs {need}")
+    return x.data_ptr()
+
+
+def _host(x, count, elem_bytes: int, name: str):
+    """Pointer of a host buffer (numpy array or CPU tensor) of `count`
+    elements, checked like `_dev`."""
+    if x is None or isinstance(x, int):
+        return x
+    if hasattr(x, "ctypes") and hasattr(x, "flags"):           # numpy
+        if not x.flags.c_contiguous:
+            raise SpecError(SPEC_ERR_ARG, f"{name}: array must be C-contiguous")
+        have, ptr = x.nbytes, x.ctypes.data
+    else:
+        if getattr(x, "is_cuda", True) or not hasattr(x, "data_ptr"):
+            raise SpecError(SPEC_ERR_ARG, f"{name}: need a host array or CPU tensor")
+        if not x.is_contiguous():
+            raise SpecError(SPEC_ERR_ARG, f"{name}: tensor must be contiguous")
+        have, ptr = x.numel() * x.element_size(), x.data_ptr()
+    need = _n(count) * elem_bytes
+    if have < need:
+        raise SpecError(SPEC_ERR_ARG, f"{name}: {have} bytes, the call needs {need}")
+    return ptr
+
+
+def _topk_bufs(check, logits, cols, V, k, out_vals, out_ids, id_map=None):
+    c = _n(cols)
+    return (check(logits, c * _n(V), 2, "logits"), check(out_vals, c * _n(k), 2, "out_vals"),
+            check(out_ids, c * _n(k), 4, "out_ids"), check(id_map, _n(V) if c else 0, 4, "id_map"))
+
+
+def _verify_bufs(check, target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids):
+    ln, g = _n(lanes), _n(gamma)
+    return (check(target_logits, ln * (g + 1) * _n(V), 2, "target_logits"), check(drafts, ln * g, 4, "drafts"),
+            check(out_accept_len, ln, 4, "out_accept_len"), check(out_commit_ids, ln * (g + 1), 4, "out_commit_ids"))
+
+
 def _use_torch_stream():
     import torch
     if torch.cuda.is_available():
@@ -101,60 +169,66 @@ def _use_torch_stream():
 # ---- same-name wrappers of the C entry points ------------------------------
 
 def spec_topk(logits, cols, V, k, out_vals, out_ids):
+    x, v, i, _ = _topk_bufs(_dev, logits, cols, V, k, out_vals, out_ids)
     _use_torch_stream()
-    _check(lib.spec_topk(_ptr(logits), cols, V, k, _ptr(out_vals), _ptr(out_ids)))
+    _check(lib.spec_topk(x, cols, V, k, v, i))
 
 
 def spec_topk_mapped(logits, cols, V, k, id_map, out_vals, out_ids):
+    x, v, i, m = _topk_bufs(_dev, logits, cols, V, k, out_vals, out_ids, id_map)
     _use_torch_stream()
-    _check(lib.spec_topk_mapped(_ptr(logits), cols, V, k, _ptr(id_map), _ptr(out_vals), _ptr(out_ids)))
+    _check(lib.spec_topk_mapped(x, cols, V, k, m, v, i))
 
 
 def spec_verify(target_logits, drafts, lanes, gamma, out_accept_len, out_commit_ids):
+    t, d, a, c = _verify_bufs(_dev, target_logits, drafts, lanes, gamma, SPEC_VOCAB, out_accept_len, out_commit_ids)
     _use_torch_stream()
-    _check(lib.spec_verify(_ptr(target_logits), _ptr(drafts), lanes, gamma, _ptr(out_accept_len),
-                           _ptr(out_commit_ids)))
+    _check(lib.spec_verify(t, d, lanes, gamma, a, c))
 
 
 def spec_verify_v(target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids):
+    t, d, a, c = _verify_bufs(_dev, target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids)
     _use_torch_stream()
-    _check(lib.spec_verify_v(_ptr(target_logits), _ptr(drafts), lanes, gamma, V, _ptr(out_accept_len),
-                             _ptr(out_commit_ids)))
+    _check(lib.spec_verify_v(t, d, lanes, gamma, V, a, c))
 
 
 def spec_round(draft_logits, cols, V, k, out_vals, out_ids, target_logits, drafts, lanes, gamma,
                out_accept_len, out_commit_ids):
+    x, v, i, _ = _topk_bufs(_dev, draft_logits, cols, V, k, out_vals, out_ids)
+    t, d, a, c = _verify_bufs(_dev, target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids)
     _use_torch_stream()
-    _check(lib.spec_round(_ptr(draft_logits), cols, V, k, _ptr(out_vals), _ptr(out_ids), _ptr(target_logits),
-                          _ptr(drafts), lanes, gamma, _ptr(out_accept_len), _ptr(out_commit_ids)))
+    _check(lib.spec_round(x, cols, V, k, v, i, t, d, lanes, gamma, a, c))
 
 
 def spec_round_noalloc(draft_logits, cols, V, k, out_vals, out_ids, target_logits, drafts, lanes, gamma,
                        out_accept_len, out_commit_ids):
     """spec_round with its scratch in a fixed device array: allocates nothing
     (for callers whose device memory all comes from their own pool)."""
+    x, v, i, _ = _topk_bufs(_dev, draft_logits, cols, V, k, out_vals, out_ids)
+    t, d, a, c = _verify_bufs(_dev, target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids)
     _use_torch_stream()
-    _check(lib.spec_round_noalloc(_ptr(draft_logits), cols, V, k, _ptr(out_vals), _ptr(out_ids),
-                                  _ptr(target_logits), _ptr(drafts), lanes, gamma, _ptr(out_accept_len),
-                                  _ptr(out_commit_ids)))
+    _check(lib.spec_round_noalloc(x, cols, V, k, v, i, t, d, lanes, gamma, a, c))
 
 
 def spec_verify_sampled(target_logits, drafts, lanes, gamma, V, temperature, top_p, top_k, uniforms,
                         out_accept_len, out_commit_ids):
     """Sampled verify with one-hot drafts; ``uniforms`` a float64 CUDA tensor
     [lanes, gamma+1, 2] of numbers in [0, 1)."""
+    t, d, a, c = _verify_bufs(_dev, target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids)
+    u = _dev(uniforms, _n(lanes) * (_n(gamma) + 1) * 2, 8, "uniforms")
     _use_torch_stream()
-    _check(lib.spec_verify_sampled(_ptr(target_logits), _ptr(drafts), lanes, gamma, V, float(temperature),
-                                   float(top_p), top_k, _ptr(uniforms), _ptr(out_accept_len), _ptr(out_commit_ids)))
+    _check(lib.spec_verify_sampled(t, d, lanes, gamma, V, float(temperature), float(top_p), top_k, u, a, c))
 
 
 def spec_round_sampled(draft_logits, cols, V, k, out_vals, out_ids, target_logits, drafts, lanes, gamma,
                        temperature, top_p, top_k, uniforms, out_accept_len, out_commit_ids):
     """spec_round with sampled verify, one launch."""
+    x, v, i, _ = _topk_bufs(_dev, draft_logits, cols, V, k, out_vals, out_ids)
+    t, d, a, c = _verify_bufs(_dev, target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids)
+    u = _dev(uniforms, _n(lanes) * (_n(gamma) + 1) * 2, 8, "uniforms")
     _use_torch_stream()
-    _check(lib.spec_round_sampled(_ptr(draft_logits), cols, V, k, _ptr(out_vals), _ptr(out_ids),
-                                  _ptr(target_logits), _ptr(drafts), lanes, gamma, float(temperature), float(top_p),
-                                  top_k, _ptr(uniforms), _ptr(out_accept_len), _ptr(out_commit_ids)))
+    _check(lib.spec_round_sampled(x, cols, V, k, v, i, t, d, lanes, gamma, float(temperature), float(top_p),
+                                  top_k, u, a, c))
 
 
 COUNTER_WORDS = 3 + 2 * SPEC_MAX_GAMMA   # uint64 words of a spec_counters block
@@ -164,10 +238,11 @@ def spec_round_counted(draft_logits, cols, V, k, out_vals, out_ids, target_logit
                        out_accept_len, out_commit_ids, counters):
     """spec_round that also adds the round to ``counters`` (an int64 CUDA
     tensor of COUNTER_WORDS, see ``new_counters``; None: no counting)."""
+    x, v, i, _ = _topk_bufs(_dev, draft_logits, cols, V, k, out_vals, out_ids)
+    t, d, a, c = _verify_bufs(_dev, target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids)
+    n = _dev(counters, COUNTER_WORDS, 8, "counters")
     _use_torch_stream()
-    _check(lib.spec_round_counted(_ptr(draft_logits), cols, V, k, _ptr(out_vals), _ptr(out_ids),
-                                  _ptr(target_logits), _ptr(drafts), lanes, gamma, _ptr(out_accept_len),
-                                  _ptr(out_commit_ids), _ptr(counters)))
+    _check(lib.spec_round_counted(x, cols, V, k, v, i, t, d, lanes, gamma, a, c, n))
 
 
 def new_counters(device="cuda"):
@@ -188,10 +263,10 @@ def read_counters(counters) -> dict:
 def spec_round_host(draft_logits, cols, V, k, out_vals, out_ids, target_logits, drafts, lanes, gamma,
                     out_accept_len, out_commit_ids):
     """Host buffers (CPU tensors, ideally pinned, or numpy arrays) in and out."""
+    x, v, i, _ = _topk_bufs(_host, draft_logits, cols, V, k, out_vals, out_ids)
+    t, d, a, c = _verify_bufs(_host, target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids)
     _use_torch_stream()
-    hp = lambda a: None if a is None else (a.ctypes.data if hasattr(a, "ctypes") else a.data_ptr())
-    _check(lib.spec_round_host(hp(draft_logits), cols, V, k, hp(out_vals), hp(out_ids), hp(target_logits),
-                               hp(drafts), lanes, gamma, hp(out_accept_len), hp(out_commit_ids)))
+    _check(lib.spec_round_host(x, cols, V, k, v, i, t, d, lanes, gamma, a, c))
 
 
 def spec_set_kernel(which: int):
