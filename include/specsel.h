@@ -12,12 +12,12 @@
  *           a certified running k-th value, and the unit that completes a
  *           split column merges the published lists (spec_set_kernel).
  *
- *   verify  section "How it works", first paragraph: a verify round runs
- *           every lane's anchor plus its drafts through the target model
- *           once; each lane commits the longest run of drafts the target
- *           itself would have picked, plus the target's own next token.
- *           Under greedy decoding ("Speculative decoding, measured on my M4
- *           Max", section 1) "would have picked" is the target argmax.
+ *   verify  section "How it works", first paragraph: the target scores
+ *           each lane's anchor and drafts in one pass; a lane keeps the
+ *           drafts up to the first one the target disagrees with, and adds
+ *           one token of the target's own choosing after them.  With greedy
+ *           decoding ("Speculative decoding, measured on my M4 Max",
+ *           section 1) the target's choice at a position is its argmax.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -64,8 +64,9 @@ typedef int spec_status;
    (same page, "How it works", third paragraph). spec_verify assumes it. */
 #define SPEC_VOCAB 248046
 /* Largest k: 64.  Largest gamma (drafts per lane): 15, the draft width of a
-   block size of 16 ("Apathy-Qwen3.8-27B-DFlash-drafter-v2" model card:
-   trained drafts = block_size - 1, and a larger gamma is refused). */
+   block size of 16 ("Apathy-Qwen3.8-27B-DFlash-drafter-v2" model card: the
+   usable draft width is one less than the block size, and the drafter's
+   loader rejects a wider gamma). */
 #define SPEC_MAX_K 64
 #define SPEC_MAX_GAMMA 15
 
@@ -84,8 +85,8 @@ typedef int spec_status;
 spec_status spec_topk(const uint16_t *logits, int64_t cols, int64_t V, int32_t k,
                       uint16_t *out_vals, int32_t *out_ids);
 
-/* Shortlist top-k ("How it works", second paragraph: an opt-in head over
- * the 131,072 most frequent tokens).  As spec_topk over [cols][V] shortlist
+/* Shortlist top-k ("How it works", second paragraph: an optional drafter
+ * head whose output covers only 131,072 of the commonest token ids).  As spec_topk over [cols][V] shortlist
  * logits, where local id i stands for vocabulary id id_map[i]:
  *   id_map    int32 [V], device, injective (distinct entries), values >= 0.
  *   out_ids   vocabulary ids id_map[i]; ties go to the smaller VOCABULARY id.

@@ -12,8 +12,9 @@
  *   top-k      For each column of V bf16 logits, the k largest values,
  *              largest first, ties going to the smaller row (token) id.
  *              ["A drafter inside the artifact" (Ignis DFlash2 page),
- *              section "How it works", third paragraph: the replacement
- *              top-k selects "largest first, ties to the smaller row id".]
+ *              section "How it works", third paragraph: the page's faster
+ *              top-k gives the same selection, order and tie-breaking by
+ *              row id as the kernel it replaced.]
  *              Written out as the definition: sort all V (value, id) pairs
  *              by value descending, then id ascending, and keep the first k.
  *              Values compare as numbers (bf16 widened exactly to double), so
@@ -23,18 +24,18 @@
  *   top-k, shortlist   The same over a shortlist column whose local ids map
  *              to vocabulary ids through id_map; ties go to the smaller
  *              vocabulary id, and the output ids are vocabulary ids.
- *              [same page, "How it works", second paragraph: the Q4
- *              "shortlist" head over the 131,072 most frequent tokens.]
+ *              [same page, "How it works", second paragraph: an optional
+ *              quantised drafter head restricted to 131,072 token ids.]
  *
  *   verify     Per lane: t[j] = argmax of target column j (j = 0..gamma),
  *              ties to the smaller id; accept the longest prefix of drafts
  *              with drafts[i] == t[i]; commit that prefix plus the target's
  *              own next token t[a]; pad with -1.
- *              [same page, "How it works", first paragraph: each lane
- *              commits the longest run the model itself would have picked,
- *              plus the model's own next token.  "Speculative decoding,
- *              measured on my M4 Max", section 1: under greedy decoding the
- *              output equals what the target alone would have written.]
+ *              [same page, "How it works", first paragraph: a lane keeps
+ *              its drafts up to the first the target disagrees with, then
+ *              one token chosen by the target.  "Speculative decoding,
+ *              measured on my M4 Max", section 1: with greedy decoding the
+ *              result is the same text the target would produce alone.]
  *
  * Parity pins (tests/test_oracle_pins.py): brute force against an
  * independent repeated-maximum selector on tiny columns and exhaustively on
