@@ -67,6 +67,9 @@ def parse_args(argv=None):
     p.add_argument("--k", type=int, default=None, help="k for C5 and C5s (1, 8, 20 or 64)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--part", default="round", choices=["round", "split", "topk", "verify"],
+                   help="round: spec_round, one fused launch (default); split: spec_topk then spec_verify_v, two "
+                        "launches a round; topk / verify: that call alone on its own columns")
     p.add_argument("--kernel", default="auto", choices=["auto", "warp", "cta"],
                    help="streaming kernel (spec_set_kernel); auto picks by round size")
     p.add_argument("--sampled", action="store_true",
@@ -334,6 +337,11 @@ def workload_config(args, r, ring):
                        else "spec_round") + ": one kernel per round; K rounds replayed as CUDA graphs"
     if args.sampled:
         c["verify"] = "sampled: T 1.0, top_p 0.95, top_k 20, one-hot drafts, seeded uniforms"
+    part = getattr(args, "part", "round")
+    if part != "round":
+        c["part"] = {"split": "spec_topk then spec_verify_v: two launches a round",
+                     "topk": "spec_topk alone on the draft columns (value = their logit GB/s)",
+                     "verify": "spec_verify_v alone on the target columns (value = their logit GB/s)"}[part]
     return c
 
 
@@ -355,8 +363,14 @@ def run_ours(args):
     r = make_workload(args.config, args.k, seed_offset=rank)   # independent lanes per GPU
     if args.sampled and r.id_map is not None:
         raise SystemExit("--sampled needs target columns; the shortlist workload has none")
+    if args.part != "round" and (args.sampled or r.id_map is not None or not r.lanes):
+        raise SystemExit("--part other than round needs a greedy round with draft and target columns")
     cols, V, k, lanes, gamma = r.cols, r.V, r.k, r.lanes, max(r.gamma, 1)
     bytes_round = r.logit_bytes()
+    # logits read per step, and per launch of the call(s) timed
+    bytes_step = {"round": bytes_round, "split": bytes_round, "topk": r.draft.nbytes,
+                  "verify": 0 if r.target is None else r.target.nbytes}[args.part]
+    per_step = 2 if args.part == "split" else 1
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     R = max(2, math.ceil(4 * l2 / bytes_round))
     xs = [torch.from_numpy(r.draft.view(np.int16)).to(dev) for _ in range(R)]
@@ -380,6 +394,16 @@ def run_ours(args):
     elif id_map is not None:
         def one(i):
             sd.spec_topk_mapped(xs[i % R], cols, V, k, id_map, vals, ids)
+    elif args.part == "split":
+        def one(i):
+            sd.spec_topk(xs[i % R], cols, V, k, vals, ids)
+            sd.spec_verify_v(ts[i % R], drafts, lanes, gamma, V, acc, com)
+    elif args.part == "topk":
+        def one(i):
+            sd.spec_topk(xs[i % R], cols, V, k, vals, ids)
+    elif args.part == "verify":
+        def one(i):
+            sd.spec_verify_v(ts[i % R], drafts, lanes, gamma, V, acc, com)
     else:
         def one(i):
             sd.spec_round(xs[i % R], cols, V, k, vals, ids, ts[i % R], drafts, lanes, gamma, acc, com)
@@ -401,7 +425,7 @@ def run_ours(args):
                 one(i)
         graphs.append(g)
     captured = sd.spec_launch_count() - c0
-    assert captured == chunk + rem
+    assert captured == (chunk + rem) * per_step
     with torch.cuda.stream(stream):
         graphs[0].replay()                   # untimed: upload / warm the graph
     stream.synchronize()
@@ -426,11 +450,11 @@ def run_ours(args):
     barrier(world, dev)
     ms = e0.elapsed_time(e1)
     ms_max = max_over_ranks(ms, world, dev)
-    launches = n_full * chunk + rem
+    launches = (n_full * chunk + rem) * per_step
 
     # end to end through the host-buffer entry point
     e2e = None
-    if not args.no_e2e and not args.sampled:
+    if not args.no_e2e and not args.sampled and args.part == "round":
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
         hd = pin(r.draft.view(np.int16))
         ht = pin(r.target.view(np.int16)) if lanes else None
@@ -483,20 +507,26 @@ def run_ours(args):
         return 0
     peak, peak_src = hbm_peak()
     us_round = ms_max * 1e3 / K
-    gbs = world * bytes_round * K / (ms_max * 1e-3) / 1e9
+    gbs = world * bytes_step * K / (ms_max * 1e-3) / 1e9
     per_launch_us = ms * 1e3 / launches
-    achieved = bytes_round / (per_launch_us * 1e-6) / 1e9
+    # the roofline of one launch; for the split round, of one step (two launches)
+    unit_us = per_launch_us * per_step
+    achieved = bytes_step / (unit_us * 1e-6) / 1e9
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    kname = kernel_name(bytes_step, sms, args.kernel) if args.part != "split" else \
+        f"{kernel_name(r.draft.nbytes, sms, args.kernel)} + {kernel_name(r.target.nbytes, sms, args.kernel)}"
     line = {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_max / K, 6), "us_per_round": round(us_round, 3),
         "pct_of_hbm_peak": round(100 * gbs / world / peak, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; see synth/)",
         "config": workload_config(args, r, (R, R * bytes_round, l2)),
-        "roofline": {"bound": "hbm", "kernel": kernel_name(bytes_round, torch.cuda.get_device_properties(dev).multi_processor_count,
-                                                        args.kernel),
+        "roofline": {"bound": "hbm", "kernel": kname,
                      "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "traffic": recorded_traffic(args.config), "algorithmic_bytes_per_launch": bytes_round,
+                     "traffic": recorded_traffic(args.config) if args.part == "round" and not args.sampled
+                     and args.kernel == "auto" else None,
+                     "algorithmic_bytes_per_launch": bytes_step if per_step == 1 else None,
                      "launch_us": round(per_launch_us, 3),
                      "timing": "CUDA events around K graph-replayed launches on the launching stream; "
                                "per-launch time includes the graph's inter-launch gap"},
@@ -505,7 +535,7 @@ def run_ours(args):
     }
     if e2e:
         line["e2e"] = e2e
-    if world == 1 and not args.no_cpu_baseline and not args.sampled:
+    if world == 1 and not args.no_cpu_baseline and not args.sampled and args.part == "round":
         line["cpu_baseline"] = cpu_baseline(r)
     print(json.dumps(line), flush=True)
     return 0

@@ -81,3 +81,15 @@ def test_shortlist_oracle_round_small():
     assert bench.oracle_round(r, 2, cols=([0, 3], []), n=1000) == 2 * 1000 * 2
     c = bench.workload_config(bench.parse_args(["--config", "C5s"]), r, None)
     assert c["workload"].startswith("C5s: shortlist") and c["lanes"] == 0
+
+
+def test_part_modes():
+    """--part: the fused round by default; the split round and each call
+    alone are labelled in the config."""
+    import synth
+    assert bench.parse_args([]).part == "round"
+    r = synth.make_c1(V=1000)
+    assert "part" not in bench.workload_config(bench.parse_args([]), r, None)
+    for part, word in (("split", "two launches"), ("topk", "spec_topk alone"), ("verify", "spec_verify_v alone")):
+        c = bench.workload_config(bench.parse_args(["--part", part]), r, None)
+        assert word in c["part"]
