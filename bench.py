@@ -261,9 +261,7 @@ def oracle_round(r, threads: int, cols=None, n: int | None = None):
     return nb
 
 
-def cpu_baseline(r, budget_s: float = 3.0):
-    threads = os.cpu_count() or 1
-    oracle_round(r, threads)                 # warm (page in, build)
+def _time_oracle_rounds(r, threads: int, budget_s: float):
     t0 = time.perf_counter()
     rounds, nbytes = 0, 0
     while True:
@@ -271,12 +269,26 @@ def cpu_baseline(r, budget_s: float = 3.0):
         rounds += 1
         if time.perf_counter() - t0 >= budget_s:
             break
-    dt = time.perf_counter() - t0
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{rounds} full rounds of the same workload ({r.cols} top-k columns + "
-                      f"{0 if r.target is None else r.target.shape[0]} verify columns each), "
-                      f"{dt:.2f} s wall on {threads} threads",
-            "us_per_round": round(dt / rounds * 1e6, 1)}
+    return rounds, nbytes, time.perf_counter() - t0
+
+
+def cpu_baseline(r, budget_s: float = 3.0, one_core_max_bytes: int = 100_000_000):
+    """The oracle over whole rounds on every host core (and, for rounds of
+    at most `one_core_max_bytes` of logits, on one core)."""
+    threads = os.cpu_count() or 1
+    oracle_round(r, threads)                 # warm (page in, build)
+    rounds, nbytes, dt = _time_oracle_rounds(r, threads, budget_s)
+    ncols = r.cols + (0 if r.target is None else r.target.shape[0])
+    out = {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+           "sample": f"{rounds} full rounds of the same workload ({r.cols} top-k columns + "
+                     f"{0 if r.target is None else r.target.shape[0]} verify columns each), "
+                     f"{dt:.2f} s wall on {threads} threads",
+           "us_per_round": round(dt / rounds * 1e6, 1), "columns_per_s": round(rounds * ncols / dt, 1)}
+    if r.logit_bytes() <= one_core_max_bytes:
+        r1, b1, d1 = _time_oracle_rounds(r, 1, 0.0)        # one round on one thread
+        out["one_core"] = {"value": round(b1 / d1 / 1e9, 4), "unit": "GB/s", "us_per_round": round(d1 / r1 * 1e6, 1),
+                           "columns_per_s": round(r1 * ncols / d1, 1)}
+    return out
 
 
 def run_reference(args):

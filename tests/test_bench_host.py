@@ -93,3 +93,13 @@ def test_part_modes():
     for part, word in (("split", "two launches"), ("topk", "spec_topk alone"), ("verify", "spec_verify_v alone")):
         c = bench.workload_config(bench.parse_args(["--part", part]), r, None)
         assert word in c["part"]
+
+
+def test_cpu_baseline_fields():
+    """The oracle leg: all cores, plus one core for small rounds."""
+    import synth
+    r = synth.make_c1(V=5000)
+    c = bench.cpu_baseline(r, budget_s=0.05)
+    assert c["kind"] == "oracle" and c["cores"] >= 1 and c["value"] > 0 and c["columns_per_s"] > 0
+    assert c["one_core"]["value"] > 0 and c["one_core"]["us_per_round"] > 0
+    assert "one_core" not in bench.cpu_baseline(r, budget_s=0.01, one_core_max_bytes=0)
