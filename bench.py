@@ -337,11 +337,19 @@ def run_reference(args):
     return 0
 
 
+def input_hashes(r) -> dict:
+    """sha256[:16] of every input buffer of the round (seeded, so fixed per
+    workload and seed)."""
+    import synth
+    bufs = (("draft_logits", r.draft), ("target_logits", r.target), ("drafts", r.drafts), ("id_map", r.id_map))
+    return {name: synth.content_hash(a) for name, a in bufs if a is not None}
+
+
 def workload_config(args, r, ring):
     desc = WORKLOADS[args.config].format(k=r.k)
     c = {"workload": f"{args.config}: {desc}", "cols": r.cols, "V": r.V, "k": r.k, "lanes": r.lanes,
          "gamma": r.gamma, "bytes_per_round": r.logit_bytes(), "parallelism": "replicas (one independent round "
-         "per GPU, no data exchange)"}
+         "per GPU, no data exchange)", "input_sha256_16": input_hashes(r)}
     if ring is not None:
         c["l2"] = (f"inputs rotated through a ring of {ring[0]} copies ({ring[1] / 1e6:.0f} MB, > 4x the "
                    f"{ring[2] / 1e6:.0f} MB L2): every round reads its logits from HBM")

@@ -138,11 +138,12 @@ class Round:
 
 
 def content_hash(*arrays: np.ndarray) -> str:
+    """sha256[:16] over the arrays' bytes (C order), hashed in place."""
     h = hashlib.sha256()
     for a in arrays:
         if a is None:
             continue
-        h.update(np.ascontiguousarray(a).view(np.uint8).tobytes())
+        h.update(memoryview(np.ascontiguousarray(a)).cast("B"))
     return h.hexdigest()[:16]
 
 

@@ -103,3 +103,17 @@ def test_cpu_baseline_fields():
     assert c["kind"] == "oracle" and c["cores"] >= 1 and c["value"] > 0 and c["columns_per_s"] > 0
     assert c["one_core"]["value"] > 0 and c["one_core"]["us_per_round"] > 0
     assert "one_core" not in bench.cpu_baseline(r, budget_s=0.01, one_core_max_bytes=0)
+
+
+def test_config_carries_input_hashes():
+    """Every input buffer's content hash is in the config: equal for equal
+    seeds, different for another seed."""
+    import synth
+    a, b, c = synth.make_c1(V=3000), synth.make_c1(V=3000), synth.make_c1(seed=2, V=3000)
+    args = bench.parse_args(["--config", "C1"])
+    ha = bench.workload_config(args, a, None)["input_sha256_16"]
+    assert set(ha) == {"draft_logits", "target_logits", "drafts"}
+    assert ha == bench.workload_config(args, b, None)["input_sha256_16"]
+    assert ha["draft_logits"] != bench.workload_config(args, c, None)["input_sha256_16"]["draft_logits"]
+    s = synth.make_c5s(cols=2, V_local=1024)
+    assert "id_map" in bench.input_hashes(s) and "target_logits" not in bench.input_hashes(s)
