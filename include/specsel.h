@@ -86,8 +86,9 @@ spec_status spec_topk(const uint16_t *logits, int64_t cols, int64_t V, int32_t k
                       uint16_t *out_vals, int32_t *out_ids);
 
 /* Shortlist top-k ("How it works", second paragraph: an optional drafter
- * head whose output covers only 131,072 of the commonest token ids).  As spec_topk over [cols][V] shortlist
- * logits, where local id i stands for vocabulary id id_map[i]:
+ * head whose output covers only 131,072 of the commonest token ids).  As
+ * spec_topk over [cols][V] shortlist logits, where local id i stands for
+ * vocabulary id id_map[i]:
  *   id_map    int32 [V], device, injective (distinct entries), values >= 0.
  *   out_ids   vocabulary ids id_map[i]; ties go to the smaller VOCABULARY id.
  * Duplicate entries in id_map are outside the contract. */
