@@ -192,7 +192,10 @@ spec_status spec_round_counted(const uint16_t *draft_logits, int64_t cols, int64
  * pointer (pinned memory copies fastest).  The call copies the inputs to
  * library-owned device staging memory, runs spec_round, copies the outputs
  * back and waits for the stream, so outputs are valid on return.  Staging
- * grows with cudaMalloc as needed (not capturable). */
+ * grows with cudaMalloc as needed (not capturable); an area a larger one
+ * replaces stays allocated until spec_release.  Host calls from several
+ * threads are serialised inside the library (each holds it until its stream
+ * has drained), so they never share the staging area while it is in use. */
 spec_status spec_round_host(const uint16_t *draft_logits, int64_t cols, int64_t V, int32_t k,
                             uint16_t *out_vals, int32_t *out_ids,
                             const uint16_t *target_logits, const int32_t *drafts, int64_t lanes,
@@ -212,6 +215,9 @@ spec_status spec_round_host(const uint16_t *draft_logits, int64_t cols, int64_t 
  *   - sizes are limited: cols + lanes*(gamma+1) <= SPEC_NOALLOC_MAX_COLS and
  *     lanes <= SPEC_NOALLOC_MAX_LANES; larger calls return SPEC_ERR_ARG with
  *     a message naming the limit;
+ *   - the array holds a fixed number of published partial lists, so a round
+ *     with a large k may be spread over fewer streaming units than spec_round
+ *     would use (same results, possibly slower: at k = 64 at most 992 units);
  *   - the first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture;
  *   - every call shares the one array and starts by clearing its tickets on

@@ -347,13 +347,13 @@ struct Sampling {
     const double *uniforms = nullptr;
 };
 
-spec_status launch_round(const uint16_t *draft, int64_t cols, int64_t V, int32_t k, const int32_t *id_map,
-                         uint16_t *vals, int32_t *ids, const uint16_t *target, const int32_t *drafts,
-                         int64_t lanes, int32_t gamma, int64_t tV, int32_t *acc, int32_t *com,
-                         spec_counters *counters = nullptr, const Sampling &smp = Sampling())
+// The caller holds g_mu.
+spec_status launch_round_locked(const uint16_t *draft, int64_t cols, int64_t V, int32_t k, const int32_t *id_map,
+                                uint16_t *vals, int32_t *ids, const uint16_t *target, const int32_t *drafts,
+                                int64_t lanes, int32_t gamma, int64_t tV, int32_t *acc, int32_t *com,
+                                spec_counters *counters = nullptr, const Sampling &smp = Sampling())
 {
     if (cols == 0 && lanes == 0) return SPEC_OK;
-    std::lock_guard<std::mutex> lock(g_mu);
     DeviceState *d = nullptr;
     spec_status st = device_state(&d);
     if (st != SPEC_OK) return st;
@@ -388,23 +388,31 @@ spec_status launch_round(const uint16_t *draft, int64_t cols, int64_t V, int32_t
     return SPEC_OK;
 }
 
+spec_status launch_round(const uint16_t *draft, int64_t cols, int64_t V, int32_t k, const int32_t *id_map,
+                         uint16_t *vals, int32_t *ids, const uint16_t *target, const int32_t *drafts,
+                         int64_t lanes, int32_t gamma, int64_t tV, int32_t *acc, int32_t *com,
+                         spec_counters *counters = nullptr, const Sampling &smp = Sampling())
+{
+    if (cols == 0 && lanes == 0) return SPEC_OK;
+    std::lock_guard<std::mutex> lock(g_mu);
+    return launch_round_locked(draft, cols, V, k, id_map, vals, ids, target, drafts, lanes, gamma, tV, acc, com,
+                               counters, smp);
+}
+
+// Grow the host-call staging area; the caller holds g_mu.  The area it
+// replaces is retired (freed by spec_release), never freed under a copy
+// that may still be in flight.
 spec_status ensure_staging(DeviceState &d, size_t bytes)
 {
     if (d.staging_bytes >= bytes) return SPEC_OK;
-    cudaError_t e;
-    if (d.staging) {
-        e = cudaDeviceSynchronize();
-        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-        cudaFree(d.staging);
-        d.staging = nullptr;
-        d.staging_bytes = 0;
-    }
-    e = cudaMalloc(&d.staging, bytes);
+    void *fresh = nullptr;
+    const cudaError_t e = cudaMalloc(&fresh, bytes);
     if (e != cudaSuccess) {
-        d.staging = nullptr;
         cudaGetLastError();
         return fail(SPEC_ERR_ALLOC, "cudaMalloc(%zu) for staging: %s", bytes, cudaGetErrorString(e));
     }
+    if (d.staging) d.retired.push_back(d.staging);
+    d.staging = fresh;
     d.staging_bytes = bytes;
     return SPEC_OK;
 }
@@ -553,25 +561,26 @@ spec_status spec_round_host(const uint16_t *draft_logits, int64_t cols, int64_t 
     size_t off[7], tot = 0;
     const size_t sz[7] = {b_dl, b_tl, b_dr, b_v, b_i, b_a, b_c};
     for (int i = 0; i < 7; ++i) { off[i] = tot; tot = align256(tot + sz[i]); }
-    char *s = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        DeviceState *d = nullptr;
-        st = device_state(&d);
-        if (st != SPEC_OK) return st;
-        st = ensure_staging(*d, tot);
-        if (st != SPEC_OK) return st;
-        s = static_cast<char *>(d->staging);
-    }
+    // The lock is held from the staging lookup until the stream has drained:
+    // host calls are serialised, so no other thread grows, frees or reuses
+    // the staging area while this call's copies or kernel use it.
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState *d = nullptr;
+    st = device_state(&d);
+    if (st != SPEC_OK) return st;
+    st = ensure_staging(*d, tot);
+    if (st != SPEC_OK) return st;
+    char *s = static_cast<char *>(d->staging);
     cudaError_t e = cudaSuccess;
     if (cols) e = cudaMemcpyAsync(s + off[0], draft_logits, b_dl, cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess && lanes) e = cudaMemcpyAsync(s + off[1], target_logits, b_tl, cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess && lanes) e = cudaMemcpyAsync(s + off[2], drafts, b_dr, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync H2D");
-    st = spec_round(cols ? (const uint16_t *)(s + off[0]) : nullptr, cols, V, k,
-                    cols ? (uint16_t *)(s + off[3]) : nullptr, cols ? (int32_t *)(s + off[4]) : nullptr,
-                    lanes ? (const uint16_t *)(s + off[1]) : nullptr, lanes ? (const int32_t *)(s + off[2]) : nullptr,
-                    lanes, gamma, lanes ? (int32_t *)(s + off[5]) : nullptr, lanes ? (int32_t *)(s + off[6]) : nullptr);
+    st = launch_round_locked(cols ? (const uint16_t *)(s + off[0]) : nullptr, cols, V, k, nullptr,
+                             cols ? (uint16_t *)(s + off[3]) : nullptr, cols ? (int32_t *)(s + off[4]) : nullptr,
+                             lanes ? (const uint16_t *)(s + off[1]) : nullptr,
+                             lanes ? (const int32_t *)(s + off[2]) : nullptr, lanes, gamma, V,
+                             lanes ? (int32_t *)(s + off[5]) : nullptr, lanes ? (int32_t *)(s + off[6]) : nullptr);
     if (st != SPEC_OK) return st;
     if (cols) e = cudaMemcpyAsync(out_vals, s + off[3], b_v, cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess && cols) e = cudaMemcpyAsync(out_ids, s + off[4], b_i, cudaMemcpyDeviceToHost, stream);
@@ -735,13 +744,12 @@ extern "C" spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t 
     st = check_verify_args(target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids);
     if (st != SPEC_OK) return st;
     if (cols == 0 && lanes == 0) return SPEC_OK;
+    // each term alone first: their sum could overflow for huge sizes
+    if (cols > kNoAllocMaxCols || lanes > kNoAllocMaxLanes || lanes * (gamma + 1) > kNoAllocMaxCols - cols)
+        return fail(SPEC_ERR_ARG, "spec_round_noalloc: %lld draft columns and %lld lanes of %d target columns "
+                    "exceed its fixed scratch limits (%lld columns in all, %lld lanes)", (long long)cols,
+                    (long long)lanes, gamma + 1, (long long)kNoAllocMaxCols, (long long)kNoAllocMaxLanes);
     const int64_t t_cols = lanes * (gamma + 1);
-    if (cols + t_cols > kNoAllocMaxCols)
-        return fail(SPEC_ERR_ARG, "spec_round_noalloc: %lld draft + target columns exceed its fixed scratch "
-                    "limit of %lld", (long long)(cols + t_cols), (long long)kNoAllocMaxCols);
-    if (lanes > kNoAllocMaxLanes)
-        return fail(SPEC_ERR_ARG, "spec_round_noalloc: %lld lanes exceed its fixed scratch limit of %lld",
-                    (long long)lanes, (long long)kNoAllocMaxLanes);
 
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceState *d = nullptr;

@@ -111,3 +111,21 @@ def test_sampled_verify_argument_checks(sd):
     assert lib.spec_verify_sampled(P, P, 1, 2, 100, 1.0, 0.95, 20, None, P, P) == sd.SPEC_ERR_ARG
     assert lib.spec_verify_sampled(P, P, 1, 2, 100, 1.0, 0.95, 20, P + 4, P, P) == sd.SPEC_ERR_ARG
     assert lib.spec_verify_sampled(None, None, 0, 2, 100, 1.0, 0.95, 20, None, None, None) == sd.SPEC_OK
+
+
+def test_noalloc_limits_checked_per_term_on_host(sd):
+    """spec_round_noalloc rejects sizes beyond its fixed scratch on the host,
+    each term on its own, so no sum of huge sizes can wrap past the check."""
+    lib = sd.lib
+    P = 0x100000          # never dereferenced: every call below fails its checks first
+    A = sd.SPEC_ERR_ARG
+    assert lib.spec_round_noalloc(P, 9000, 1000, 8, P, P, P, P, 1, 7, P, P) == A       # draft columns alone
+    assert "8192" in sd.spec_last_error()
+    assert lib.spec_round_noalloc(P, 1, 1000, 8, P, P, P, P, 513, 1, P, P) == A        # lanes alone
+    assert "512" in sd.spec_last_error()
+    assert lib.spec_round_noalloc(P, 8000, 1000, 8, P, P, P, P, 64, 7, P, P) == A      # the sum
+    # lanes * (gamma + 1) near 2^63 with V = 1: passes the generic size checks,
+    # and cols + lanes * (gamma + 1) would wrap negative
+    huge = (2 ** 63 - 1) // 2 - 8
+    assert lib.spec_round_noalloc(P, 100, 1, 1, P, P, P, P, huge, 1, P, P) == A
+    assert lib.spec_launch_count() == 0

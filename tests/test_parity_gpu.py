@@ -89,29 +89,40 @@ def _torch_topk_properties(x_dev, V, k, vals, ids):
     del cols
 
 
-def test_c5_full_size_sampled():
-    """3,840 x 248,046 draft columns (k = 64) and 256 x 16 verify columns in
-    one launch; every column checked by properties on the device, 64 sampled
-    columns and every verify lane against the oracle."""
+@pytest.fixture(scope="module")
+def c5_inputs():
+    """The full C5 round (3,840 draft columns, 256 lanes x 16 target columns,
+    V = 248,046), drawn once and kept on the device for every k and kernel."""
+    r = synth.make_c5(k=8)
+    x, t = gu.dev_u16(r.draft), gu.dev_u16(r.target)
+    want_v = oracle.verify(r.target, r.drafts)
+    assert want_v[0].tolist() == r.planted_accept.tolist()
+    return r, x, t, gu.dev_i32(r.drafts), want_v
+
+
+@pytest.mark.parametrize("k", [1, 8, 20, 64])
+def test_c5_full_size_sampled(c5_inputs, k):
+    """The whole C5 round in one launch at every k of the sweep: every column
+    checked by properties on the device, 64 seeded columns and every verify
+    lane against the oracle."""
     import torch
     sd = gu.sd_module()
-    r = synth.make_c5(k=64)
-    cols, V, k = r.cols, r.V, r.k
-    x = gu.dev_u16(r.draft)
-    t = gu.dev_u16(r.target)
-    vals = torch.empty((cols, k), dtype=torch.int16, device="cuda")
-    ids = torch.empty((cols, k), dtype=torch.int32, device="cuda")
-    acc = torch.empty(r.lanes, dtype=torch.int32, device="cuda")
-    com = torch.empty((r.lanes, r.gamma + 1), dtype=torch.int32, device="cuda")
-    sd.spec_round(x, cols, V, k, vals, ids, t, gu.dev_i32(r.drafts), r.lanes, r.gamma, acc, com)
+    r, x, t, d, (wa, wc) = c5_inputs
+    cols, V = r.cols, r.V
+    vals = torch.full((cols, k), 0x5A5A, dtype=torch.int16, device="cuda")
+    ids = torch.full((cols, k), -7, dtype=torch.int32, device="cuda")
+    acc = torch.full((r.lanes,), -7, dtype=torch.int32, device="cuda")
+    com = torch.full((r.lanes, r.gamma + 1), -7, dtype=torch.int32, device="cuda")
+    sd.spec_round(x, cols, V, k, vals, ids, t, d, r.lanes, r.gamma, acc, com)
     torch.cuda.synchronize()
+    sd.spec_device_status()
     for c0 in range(0, cols, 256):
         _torch_topk_properties(x[c0:c0 + 256], V, k, vals[c0:c0 + 256], ids[c0:c0 + 256])
-    pick = np.sort(synth.rng(99, 0).choice(cols, size=64, replace=False))
+    pick = np.sort(synth.rng(99, k).choice(cols, size=64, replace=False))
     wv, wi = oracle.topk(r.draft[pick], k)
-    gu.assert_topk_equal((vals.cpu().numpy().view(np.uint16)[pick], ids.cpu().numpy()[pick]), (wv, wi), "C5 sampled")
-    gu.assert_verify_equal((acc.cpu().numpy(), com.cpu().numpy()), oracle.verify(r.target, r.drafts), "C5 verify")
-    assert acc.cpu().numpy().tolist() == r.planted_accept.tolist()
+    gu.assert_topk_equal((vals.cpu().numpy().view(np.uint16)[pick], ids.cpu().numpy()[pick]), (wv, wi),
+                         f"C5 k={k} sampled columns")
+    gu.assert_verify_equal((acc.cpu().numpy(), com.cpu().numpy()), (wa, wc), f"C5 k={k} verify")
 
 
 @pytest.mark.parametrize("k", [1, 8, 20, 64])
@@ -121,25 +132,59 @@ def test_c5_shortlist_reduced(k):
     gu.assert_topk_equal(got, oracle.topk_mapped(r.draft, k, r.id_map), f"C5s k={k}")
 
 
-def test_c5_shortlist_full_size_sampled():
+@pytest.fixture(scope="module")
+def c5s_inputs():
+    """The full shortlist round (3,840 x 131,072 columns and the id map),
+    drawn once and kept on the device."""
+    r = synth.make_c5s(k=8)
+    return r, gu.dev_u16(r.draft), gu.dev_i32(r.id_map)
+
+
+@pytest.mark.parametrize("k", [1, 8, 20, 64])
+def test_c5_shortlist_full_size_sampled(c5s_inputs, k):
+    """spec_topk_mapped on the full shortlist round at every k: 96 seeded
+    columns against the oracle, and every column: ids in the map's image,
+    values the mapped elements' own bits, non-increasing."""
     import torch
     sd = gu.sd_module()
-    r = synth.make_c5s(k=20)
-    cols, V, k = r.cols, r.V, r.k
-    x = gu.dev_u16(r.draft)
-    vals = torch.empty((cols, k), dtype=torch.int16, device="cuda")
-    ids = torch.empty((cols, k), dtype=torch.int32, device="cuda")
-    sd.spec_topk_mapped(x, cols, V, k, gu.dev_i32(r.id_map), vals, ids)
+    r, x, m = c5s_inputs
+    cols, V = r.cols, r.V
+    vals = torch.full((cols, k), 0x5A5A, dtype=torch.int16, device="cuda")
+    ids = torch.full((cols, k), -7, dtype=torch.int32, device="cuda")
+    sd.spec_topk_mapped(x, cols, V, k, m, vals, ids)
     torch.cuda.synchronize()
-    pick = np.sort(synth.rng(98, 0).choice(cols, size=96, replace=False))
+    sd.spec_device_status()
+    pick = np.sort(synth.rng(98, k).choice(cols, size=96, replace=False))
     gu.assert_topk_equal((vals.cpu().numpy().view(np.uint16)[pick], ids.cpu().numpy()[pick]),
-                         oracle.topk_mapped(r.draft[pick], k, r.id_map), "C5s sampled")
-    # every column: mapped ids lie in the map's image and values match
+                         oracle.topk_mapped(r.draft[pick], k, r.id_map), f"C5s k={k} sampled columns")
     inv = torch.full((synth.VOCAB,), -1, dtype=torch.int64, device="cuda")
-    inv[gu.dev_i32(r.id_map).long()] = torch.arange(V, device="cuda")
+    inv[m.long()] = torch.arange(V, device="cuda")
     loc = inv[ids.long()]
     assert int(loc.min()) >= 0
     assert torch.equal(torch.gather(x, 1, loc), vals)
+    vf = (vals.to(torch.int32) & 0xFFFF).bitwise_left_shift(16).view(torch.float32)
+    assert bool((vf[:, 1:] <= vf[:, :-1]).all())
+
+
+@pytest.mark.parametrize("name", ["C1", "C2"])
+def test_spec_verify_fixed_vocabulary(name):
+    """spec_verify, the call with no V argument (it runs over the pages'
+    248,046-token vocabulary), on the C1 and C2 target columns."""
+    import torch
+    sd = gu.sd_module()
+    r = synth.CONFIGS[name]()
+    assert r.V == sd.SPEC_VOCAB
+    t = gu.dev_u16(r.target, 3)
+    acc = gu.Guarded(r.lanes, torch.int32)
+    com = gu.Guarded(r.lanes * (r.gamma + 1), torch.int32)
+    sd.spec_verify(t, gu.dev_i32(r.drafts), r.lanes, r.gamma, acc.view, com.view)
+    torch.cuda.synchronize()
+    sd.spec_device_status()
+    acc.check_guards()
+    com.check_guards()
+    got = (acc.host(), com.host().reshape(r.lanes, r.gamma + 1))
+    gu.assert_verify_equal(got, oracle.verify(r.target, r.drafts), f"{name} spec_verify")
+    assert got[0].tolist() == r.planted_accept.tolist()
 
 
 # ---------------------------------------------------------------------------

@@ -6,8 +6,9 @@ the library, shared by every call.
 
 The test calls it through the C ABI twice in a row, on different inputs, and
 checks each result bit for bit against spec_round (the allocating entry
-point).  It lives in a file of its own that pytest collects last, and it
-passes alone in a fresh process as well as after the other tests.
+point) and against the CPU oracle.  It lives in a file of its own that
+pytest collects last, and it passes alone in a fresh process as well as
+after the other tests.
 """
 from __future__ import annotations
 
@@ -16,6 +17,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 import synth
 from tests import gpu_util as gu
 
@@ -66,6 +68,10 @@ def test_noalloc_matches_spec_round_twice_in_a_row(sd, which):
         got = _call(sd, sd.lib.spec_round_noalloc, r, k, x, t, d, _outputs(r, k))
         for g_, w_ in zip(got, want):
             assert np.array_equal(g_, w_)
+        ov, oi = oracle.topk(r.draft, k)
+        oa, oc = oracle.verify(r.target, r.drafts)
+        assert np.array_equal(got[0].view(np.uint16), ov) and np.array_equal(got[1], oi)
+        assert np.array_equal(got[2], oa) and np.array_equal(got[3], oc)
         assert got[2].tolist() == r.planted_accept.tolist()
 
 
