@@ -347,3 +347,38 @@ def planted_verify(seed: int, lanes: int, gamma: int, V: int, sigma: float = 3.0
         accept = rng(seed, _S_MISC).integers(0, gamma + 1, size=lanes).astype(np.int32)
     drafts = _plant_drafts(seed, t_arg, accept, V)
     return tgt, drafts, np.asarray(accept, dtype=np.int32), t_arg
+
+
+# ----------------------------------------------------------------------------
+# Q4 shortlist head (weights, scales, hidden states)
+# ----------------------------------------------------------------------------
+
+HIDDEN = 5120           # hidden width that gives the head's size: 131,072 x (2,560 + 160) B = 356.5 MB
+_S_HEAD = 4 << 24
+
+
+def q4_head(seed: int, rows: int = SHORTLIST, d: int = HIDDEN, scale_lo: float = 0.006,
+            scale_hi: float = 0.012, rows_per_stream: int = 4096):
+    """A synthetic Q4 head: packed nibbles uint8 [rows][d/2] (uniform bytes:
+    every nibble 0..15, i.e. weights -8..7) and fp16 scale bit patterns
+    [rows][d/64] uniform in [scale_lo, scale_hi] (rounded to fp16).  With
+    N(0,1) hidden states the logits come out near N(0, 3^2).  One Philox
+    stream per block of rows."""
+    assert d % 64 == 0
+    wq = np.empty((rows, d // 2), dtype=np.uint8)
+    sc = np.empty((rows, d // 64), dtype=np.uint16)
+    for r0 in range(0, rows, rows_per_stream):
+        r1 = min(rows, r0 + rows_per_stream)
+        g = rng(seed, _S_HEAD + r0 // rows_per_stream)
+        wq[r0:r1] = g.integers(0, 256, size=(r1 - r0, d // 2), dtype=np.uint8)
+        s = g.uniform(scale_lo, scale_hi, size=(r1 - r0, d // 64)).astype(np.float16)
+        sc[r0:r1] = s.view(np.uint16)
+    return wq, sc
+
+
+def hidden_states(seed: int, cols: int, d: int = HIDDEN) -> np.ndarray:
+    """bf16 bit patterns [cols][d], N(0,1) rounded to bf16 (RNE)."""
+    out = np.empty((cols, d), dtype=np.uint16)
+    for c in range(cols):
+        out[c] = f32_to_bf16_bits(rng(seed, _S_HEAD + (1 << 20) + c).standard_normal(d, dtype=np.float32))
+    return out
