@@ -230,6 +230,51 @@ spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t cols, int64
                                const uint16_t *target_logits, const int32_t *drafts, int64_t lanes,
                                int32_t gamma, int32_t *out_accept_len, int32_t *out_commit_ids);
 
+/* ---- The Q4 shortlist head ("A drafter inside the artifact", Ignis DFlash2
+ * page, section "How it works", second paragraph: an opt-in 4-bit head over
+ * the 131,072 most frequent tokens, about 356 MB, in place of the drafter's
+ * full output head).  The page gives the bit width, the row count and the
+ * size; the layout below is the reading taken (with a hidden width d of 5,120
+ * it gives 131,072 x (2,560 + 160) bytes = 356.5 MB):
+ *   weights  uint8 [rows][d/2]: byte j of a row holds weight 2j in its low
+ *            nibble and weight 2j+1 in its high nibble; a nibble n stands for
+ *            the integer n - 8;
+ *   scales   fp16 bit patterns [rows][d/64]: scale b multiplies weights
+ *            64b .. 64b+63 of its row.
+ * The logit of row i for a hidden state h (bf16, length d) is
+ *   sum_b scale[i][b] * sum_{j in block b} (n_ij - 8) * h_j,
+ * summed in fp32 (each 64-weight block's products on the tensor cores, then
+ * scaled and added) and rounded once to bf16, to nearest even.  It differs
+ * from the exact value by at most half a bf16 unit plus 2^-16 times
+ * sum_j |scale (n_ij - 8) h_j| (the bound the tests hold it to).
+ * rows: a positive multiple of 16 below 2^31; d: a multiple of 64, at most 6,144. */
+
+/* Reorder a head into the layout the logits kernel streams (once, at load):
+ *   weights, scales  the head as above (device memory, caller-owned);
+ *   wpack            device, rows*d/2 bytes, 16-byte aligned (the same size as weights);
+ *   spack            device, rows*(d/64)*2 bytes, 4-byte aligned (the same size as scales).
+ * Enqueued on the calling thread's stream; SPEC_ERR_ARG for bad sizes, null or
+ * misaligned pointers. */
+spec_status spec_shortlist_pack(const uint8_t *weights, const uint16_t *scales, int64_t rows, int64_t d,
+                                void *wpack, void *spack);
+
+/* The head's logits: hidden bf16 [cols][d] (4-byte aligned) -> out_logits
+ * bf16 [cols][rows] (row i of column c at c*rows + i).  wpack/spack from
+ * spec_shortlist_pack.  One launch per 16 hidden states, each streaming the
+ * packed head once.  cols == 0 is a no-op. */
+spec_status spec_shortlist_logits(const uint16_t *hidden, int64_t cols, int64_t d, const void *wpack,
+                                  const void *spack, int64_t rows, uint16_t *out_logits);
+
+/* The shortlist proposal of each hidden state: its logits (as
+ * spec_shortlist_logits, into the caller's logits buffer [cols][rows], which
+ * the call uses as its workspace and leaves filled), then spec_topk_mapped
+ * over them with id_map [rows] (local row -> vocabulary id, injective): the k
+ * largest, ties to the smaller vocabulary id, out_ids vocabulary ids.
+ * 1 <= k <= min(rows, 64).  The top-k is bit-exact on the logits it leaves. */
+spec_status spec_shortlist_topk(const uint16_t *hidden, int64_t cols, int64_t d, const void *wpack,
+                                const void *spack, int64_t rows, const int32_t *id_map, int32_t k,
+                                uint16_t *logits, uint16_t *out_vals, int32_t *out_ids);
+
 /* Which streaming kernel runs a round.  Both compute the same results (every
  * output is the unique exact answer); they differ only in speed:
  *   SPEC_KERNEL_CTA  -- the CTAs of a full-GPU grid each stream a contiguous

@@ -29,6 +29,7 @@ __all__ = [
     "spec_set_kernel", "spec_get_kernel", "SPEC_KERNEL_AUTO", "SPEC_KERNEL_WARP", "SPEC_KERNEL_CTA",
     "spec_set_stream", "spec_get_stream", "spec_reserve", "spec_release", "spec_last_error",
     "spec_launch_count", "spec_device_status", "topk", "topk_mapped", "verify", "round_step", "EXPORTS",
+    "spec_shortlist_pack", "spec_shortlist_logits", "spec_shortlist_topk",
 ]
 
 SPEC_OK, SPEC_ERR_ARG, SPEC_ERR_ALLOC, SPEC_ERR_CUDA = 0, -1, -2, -3
@@ -65,6 +66,9 @@ _SIGS = {
     "spec_launch_count": [],
     "spec_device_status": [],
     "spec_selftest_wait_timeout": [_i64, _p],
+    "spec_shortlist_pack": [_p, _p, _i64, _i64, _p, _p],
+    "spec_shortlist_logits": [_p, _i64, _i64, _p, _p, _i64, _p],
+    "spec_shortlist_topk": [_p, _i64, _i64, _p, _p, _i64, _p, _i32, _p, _p, _p],
 }
 EXPORTS = tuple(_SIGS)
 for _name, _args in _SIGS.items():
@@ -267,6 +271,41 @@ def spec_round_host(draft_logits, cols, V, k, out_vals, out_ids, target_logits, 
     t, d, a, c = _verify_bufs(_host, target_logits, drafts, lanes, gamma, V, out_accept_len, out_commit_ids)
     _use_torch_stream()
     _check(lib.spec_round_host(x, cols, V, k, v, i, t, d, lanes, gamma, a, c))
+
+
+def spec_shortlist_pack(weights, scales, rows, d, wpack, spack):
+    """Reorder a Q4 head (uint8 [rows, d/2], fp16 bits [rows, d/64]) into the
+    streamed layout (buffers of the same sizes)."""
+    r, dd = _n(rows), _n(d)
+    w = _dev(weights, r * (dd // 2), 1, "weights")
+    sc = _dev(scales, r * (dd // 64), 2, "scales")
+    wp = _dev(wpack, r * (dd // 2), 1, "wpack")
+    sp = _dev(spack, r * (dd // 64), 2, "spack")
+    _use_torch_stream()
+    _check(lib.spec_shortlist_pack(w, sc, rows, d, wp, sp))
+
+
+def _head_bufs(hidden, cols, d, wpack, spack, rows):
+    c, r, dd = _n(cols), _n(rows), _n(d)
+    return (_dev(hidden, c * dd, 2, "hidden"), _dev(wpack, r * (dd // 2), 1, "wpack"),
+            _dev(spack, r * (dd // 64), 2, "spack"))
+
+
+def spec_shortlist_logits(hidden, cols, d, wpack, spack, rows, out_logits):
+    h, wp, sp = _head_bufs(hidden, cols, d, wpack, spack, rows)
+    lg = _dev(out_logits, _n(cols) * _n(rows), 2, "out_logits")
+    _use_torch_stream()
+    _check(lib.spec_shortlist_logits(h, cols, d, wp, sp, rows, lg))
+
+
+def spec_shortlist_topk(hidden, cols, d, wpack, spack, rows, id_map, k, logits, out_vals, out_ids):
+    h, wp, sp = _head_bufs(hidden, cols, d, wpack, spack, rows)
+    lg = _dev(logits, _n(cols) * _n(rows), 2, "logits")
+    m = _dev(id_map, _n(rows), 4, "id_map")
+    v = _dev(out_vals, _n(cols) * _n(k), 2, "out_vals")
+    i = _dev(out_ids, _n(cols) * _n(k), 4, "out_ids")
+    _use_torch_stream()
+    _check(lib.spec_shortlist_topk(h, cols, d, wp, sp, rows, m, k, lg, v, i))
 
 
 def spec_set_kernel(which: int):

@@ -30,6 +30,7 @@
 #include "common.cuh"
 #include "round_cta.cuh"
 #include "round_warp.cuh"
+#include "head_q4.cuh"
 
 namespace {
 
@@ -591,6 +592,129 @@ spec_status spec_round_host(const uint16_t *draft_logits, int64_t cols, int64_t 
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     return SPEC_OK;
 }
+
+}  // extern "C"
+
+// ---- the Q4 shortlist head ---------------------------------------------------
+
+namespace {
+
+spec_status check_head(int64_t rows, int64_t d, const void *wpack, const void *spack)
+{
+    if (rows < 16 || rows % 16 != 0 || rows > INT32_MAX)
+        return fail(SPEC_ERR_ARG, "rows = %lld: need a positive multiple of 16 below 2^31", (long long)rows);
+    if (d < 64 || d % 64 != 0 || d > q4::kMaxD)
+        return fail(SPEC_ERR_ARG, "d = %lld: need a multiple of 64 in [64, %lld]", (long long)d, (long long)q4::kMaxD);
+    if (!wpack || !spack) return fail(SPEC_ERR_ARG, "null pointer");
+    if (misaligned(wpack, 16) || misaligned(spack, 4))
+        return fail(SPEC_ERR_ARG, "misaligned packed head (weights need 16 bytes, scales 4)");
+    return SPEC_OK;
+}
+
+// The head's logits for hidden states [cols][d] into logits [cols][rows],
+// kColsPass hidden states per launch.  The caller holds g_mu.
+spec_status launch_head_logits(const uint16_t *hidden, int64_t cols, int64_t d, const void *wpack, const void *spack,
+                               int64_t rows, uint16_t *logits, cudaStream_t stream)
+{
+    DeviceState *dv = nullptr;
+    spec_status st = device_state(&dv);
+    if (st != SPEC_OK) return st;
+    static bool attr_set[kMaxDevices] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!attr_set[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(q4::logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)q4::smem_bytes(q4::kMaxD));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+        attr_set[dev] = true;
+    }
+    const int64_t tiles = rows / 16;
+    int64_t grid = (int64_t)dv->sms;
+    const int64_t need = (tiles + q4::kWarps - 1) / q4::kWarps;
+    if (grid > need) grid = need;
+    for (int64_t c0 = 0; c0 < cols; c0 += q4::kColsPass) {
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(q4::kThreads);
+        cfg.dynamicSmemBytes = q4::smem_bytes(d);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, q4::logits_kernel, hidden, cols, d,
+                                                 static_cast<const uint4 *>(wpack), static_cast<const uint32_t *>(spack),
+                                                 rows, c0, logits);
+        if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
+    return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+spec_status spec_shortlist_pack(const uint8_t *weights, const uint16_t *scales, int64_t rows, int64_t d,
+                                void *wpack, void *spack)
+{
+    t_err.clear();
+    spec_status st = check_head(rows, d, wpack, spack);
+    if (st != SPEC_OK) return st;
+    if (!weights || !scales) return fail(SPEC_ERR_ARG, "null pointer");
+    if (misaligned(scales, 2)) return fail(SPEC_ERR_ARG, "misaligned scales");
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState *dv = nullptr;
+    st = device_state(&dv);
+    if (st != SPEC_OK) return st;
+    q4::pack_kernel<<<dv->sms * 4, 256, 0, t_stream>>>(weights, scales, rows, d, static_cast<uint32_t *>(wpack),
+                                                         static_cast<uint32_t *>(spack));
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return SPEC_OK;
+}
+
+spec_status spec_shortlist_logits(const uint16_t *hidden, int64_t cols, int64_t d, const void *wpack,
+                                  const void *spack, int64_t rows, uint16_t *out_logits)
+{
+    t_err.clear();
+    if (cols < 0) return fail(SPEC_ERR_ARG, "cols = %lld < 0", (long long)cols);
+    spec_status st = check_head(rows, d, wpack, spack);
+    if (st != SPEC_OK) return st;
+    if (cols == 0) return SPEC_OK;
+    if (!hidden || !out_logits) return fail(SPEC_ERR_ARG, "null pointer");
+    if (misaligned(hidden, 4) || misaligned(out_logits, 2))
+        return fail(SPEC_ERR_ARG, "misaligned pointer (hidden states need 4 bytes, logits 2)");
+    std::lock_guard<std::mutex> lock(g_mu);
+    return launch_head_logits(hidden, cols, d, wpack, spack, rows, out_logits, t_stream);
+}
+
+spec_status spec_shortlist_topk(const uint16_t *hidden, int64_t cols, int64_t d, const void *wpack,
+                                const void *spack, int64_t rows, const int32_t *id_map, int32_t k,
+                                uint16_t *logits, uint16_t *out_vals, int32_t *out_ids)
+{
+    t_err.clear();
+    if (cols < 0) return fail(SPEC_ERR_ARG, "cols = %lld < 0", (long long)cols);
+    spec_status st = check_head(rows, d, wpack, spack);
+    if (st != SPEC_OK) return st;
+    st = check_topk_args(logits, cols, rows, k, out_vals, out_ids);
+    if (st != SPEC_OK) return st;
+    if (cols == 0) return SPEC_OK;
+    if (!hidden || misaligned(hidden, 4)) return fail(SPEC_ERR_ARG, "hidden states null or misaligned (4 bytes)");
+    if (!id_map || misaligned(id_map, 4)) return fail(SPEC_ERR_ARG, "id_map null or misaligned");
+    std::lock_guard<std::mutex> lock(g_mu);
+    st = launch_head_logits(hidden, cols, d, wpack, spack, rows, logits, t_stream);
+    if (st != SPEC_OK) return st;
+    return launch_round_locked(logits, cols, rows, k, id_map, out_vals, out_ids, nullptr, nullptr, 0, 1, 1, nullptr,
+                               nullptr);
+}
+
+}  // extern "C"
+
+extern "C" {
 
 spec_status spec_set_kernel(int32_t which)
 {

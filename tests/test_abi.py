@@ -129,3 +129,17 @@ def test_noalloc_limits_checked_per_term_on_host(sd):
     huge = (2 ** 63 - 1) // 2 - 8
     assert lib.spec_round_noalloc(P, 100, 1, 1, P, P, P, P, huge, 1, P, P) == A
     assert lib.spec_launch_count() == 0
+
+
+def test_shortlist_head_argument_checks(sd):
+    lib = sd.lib
+    P = 0x100000          # never dereferenced: every call below fails its checks first
+    A = sd.SPEC_ERR_ARG
+    assert lib.spec_shortlist_pack(P, P, 24, 128, P, P) == A        # rows not a multiple of 16
+    assert lib.spec_shortlist_pack(P, P, 32, 96, P, P) == A         # d not a multiple of 64
+    assert lib.spec_shortlist_pack(P, P, 32, 8192, P, P) == A       # d above the staged maximum
+    assert lib.spec_shortlist_pack(P, P, 32, 128, P + 8, P) == A    # packed weights not 16-byte aligned
+    assert lib.spec_shortlist_logits(P + 2, 1, 128, P, P, 32, P) == A   # hidden not 4-byte aligned
+    assert lib.spec_shortlist_topk(P, 1, 128, P, P, 32, P, 33, P, P, P) == A   # k > rows
+    assert lib.spec_shortlist_logits(None, 0, 128, P, P, 32, None) == sd.SPEC_OK
+    assert lib.spec_launch_count() == 0
