@@ -78,6 +78,9 @@ def parse_args(argv=None):
                    help="verify by speculative sampling (T 1.0, top_p 0.95, top_k 20, one-hot drafts; "
                         "spec_round_sampled) instead of greedy; measures the kernel line only (no e2e, no CPU arm)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--head", type=int, default=0, metavar="N",
+                   help="instead of a round: N hidden states through the full Q4 shortlist head "
+                        "(131,072 x 5,120, 356.5 MB) and the mapped top-k (k=8), spec_shortlist_topk")
     p.add_argument("--no-also", action="store_true",
                    help="skip the extra kernel timings of C1 and C4 that the default C2 run reports under 'also'")
     return p.parse_args(argv)
@@ -664,10 +667,89 @@ def run_ours(args):
     return 0
 
 
+def run_head(args):
+    """The Q4 shortlist head workload: N hidden states (5,120 wide, N(0,1))
+    through the full head (131,072 rows, 356.5 MB of packed weights and
+    scales, larger than L2, so every call streams it from HBM) into logits,
+    then the mapped top-k (k = 8).  One spec_shortlist_topk per step."""
+    import numpy as np
+    import torch
+    import synth
+    import speculative_decoding_draft_column_gb300 as sd
+    world, rank, local = dist_env()
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device (there is no CPU fallback)"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cols, k = args.head, 8
+    rows, d = synth.SHORTLIST, synth.HIDDEN
+    wq, sc = synth.q4_head(41 + rank)
+    h = synth.hidden_states(42 + rank, cols, d)
+    id_map = synth.shortlist_map(43)
+    w = torch.from_numpy(wq).to(dev)
+    s = torch.from_numpy(sc.view(np.int16)).to(dev)
+    wp, sp = torch.empty_like(w), torch.empty_like(s)
+    sd.spec_shortlist_pack(w, s, rows, d, wp, sp)
+    del w, s
+    hd = torch.from_numpy(h.view(np.int16)).to(dev)
+    m = torch.from_numpy(id_map).to(dev)
+    lg = torch.empty((cols, rows), dtype=torch.int16, device=dev)
+    vals = torch.empty((cols, k), dtype=torch.int16, device=dev)
+    ids = torch.empty((cols, k), dtype=torch.int32, device=dev)
+    sd.spec_reserve(cols, k, 0, 1)
+    stream = torch.cuda.Stream(device=dev)
+
+    def one(i):
+        sd.spec_shortlist_topk(hd, cols, d, wp, sp, rows, m, k, lg, vals, ids)
+
+    def logits_only(i):
+        sd.spec_shortlist_logits(hd, cols, d, wp, sp, rows, lg)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            one(i)
+    stream.synchronize()
+    K = args.steps
+    uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
+    clocks.start()
+    us = replay_us(one, K, 1, stream, sd)
+    us_logits = replay_us(logits_only, K, 1, stream, sd)
+    clk = clocks.stop()
+    head_bytes = wq.nbytes + sc.nbytes
+    passes = -(-cols // 16)
+    peak, peak_src = hbm_peak()
+    tflops = 2.0 * rows * d * cols / (us_logits * 1e-6) / 1e12
+    line = {
+        "metric": "µs per call and head GB/s, Q4 shortlist head logits + mapped top-k", "value": round(us, 3),
+        "unit": "µs", "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 6),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x int4 -> fp32",
+        "data": "synthetic (seeded; see synth/)",
+        "config": {"workload": f"{cols} hidden states x 5,120 (bf16 N(0,1)) through the Q4 shortlist head "
+                               f"(131,072 rows; 4-bit weights, fp16 scale per 64; 356.5 MB), mapped top-k k={k}",
+                   "l2": "the head (356.5 MB) exceeds the L2: every call streams it from HBM",
+                   "launch": f"spec_shortlist_topk: {passes} logits launch(es) of up to 16 hidden states, "
+                             "then one spec_topk_mapped launch; K calls replayed as CUDA graphs"},
+        "us_logits": round(us_logits, 3), "us_topk": round(us - us_logits, 3),
+        "roofline": {"bound": "hbm", "kernel": "q4::logits_kernel",
+                     "achieved": round(head_bytes * passes / (us_logits * 1e-6) / 1e9, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(head_bytes * passes / (us_logits * 1e-6) / 1e9 / peak, 4),
+                     "peak_source": peak_src, "traffic": None,
+                     "algorithmic_bytes_per_launch": head_bytes,
+                     "head_passes_per_call": passes, "tensor_tflops": round(tflops, 1)},
+        "gpu_launches": int(K * (passes + 1)),
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.head:
+        return run_head(args)
     return run_ours(args)
 
 

@@ -258,7 +258,7 @@ spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t cols, int64
 spec_status spec_shortlist_pack(const uint8_t *weights, const uint16_t *scales, int64_t rows, int64_t d,
                                 void *wpack, void *spack);
 
-/* The head's logits: hidden bf16 [cols][d] (4-byte aligned) -> out_logits
+/* The head's logits: hidden bf16 [cols][d] (16-byte aligned) -> out_logits
  * bf16 [cols][rows] (row i of column c at c*rows + i).  wpack/spack from
  * spec_shortlist_pack.  One launch per 16 hidden states, each streaming the
  * packed head once.  cols == 0 is a no-op. */

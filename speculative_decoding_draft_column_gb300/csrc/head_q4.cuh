@@ -13,9 +13,11 @@
 // loads one 16-byte word per tile and block (coalesced, 512 B a warp) and
 // turns two nibbles into a bf16 pair with one lop3 and one subtraction:
 // bf16 0x4300 | n is 128 + n, and 128 + n - 136 = n - 8 exactly.  The
-// block's products are summed by the tensor cores in fp32 from zero, and the
-// block's per-row scale is applied in registers (one FMA per accumulator), so
-// every 64-weight partial sum gets its own scale.  A TMEM accumulator
+// block's products are summed by the tensor cores in fp32 (each k16 step from
+// zero into an accumulator of its own, so that the four MMAs of a block do not
+// wait on each other, then the four added), and the block's per-row scale is
+// applied in registers (one FMA per accumulator), so every 64-weight partial
+// sum gets its own scale.  A TMEM accumulator
 // (tcgen05) would need a TMEM round trip per block and tile for that, which
 // is why this contraction stays on the register-accumulator MMA.
 #pragma once
@@ -28,11 +30,12 @@ constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kNT = 2;                    // n-tiles of 8 hidden states per pass
 constexpr int kColsPass = 8 * kNT;        // hidden states per pass over the head
-constexpr int kAhead = 8;                 // blocks of weights each lane has in flight
+constexpr int kAhead = 8;                 // blocks of weights a lane loads together
 constexpr int kPadWords = 4;              // padding of a staged hidden state (spreads the banks)
 constexpr int64_t kMaxD = 6144;           // staged hidden states must fit in shared memory
 
-inline size_t smem_bytes(int64_t d) { return (size_t)kColsPass * (size_t)(d / 2 + kPadWords) * 4; }
+// staged hidden states (bf16 pairs, padded rows)
+inline size_t smem_bytes(int64_t d, int nt) { return (size_t)(8 * nt) * (size_t)(d / 2 + kPadWords) * 4; }
 
 // One packed word: tile T, block B, lane L = 4g + t, k16 step s holds the
 // nibbles of (row 16T+g / 16T+g+8, weight 64B + 16s + 2t + {0, 1, 8, 9}) at
@@ -99,72 +102,91 @@ __device__ __forceinline__ void mma_bf16(float (&dd)[4], const uint32_t (&a)[4],
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
 }
 
-// Logits of hidden states c0 .. c0 + kColsPass - 1 (fewer at the end) for
-// every row of the packed head: logits[c][row] (bf16, round to nearest even
-// from the fp32 sum).  Each warp takes whole tiles of 16 rows.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+
+// Logits of hidden states c0 .. c0 + 8*NT - 1 (fewer at the end) for every
+// row of the packed head: logits[c][row] (bf16, round to nearest even from
+// the fp32 sum).  Each warp takes whole tiles of 16 rows.
+//
+// The weights enter the MMA as their exact values n - 8 (bf16 0x4300 | n is
+// 128 + n; minus 136 exactly): folding the offset out of the sum instead
+// would make every block's sum about 30 times larger than its terms, and its
+// rounding with it.
+template <int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     logits_kernel(const uint16_t *__restrict__ hidden, int64_t cols, int64_t d, const uint4 *__restrict__ wp,
                   const uint32_t *__restrict__ sp, int64_t rows, int64_t c0, uint16_t *__restrict__ logits)
 {
     pdl_launch_dependents();
     pdl_wait();
-    extern __shared__ uint32_t hs[];   // [kColsPass][d/2 + kPadWords]: bf16 pairs of each staged hidden state
-    const int64_t words = d / 2, stride = words + kPadWords;
-    const int nc = (int)(cols - c0 < kColsPass ? cols - c0 : kColsPass);
-    for (int64_t i = threadIdx.x; i < kColsPass * words; i += kThreads) {
-        const int c = (int)(i / words);
-        const int64_t j = i - c * words;
-        hs[c * stride + j] = c < nc ? __ldg(reinterpret_cast<const uint32_t *>(hidden + (c0 + c) * d) + j) : 0u;
+    extern __shared__ uint32_t hs[];   // [8*NT][d/2 + kPadWords] bf16 pairs
+    const int words = (int)(d / 2), stride = words + kPadWords, nb = (int)(d / 64);
+    const int nc = (int)(cols - c0 < 8 * NT ? cols - c0 : 8 * NT);
+    {
+        const int q4w = words / 4;   // 16-byte pieces of a hidden state
+        const uint4 *src = reinterpret_cast<const uint4 *>(hidden + c0 * d);
+        for (int i = threadIdx.x; i < 8 * NT * q4w; i += kThreads) {
+            const int c = i / q4w, j = i - c * q4w;
+            uint4 *dst = reinterpret_cast<uint4 *>(hs + c * stride) + j;
+            if (c < nc) cp_async16(dst, src + (int64_t)c * q4w + j);
+            else *dst = make_uint4(0, 0, 0, 0);
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncthreads();
     }
-    __syncthreads();
 
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
-    const int64_t tiles = rows / 16, nb = d / 64;
+    const int64_t tiles = rows / 16;
     const int64_t nwarps = (int64_t)gridDim.x * kWarps;
     const uint32_t kMask = 0x000F000Fu, kBias = 0x43004300u, kOff = 0x43084308u;   // 128 + n; 136 = 128 + 8
-    const uint32_t *hrow[kNT];
+    const uint32_t *hrow[NT];
 #pragma unroll
-    for (int n = 0; n < kNT; ++n) hrow[n] = hs + (n * 8 + g) * stride + t;
+    for (int n = 0; n < NT; ++n) hrow[n] = hs + (n * 8 + g) * stride + t;
 
     for (int64_t T = (int64_t)blockIdx.x * kWarps + w; T < tiles; T += nwarps) {
         const uint4 *wt = wp + T * nb * 32 + lane;
         const uint32_t *st = sp + T * nb * 8 + g;
-        float acc[kNT][4];
+        float acc[NT][4];
 #pragma unroll
-        for (int n = 0; n < kNT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-        uint4 pw[kAhead];
-        uint32_t ps[kAhead];
-#pragma unroll
-        for (int a = 0; a < kAhead; ++a) {
-            pw[a] = a < nb ? __ldcs(wt + a * 32) : make_uint4(0, 0, 0, 0);
-            ps[a] = a < nb ? __ldg(st + a * 8) : 0u;
-        }
-        for (int64_t B0 = 0; B0 < nb; B0 += kAhead) {
+        for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+        // kAhead blocks of the tile at a time: all their loads first, then
+        // their arithmetic (issued this way the loads stay in flight
+        // together; refilling one slot per block as it is used held the
+        // stream to about a third of the rate)
+        for (int B0 = 0; B0 < nb; B0 += kAhead) {
+            uint4 pw[kAhead];
+            uint32_t ps[kAhead];
 #pragma unroll
             for (int a = 0; a < kAhead; ++a) {
-                const int64_t B = B0 + a;
+                const bool in = B0 + a < nb;
+                pw[a] = in ? __ldcs(wt + (B0 + a) * 32) : make_uint4(0, 0, 0, 0);
+                ps[a] = in ? __ldg(st + (B0 + a) * 8) : 0u;
+            }
+#pragma unroll
+            for (int a = 0; a < kAhead; ++a) {
+                const int B = B0 + a;
                 if (B < nb) {
                     const uint4 wv = pw[a];
                     const uint32_t sv = ps[a];
-                    if (B + kAhead < nb) {   // refill this slot with the block kAhead ahead
-                        pw[a] = __ldcs(wt + (B + kAhead) * 32);
-                        ps[a] = __ldg(st + (B + kAhead) * 8);
-                    }
-                    float dd[kNT][4];
+                    float dd[NT][4];
                     const uint32_t wds[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
                         const uint32_t word = wds[s];
-                        uint32_t ar[4];
+                        const uint32_t ar[4] = {sub_bf16x2(lop3_and_or(word, kMask, kBias), kOff),
+                                                sub_bf16x2(lop3_and_or(word >> 4, kMask, kBias), kOff),
+                                                sub_bf16x2(lop3_and_or(word >> 8, kMask, kBias), kOff),
+                                                sub_bf16x2(lop3_and_or(word >> 12, kMask, kBias), kOff)};
+                        const int kw = B * 32 + 8 * s;   // word offset of k in a staged row
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) ar[r] = sub_bf16x2(lop3_and_or(word >> (4 * r), kMask, kBias), kOff);
-                        const int64_t kw = (B * 64 + 16 * s) / 2;   // word offset of k in a staged row
-#pragma unroll
-                        for (int n = 0; n < kNT; ++n) mma_bf16(dd[n], ar, hrow[n][kw], hrow[n][kw + 4], s == 0);
+                        for (int n = 0; n < NT; ++n) mma_bf16(dd[n], ar, hrow[n][kw], hrow[n][kw + 4], s == 0);
                     }
                     const float s0 = f16_as_float(sv & 0xFFFFu), s1 = f16_as_float(sv >> 16);
 #pragma unroll
-                    for (int n = 0; n < kNT; ++n) {
+                    for (int n = 0; n < NT; ++n) {
                         acc[n][0] = fmaf(s0, dd[n][0], acc[n][0]);
                         acc[n][1] = fmaf(s0, dd[n][1], acc[n][1]);
                         acc[n][2] = fmaf(s1, dd[n][2], acc[n][2]);
@@ -175,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int64_t r0 = T * 16 + g, r1 = r0 + 8;
 #pragma unroll
-        for (int n = 0; n < kNT; ++n) {
+        for (int n = 0; n < NT; ++n) {
             const int cc = n * 8 + 2 * t;
             if (cc < nc) {
                 logits[(c0 + cc) * rows + r0] = bf16_rn(acc[n][0]);

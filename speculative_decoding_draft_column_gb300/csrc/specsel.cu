@@ -623,8 +623,11 @@ spec_status launch_head_logits(const uint16_t *hidden, int64_t cols, int64_t d, 
     int dev = 0;
     cudaGetDevice(&dev);
     if (!attr_set[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(q4::logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)q4::smem_bytes(q4::kMaxD));
+        cudaError_t e = cudaFuncSetAttribute(q4::logits_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)q4::smem_bytes(q4::kMaxD, 1));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(q4::logits_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)q4::smem_bytes(q4::kMaxD, 2));
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         attr_set[dev] = true;
     }
@@ -637,16 +640,20 @@ spec_status launch_head_logits(const uint16_t *hidden, int64_t cols, int64_t d, 
         memset(&cfg, 0, sizeof cfg);
         cfg.gridDim = dim3((unsigned)grid);
         cfg.blockDim = dim3(q4::kThreads);
-        cfg.dynamicSmemBytes = q4::smem_bytes(d);
+        const int nt = cols - c0 > 8 ? 2 : 1;   // one n-tile when at most 8 hidden states are left
+        cfg.dynamicSmemBytes = q4::smem_bytes(d, nt);
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, q4::logits_kernel, hidden, cols, d,
-                                                 static_cast<const uint4 *>(wpack), static_cast<const uint32_t *>(spack),
-                                                 rows, c0, logits);
+        const uint4 *w4 = static_cast<const uint4 *>(wpack);
+        const uint32_t *s4 = static_cast<const uint32_t *>(spack);
+        const cudaError_t e = nt == 2 ? cudaLaunchKernelEx(&cfg, q4::logits_kernel<2>, hidden, cols, d, w4, s4, rows, c0,
+                                                           logits)
+                                      : cudaLaunchKernelEx(&cfg, q4::logits_kernel<1>, hidden, cols, d, w4, s4, rows, c0,
+                                                           logits);
         if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
         g_launches.fetch_add(1, std::memory_order_relaxed);
     }
@@ -686,8 +693,8 @@ spec_status spec_shortlist_logits(const uint16_t *hidden, int64_t cols, int64_t 
     if (st != SPEC_OK) return st;
     if (cols == 0) return SPEC_OK;
     if (!hidden || !out_logits) return fail(SPEC_ERR_ARG, "null pointer");
-    if (misaligned(hidden, 4) || misaligned(out_logits, 2))
-        return fail(SPEC_ERR_ARG, "misaligned pointer (hidden states need 4 bytes, logits 2)");
+    if (misaligned(hidden, 16) || misaligned(out_logits, 2))
+        return fail(SPEC_ERR_ARG, "misaligned pointer (hidden states need 16 bytes, logits 2)");
     std::lock_guard<std::mutex> lock(g_mu);
     return launch_head_logits(hidden, cols, d, wpack, spack, rows, out_logits, t_stream);
 }
@@ -703,7 +710,7 @@ spec_status spec_shortlist_topk(const uint16_t *hidden, int64_t cols, int64_t d,
     st = check_topk_args(logits, cols, rows, k, out_vals, out_ids);
     if (st != SPEC_OK) return st;
     if (cols == 0) return SPEC_OK;
-    if (!hidden || misaligned(hidden, 4)) return fail(SPEC_ERR_ARG, "hidden states null or misaligned (4 bytes)");
+    if (!hidden || misaligned(hidden, 16)) return fail(SPEC_ERR_ARG, "hidden states null or misaligned (16 bytes)");
     if (!id_map || misaligned(id_map, 4)) return fail(SPEC_ERR_ARG, "id_map null or misaligned");
     std::lock_guard<std::mutex> lock(g_mu);
     st = launch_head_logits(hidden, cols, d, wpack, spack, rows, logits, t_stream);
