@@ -152,19 +152,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         float acc[NT][4];
 #pragma unroll
         for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-        // kAhead blocks of the tile at a time: all their loads first, then
-        // their arithmetic (issued this way the loads stay in flight
-        // together; refilling one slot per block as it is used held the
-        // stream to about a third of the rate)
-        for (int B0 = 0; B0 < nb; B0 += kAhead) {
-            uint4 pw[kAhead];
-            uint32_t ps[kAhead];
+        // kAhead blocks of the tile at a time, double buffered: the next
+        // group's loads all go out together before this group's arithmetic
+        // (issued as a group the loads stay in flight together; refilling one
+        // slot per block as it is used held the stream to about a third of
+        // the rate)
+        auto load_group = [&](int B0, uint4 (&pw)[kAhead], uint32_t (&ps)[kAhead]) {
 #pragma unroll
             for (int a = 0; a < kAhead; ++a) {
                 const bool in = B0 + a < nb;
                 pw[a] = in ? __ldcs(wt + (B0 + a) * 32) : make_uint4(0, 0, 0, 0);
                 ps[a] = in ? __ldg(st + (B0 + a) * 8) : 0u;
             }
+        };
+        auto run_group = [&](int B0, const uint4 (&pw)[kAhead], const uint32_t (&ps)[kAhead]) {
 #pragma unroll
             for (int a = 0; a < kAhead; ++a) {
                 const int B = B0 + a;
@@ -194,6 +195,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+        };
+        uint4 pa[kAhead], pb[kAhead];
+        uint32_t sa[kAhead], sb[kAhead];
+        load_group(0, pa, sa);
+        for (int B0 = 0; B0 < nb; B0 += 2 * kAhead) {
+            if (B0 + kAhead < nb) load_group(B0 + kAhead, pb, sb);
+            run_group(B0, pa, sa);
+            if (B0 + kAhead >= nb) break;
+            if (B0 + 2 * kAhead < nb) load_group(B0 + 2 * kAhead, pa, sa);
+            run_group(B0 + kAhead, pb, sb);
         }
         const int64_t r0 = T * 16 + g, r1 = r0 + 8;
 #pragma unroll
