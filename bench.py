@@ -72,7 +72,7 @@ def parse_args(argv=None):
     p.add_argument("--part", default="round", choices=["round", "split", "topk", "verify"],
                    help="round: spec_round, one fused launch (default); split: spec_topk then spec_verify_v, two "
                         "launches a round; topk / verify: that call alone on its own columns")
-    p.add_argument("--kernel", default="auto", choices=["auto", "warp", "cta"],
+    p.add_argument("--kernel", default="auto", choices=["auto", "warp", "cta", "gm"],
                    help="streaming kernel (spec_set_kernel); auto picks by round size")
     p.add_argument("--sampled", action="store_true",
                    help="verify by speculative sampling (T 1.0, top_p 0.95, top_k 20, one-hot drafts; "
@@ -108,16 +108,14 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-# The library runs a round on its CTA-cooperative kernel while the round's
-# logits are at most 6 MiB per SM and on its per-warp kernel above (the
-# automatic choice of spec_set_kernel); the bench names the one that ran.
-CTA_MAX_BYTES_PER_SM = 6 << 20
+# The bench names the kernel that ran, as the library reports it
+# (spec_last_kernel: the kernel of the calling thread's last round launch).
+KERNEL_NAMES = {1: "wrp::spec_round_kernel", 2: "cta::spec_round_kernel", 3: "gm::spec_round_kernel"}
+KERNEL_CHOICES = {"auto": 0, "warp": 1, "cta": 2, "gm": 3}
 
 
-def kernel_name(bytes_round: int, sms: int, forced: str = "auto") -> str:
-    if forced != "auto":
-        return "cta::spec_round_kernel" if forced == "cta" else "wrp::spec_round_kernel"
-    return "cta::spec_round_kernel" if bytes_round <= CTA_MAX_BYTES_PER_SM * sms else "wrp::spec_round_kernel"
+def kernel_name(sd) -> str:
+    return KERNEL_NAMES.get(sd.spec_last_kernel(), "unknown")
 
 
 def recorded_traffic(config: str):
@@ -449,6 +447,7 @@ def also_rounds(dev, stream, sd, peak: float, clocks) -> dict:
             for i in range(5):
                 one(i)
         stream.synchronize()
+        kname = kernel_name(sd)
         us = replay_us(one, K, R, stream, sd)
         b = r.logit_bytes()
         floor_meas, floor_nom = b / (peak * 1e3), b / (NOMINAL_HBM_GBS * 1e3)
@@ -458,7 +457,7 @@ def also_rounds(dev, stream, sd, peak: float, clocks) -> dict:
                      "frac_of_nominal_hbm": round(b / us / 1e3 / NOMINAL_HBM_GBS, 4),
                      "floor_us_measured_hbm": round(floor_meas, 3), "floor_multiple_measured": round(us / floor_meas, 2),
                      "floor_us_nominal_hbm": round(floor_nom, 3), "floor_multiple_nominal": round(us / floor_nom, 2),
-                     "rounds": K, "kernel": kernel_name(b, torch.cuda.get_device_properties(dev).multi_processor_count)}
+                     "rounds": K, "kernel": kname}
         del xs, ts
         torch.cuda.empty_cache()
     out["clocks"] = clocks.stop()
@@ -498,7 +497,7 @@ def run_ours(args):
     ids = torch.empty((cols, k), dtype=torch.int32, device=dev)
     acc = torch.empty(max(lanes, 1), dtype=torch.int32, device=dev)
     com = torch.empty((max(lanes, 1), gamma + 1), dtype=torch.int32, device=dev)
-    sd.spec_set_kernel({"auto": sd.SPEC_KERNEL_AUTO, "warp": sd.SPEC_KERNEL_WARP, "cta": sd.SPEC_KERNEL_CTA}[args.kernel])
+    sd.spec_set_kernel(KERNEL_CHOICES[args.kernel])
     sd.spec_reserve(cols, k, lanes, gamma)
     stream = torch.cuda.Stream(device=dev)
 
@@ -528,6 +527,13 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             one(i)
+        if args.part == "split":
+            sd.spec_topk(xs[0], cols, V, k, vals, ids)
+            kname = kernel_name(sd)
+            sd.spec_verify_v(ts[0], drafts, lanes, gamma, V, acc, com)
+            kname += " + " + kernel_name(sd)
+        else:
+            kname = kernel_name(sd)
     stream.synchronize()
 
     K = args.steps
@@ -633,9 +639,6 @@ def run_ours(args):
     # the roofline of one launch; for the split round, of one step (two launches)
     unit_us = per_launch_us * per_step
     achieved = bytes_step / (unit_us * 1e-6) / 1e9
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    kname = kernel_name(bytes_step, sms, args.kernel) if args.part != "split" else \
-        f"{kernel_name(r.draft.nbytes, sms, args.kernel)} + {kernel_name(r.target.nbytes, sms, args.kernel)}"
     line = {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_max / K, 6), "us_per_round": round(us_round, 3),

@@ -275,24 +275,41 @@ spec_status spec_shortlist_topk(const uint16_t *hidden, int64_t cols, int64_t d,
                                 const void *spack, int64_t rows, const int32_t *id_map, int32_t k,
                                 uint16_t *logits, uint16_t *out_vals, int32_t *out_ids);
 
-/* Which streaming kernel runs a round.  Both compute the same results (every
+/* Which streaming kernel runs a round.  All compute the same results (every
  * output is the unique exact answer); they differ only in speed:
+ *   SPEC_KERNEL_GROUPMAX -- two phases in one launch.  The CTAs of a full-GPU
+ *                       grid stream their slices keeping only the maximum of
+ *                       each thread's group of 8-64 elements (2 bytes of
+ *                       scratch per group); the last CTA done with a column
+ *                       takes the k-th largest of its threads' maxima as a
+ *                       bound, re-reads the few groups that reach it and
+ *                       ranks their elements.  Needs V >= 4096 and scratch
+ *                       of about 2 bytes per 8-64 logits (the CTA kernel runs
+ *                       instead when either is missing, e.g. inside a graph
+ *                       capture that the scratch does not yet cover -- one
+ *                       call of the same sizes before capturing makes room).
+ *                       Fastest while each SM streams a few columns at most.
  *   SPEC_KERNEL_CTA  -- the CTAs of a full-GPU grid each stream a contiguous
  *                       slice in 60 KiB chunks; per column one threshold per
  *                       CTA (the k-th best the CTA has seen), kept by a
- *                       merging warp.  Fastest while each SM streams a few
- *                       columns at most (rounds of up to ~950 MB of logits).
+ *                       merging warp.
  *   SPEC_KERNEL_WARP -- every warp streams its own slice with its own ring,
  *                       buffer and threshold; no coordination inside the
  *                       stream.  Fastest for large rounds.
- *   SPEC_KERNEL_AUTO -- (default) CTA while the round's logits are at most
- *                       6 MiB per SM, WARP above.
+ *   SPEC_KERNEL_AUTO -- (default) GROUPMAX (else CTA) while the round's
+ *                       logits are at most 6 MiB per SM, WARP above.
  * The choice is process-wide; SPEC_ERR_ARG for any other value. */
 #define SPEC_KERNEL_AUTO 0
 #define SPEC_KERNEL_WARP 1
 #define SPEC_KERNEL_CTA 2
+#define SPEC_KERNEL_GROUPMAX 3
 spec_status spec_set_kernel(int32_t which);
 int32_t spec_get_kernel(void);
+
+/* The streaming kernel (SPEC_KERNEL_WARP, _CTA or _GROUPMAX) of the round
+ * the calling thread launched last (spec_round and the entry points built on
+ * it); SPEC_KERNEL_AUTO before the first.  Host-side bookkeeping only. */
+int32_t spec_last_kernel(void);
 
 /* Set the stream (a cudaStream_t, may be NULL for the legacy default stream)
  * that the calling thread's subsequent calls enqueue on.  Thread-local. */

@@ -26,7 +26,8 @@ __all__ = [
     "SPEC_MAX_GAMMA", "SpecError", "LIB_PATH", "lib",
     "spec_topk", "spec_topk_mapped", "spec_verify", "spec_verify_v", "spec_round", "spec_round_host",
     "spec_round_noalloc", "spec_round_counted", "spec_verify_sampled", "spec_round_sampled", "new_counters", "read_counters", "COUNTER_WORDS",
-    "spec_set_kernel", "spec_get_kernel", "SPEC_KERNEL_AUTO", "SPEC_KERNEL_WARP", "SPEC_KERNEL_CTA",
+    "spec_set_kernel", "spec_get_kernel", "spec_last_kernel", "SPEC_KERNEL_AUTO", "SPEC_KERNEL_WARP", "SPEC_KERNEL_CTA",
+    "SPEC_KERNEL_GROUPMAX",
     "spec_set_stream", "spec_get_stream", "spec_reserve", "spec_release", "spec_last_error",
     "spec_launch_count", "spec_device_status", "topk", "topk_mapped", "verify", "round_step", "EXPORTS",
     "spec_shortlist_pack", "spec_shortlist_logits", "spec_shortlist_topk",
@@ -34,7 +35,7 @@ __all__ = [
 
 SPEC_OK, SPEC_ERR_ARG, SPEC_ERR_ALLOC, SPEC_ERR_CUDA = 0, -1, -2, -3
 SPEC_VOCAB, SPEC_MAX_K, SPEC_MAX_GAMMA = 248_046, 64, 15
-SPEC_KERNEL_AUTO, SPEC_KERNEL_WARP, SPEC_KERNEL_CTA = 0, 1, 2
+SPEC_KERNEL_AUTO, SPEC_KERNEL_WARP, SPEC_KERNEL_CTA, SPEC_KERNEL_GROUPMAX = 0, 1, 2, 3
 LIB_PATH = _build.LIB
 
 if not os.path.exists(LIB_PATH):
@@ -58,6 +59,7 @@ _SIGS = {
                            _p, _p, _p],
     "spec_set_kernel": [_i32],
     "spec_get_kernel": [],
+    "spec_last_kernel": [],
     "spec_set_stream": [_p],
     "spec_get_stream": [],
     "spec_reserve": [_i64, _i32, _i64, _i32],
@@ -309,12 +311,17 @@ def spec_shortlist_topk(hidden, cols, d, wpack, spack, rows, id_map, k, logits, 
 
 
 def spec_set_kernel(which: int):
-    """Choose the streaming kernel: SPEC_KERNEL_AUTO (default), _WARP or _CTA."""
+    """Choose the streaming kernel: SPEC_KERNEL_AUTO (default), _WARP, _CTA or _GROUPMAX."""
     _check(lib.spec_set_kernel(which))
 
 
 def spec_get_kernel() -> int:
     return int(lib.spec_get_kernel())
+
+
+def spec_last_kernel() -> int:
+    """The kernel (SPEC_KERNEL_WARP, _CTA or _GROUPMAX) of this thread's last round launch."""
+    return int(lib.spec_last_kernel())
 
 
 def spec_set_stream(stream):

@@ -45,6 +45,7 @@ struct RoundArgs {
     unsigned int *lane_ticket;      // [lanes]: the lane's finished columns (per-warp kernel); with, from
                                     // bit 8 on, a bit per matching draft (CTA kernel)
     int32_t pstride;
+    uint16_t *gkeys;                // group-maxima kernel: group keys of both runs (in the partials area)
     spec_counters *counters;        // null: no counting
     // sampled verify (uniforms non-null): the target columns keep their
     // top t_k (else t_k = 1, the argmax)

@@ -1,0 +1,601 @@
+// The group-maxima kernel: small rounds over vocabulary-sized columns, in one
+// launch and two phases.
+//
+// Phase 1 streams.  The CTAs of a full-GPU grid each own a contiguous run of
+// batches of the flat run of logits.  A batch is 512 * U 16-byte vectors;
+// thread t of a CTA loads vectors t, t + 512, ..., t + 512 (U - 1) of it, one
+// group of 8U elements, and keeps nothing but the group's maximum (one per
+// column where the batch crosses a column boundary), written to global
+// memory as a 2-byte order key.  The loads go out eight per thread at a time,
+// then a bf16x2 max tree; there is no other work in the stream.
+//
+// Phase 2 selects, column by column, as soon as a column is complete: inside
+// the stream for a column that lies in one CTA's slice, at the end of the
+// slice for a column that CTAs share (a ticket per column: a CTA whose part
+// of it ends inside its slice takes the ticket right there, the CTA whose
+// part ends its slice comes last and finishes the column; a CTA that finds
+// every other part in needs no atomic at all).  The finishing CTA loads the
+// column's group keys, all at once, into shared memory.  Eight consecutive
+// threads form a section; T, the kk-th largest of the 64 section maxima, is
+// the key of kk distinct groups, so kk elements reach T and every one of the
+// column's kk best elements lies in a group whose key reaches T: every group
+// above T, and of the groups at T (ties) -- with token ids, which grow batch
+// by batch -- those of the first batches that hold kk of them.  The CTA
+// re-reads these groups from L2 with one 16-byte load per thread, collects
+// their elements >= T and ranks them (value desc, id asc): ranks below kk
+// are the column's top-kk in order.  Many candidates go through sorted lists
+// per warp instead, merged at the end; more than the buffers hold, and the
+// CTA scans the whole column exactly.  A target column then goes to greedy
+// (or sampled) verify.  Every step of phase 2 issues its global loads
+// together: a few round trips to L2 in all.
+//
+// The operations are those of the other two kernels ("A drafter inside the
+// artifact", Ignis DFlash2 page, section "How it works"): top-k per draft
+// column, largest first, ties to the smaller id; greedy verify.
+#pragma once
+
+#include "common.cuh"
+#include "round_cta.cuh"
+
+namespace gm {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kLoads = 8;             // 16-byte loads in flight per thread per step
+constexpr int kCap = 4096;            // phase 2 candidate elements
+constexpr int kGroupCap = 4096;       // phase 2 candidate groups
+constexpr int kKeyRows = 64;          // batches of a column whose keys phase 2 keeps in shared memory
+constexpr int kRankMax = 512;         // candidates ranked directly (more: sorted lists per warp)
+constexpr int64_t kMinV = 8 * 512;    // elements per column at least: a batch touches two columns at most
+
+struct Smem {
+    unsigned long long cand[kCap];
+    unsigned long long wl[kWarps][SPEC_MAX_K];   // sorted lists, one per warp; wl[0] ends as the column's list
+    uint32_t grp[kGroupCap];                     // candidate groups: (batch - first batch) << 9 | thread
+    uint16_t keys[kKeyRows][512];                // the column's group keys, [batch - first batch][thread]
+    uint32_t sec[64];                            // section maxima
+    uint32_t tiecnt[kKeyRows];                   // groups at the bound, per batch
+    int32_t wn[kWarps];
+    uint32_t ncand, ngrp;
+    uint32_t last[2];                            // the CTA completes its first / last column
+};
+
+constexpr size_t kSmemBytes = sizeof(Smem);
+static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM must fit");
+
+// One run (the draft or the target logits) on the 16-byte vector grid, as in
+// the other kernels: vector j holds elements [8j - mis, 8j - mis + 8) of the
+// flat run of N = cols * V elements; [jlo, jhi) lie wholly inside the buffer.
+// Batches of 512 * U vectors, NB of them; CTA b owns batches
+// [floor(b NB / W), floor((b + 1) NB / W)).
+struct GmRun {
+    const uint16_t *buf;
+    const uint4 *vb;
+    int64_t V, N, NV, jlo, jhi, NB;
+    uint16_t *G;             // [NB][512]: group keys of each batch's first column
+    uint16_t *H;             // [cols][512]: group keys of a column starting inside a batch, in that batch
+    unsigned int *ticket;    // [cols]
+    const int32_t *id_map;   // draft run only: local id -> vocabulary id (null: token ids)
+    int W, kk, mis;
+    bool draft;
+};
+
+__device__ __forceinline__ int64_t run_vectors(const uint16_t *buf, int64_t n)
+{
+    const int64_t mis = (int64_t)((reinterpret_cast<uintptr_t>(buf) >> 1) & 7);
+    return n > 0 ? (n + mis + 7) >> 3 : 0;
+}
+
+template <int U>
+__device__ __forceinline__ GmRun make_run(const RoundArgs &a, bool draft)
+{
+    constexpr int64_t B = 512 * U;
+    const int64_t nbd = (run_vectors(a.draft, a.d_cols * a.d_V) + B - 1) / B;
+    const int64_t nbt = (run_vectors(a.target, a.t_cols * a.t_V) + B - 1) / B;
+    GmRun r;
+    r.draft = draft;
+    r.buf = draft ? a.draft : a.target;
+    r.V = draft ? a.d_V : a.t_V;
+    const int64_t cols = draft ? a.d_cols : a.t_cols;
+    r.N = cols * r.V;
+    r.W = draft ? a.d_units : a.t_units;
+    r.kk = draft ? a.k : a.t_k;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(r.buf);
+    r.mis = (int)((a0 >> 1) & 7);
+    r.vb = reinterpret_cast<const uint4 *>(a0 - 2 * (uintptr_t)r.mis);
+    r.NV = (r.N + r.mis + 7) >> 3;
+    r.jlo = r.mis ? 1 : 0;
+    r.jhi = ((r.N + r.mis) & 7) ? r.NV - 1 : r.NV;
+    if (r.jhi < r.jlo) r.jhi = r.jlo;
+    r.NB = draft ? nbd : nbt;
+    uint16_t *hd = a.gkeys + (nbd + nbt) * 512;
+    r.G = draft ? a.gkeys : a.gkeys + nbd * 512;
+    r.H = draft ? hd : hd + a.d_cols * 512;
+    r.ticket = a.col_ticket + (draft ? 0 : a.d_cols);
+    r.id_map = draft ? a.id_map : nullptr;
+    return r;
+}
+
+// elements [elem_lo, elem_hi) of batch g; the batch holding element e
+template <int U>
+__device__ __forceinline__ int64_t elem_lo(const GmRun &r, int64_t g)
+{
+    const int64_t e = 8 * g * (512 * U) - r.mis;
+    return e > 0 ? e : 0;
+}
+template <int U>
+__device__ __forceinline__ int64_t elem_hi(const GmRun &r, int64_t g)
+{
+    const int64_t e = 8 * (g + 1) * (512 * U) - r.mis;
+    return e < r.N ? e : r.N;
+}
+template <int U>
+__device__ __forceinline__ int64_t batch_of(const GmRun &r, int64_t e) { return ((e + r.mis) >> 3) / (512 * U); }
+
+__device__ __forceinline__ int64_t slice_lo(const GmRun &r, int64_t b) { return b * r.NB / r.W; }
+__device__ __forceinline__ int64_t owner_of(const GmRun &r, int64_t g) { return ((g + 1) * r.W - 1) / r.NB; }
+
+__device__ __forceinline__ uint32_t key_of(uint32_t m2) { return order_key(hmax_splat(m2) & 0xFFFFu); }
+
+// Fold vector q (elements [g0, g0 + 8)) into the maxima of the column
+// before element cut (ma) and of the one from it on (mb).
+__device__ __forceinline__ void split_max(const uint4 &q, int64_t g0, int64_t cut, uint32_t &ma, uint32_t &mb)
+{
+    if (g0 + 8 <= cut) {
+        ma = bmax2(ma, vmax(q));
+    } else if (g0 >= cut) {
+        mb = bmax2(mb, vmax(q));
+    } else {
+        const int s = (int)(cut - g0);   // elements [0, s) before the cut
+        const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+        uint32_t wa[4], wb[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const bool lo_a = 2 * h < s, hi_a = 2 * h + 1 < s;
+            wa[h] = (lo_a ? (wd[h] & 0xFFFFu) : 0x7FFFu) | (hi_a ? (wd[h] & 0xFFFF0000u) : 0x7FFF0000u);
+            wb[h] = (lo_a ? 0x7FFFu : (wd[h] & 0xFFFFu)) | (hi_a ? 0x7FFF0000u : (wd[h] & 0xFFFF0000u));
+        }
+        ma = bmax2(ma, bmax2(bmax2(wa[0], wa[1]), bmax2(wa[2], wa[3])));
+        mb = bmax2(mb, bmax2(bmax2(wb[0], wb[1]), bmax2(wb[2], wb[3])));
+    }
+}
+
+// Phase 1, one step: the kLoads vectors of every thread in batches
+// [gb, gb + 8 / U) of the slice (which ends at batch g1b); each group's key
+// to G, and to H where a batch crosses into the next column.  cn is the
+// column after the one in progress and cut its first element.
+template <int U>
+__device__ __forceinline__ void stream_step(const GmRun &r, int64_t gb, int64_t g1b, int64_t &cn, int64_t &cut)
+{
+    constexpr int P = kLoads / U;
+    constexpr int64_t B = 512 * U;
+    const int t = threadIdx.x;
+    uint4 q[kLoads];
+#pragma unroll
+    for (int v = 0; v < kLoads; ++v) {
+        const int64_t j = (gb + v / U) * B + (v % U) * 512 + t;
+        q[v] = (gb + v / U < g1b && j >= r.jlo && j < r.jhi) ? __ldg(r.vb + j) : make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
+    }
+    if (gb * B < r.jlo || (gb + P) * B > r.jhi) {
+        // the buffer's edge vectors (at most one at each end), element by element
+#pragma unroll
+        for (int v = 0; v < kLoads; ++v) {
+            const int64_t j = (gb + v / U) * B + (v % U) * 512 + t;
+            if (gb + v / U < g1b && j < r.NV && (j < r.jlo || j >= r.jhi)) q[v] = load_edge(r.buf, j, r.mis, 0, r.N);
+        }
+    }
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+        const int64_t g = gb + p;
+        if (g >= g1b) break;
+        const int64_t e1 = elem_hi<U>(r, g);
+        uint32_t ma = kNaN2, mb = kNaN2;
+        if (e1 <= cut) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) ma = bmax2(ma, vmax(q[p * U + u]));
+        } else {
+#pragma unroll
+            for (int u = 0; u < U; ++u) split_max(q[p * U + u], 8 * (g * B + u * 512 + t) - r.mis, cut, ma, mb);
+            r.H[cn * 512 + t] = (uint16_t)key_of(mb);
+        }
+        r.G[g * 512 + t] = (uint16_t)key_of(ma);
+        if (e1 >= cut) {   // the next batch starts in column cn
+            ++cn;
+            cut += r.V;
+        }
+    }
+}
+
+// The largest T such that at least kk of the 64 values {v0, v1 of every
+// lane} reach T (the kk-th largest; 1 <= kk <= 64): a bisection between the
+// smallest and the largest value, in every lane of the warp (the values
+// cluster: a few steps).
+__device__ __forceinline__ uint32_t kth_of_64(uint32_t v0, uint32_t v1, int kk)
+{
+    uint32_t lo = __reduce_min_sync(kFull, v0 < v1 ? v0 : v1);   // all 64 reach it
+    uint32_t hi = __reduce_max_sync(kFull, v0 > v1 ? v0 : v1);
+    while (lo < hi) {
+        const uint32_t mid = (lo + hi + 1) >> 1;
+        const int n = __popc(__ballot_sync(kFull, v0 >= mid)) + __popc(__ballot_sync(kFull, v1 >= mid));
+        if (n >= kk) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Append group id gid of this lane (if take) to the group list, one shared
+// atomic per warp.
+__device__ __forceinline__ void append_group(Smem &s, bool take, uint32_t gid, int lane)
+{
+    const uint32_t bal = __ballot_sync(kFull, take);
+    if (!bal) return;
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(&s.ngrp, (uint32_t)__popc(bal));
+    base = __shfl_sync(kFull, base, 0);
+    const uint32_t pos = base + (uint32_t)__popc(bal & lanemask_lt());
+    if (take && pos < (uint32_t)kGroupCap) s.grp[pos] = gid;
+}
+
+// What phase 2's rare paths need of a run, passed by value (a GmRun passed
+// by reference would have to live in local memory).
+struct RunView {
+    const uint16_t *buf;
+    const uint4 *vb;
+    const int32_t *id_map;
+    int64_t jlo, jhi;
+    int mis, kk;
+};
+
+__device__ __forceinline__ RunView view_of(const GmRun &r)
+{
+    return RunView{r.buf, r.vb, r.id_map, r.jlo, r.jhi, r.mis, r.kk};
+}
+
+// Vector j restricted to column [cb, ce): elements outside it (or outside
+// the buffer) as NaN.
+__device__ __forceinline__ uint4 load_col_vec(const RunView &v, int64_t j, int64_t cb, int64_t ce)
+{
+    const int64_t g0 = 8 * j - v.mis;
+    if (j >= v.jlo && j < v.jhi && g0 >= cb && g0 + 8 <= ce) return __ldg(v.vb + j);
+    return load_edge(v.buf, j, v.mis, cb, ce);
+}
+
+__device__ __forceinline__ uint32_t half_of(const uint4 &q, int e)
+{
+    const uint32_t w = (e & 4) ? ((e & 2) ? q.w : q.z) : ((e & 2) ? q.y : q.x);
+    return (e & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+
+__device__ __forceinline__ unsigned long long make_entry(uint32_t key, uint32_t id, uint32_t raw)
+{
+    return ((unsigned long long)key << 48) | ((unsigned long long)(~id) << 16) | raw;
+}
+
+// Warp 0 merges the sixteen warps' sorted lists (s.wl[w][0 .. s.wn[w])) into
+// s.wl[0]: the kk best of all of them.  Every thread of the CTA must call it.
+__device__ __forceinline__ void merge_lists(Smem &s, int kk, int lane, int w)
+{
+    __syncthreads();
+    if (w != 0) return;
+    int n0 = s.wn[0];
+    for (int q = 1; q < kWarps; ++q) {
+        const int nq = s.wn[q];
+        for (int b2 = 0; b2 < nq; b2 += 32) {
+            unsigned long long e = b2 + lane < nq ? s.wl[q][b2 + lane] : 0ull;
+            if (n0 == kk && e < s.wl[0][kk - 1]) e = 0ull;
+            n0 = cta::list_merge32(s.wl[0], n0, e, kk, lane);
+        }
+    }
+}
+
+// The kk best of the n candidates in s.cand (many of them: ties at the
+// bound), into s.wl[0]: every warp folds a share into its own sorted list,
+// behind the list's kk-th entry, then the lists are merged.
+__device__ __noinline__ void select_many(int n, int kk, Smem &s, int lane, int w)
+{
+    unsigned long long *wl = s.wl[w];
+    int nw = 0;
+    for (int base = 32 * w; base < n; base += kThreads) {
+        unsigned long long e = base + lane < n ? s.cand[base + lane] : 0ull;
+        if (nw == kk && e < wl[kk - 1]) e = 0ull;
+        nw = cta::list_merge32(wl, nw, e, kk, lane);
+    }
+    if (lane == 0) s.wn[w] = nw;
+    merge_lists(s, kk, lane, w);
+}
+
+// Exact top-kk of column [cb, ce) among its elements >= T, for any input
+// (the path for massive ties): every warp scans a share of the column's
+// vectors into its own sorted list, keeping only entries above the list's
+// kk-th; the lists are then merged into s.wl[0].  Every thread of the CTA
+// must call it.
+__device__ __noinline__ void exact_scan(const RunView r, int64_t cb, int64_t ce, uint32_t T, Smem &s, int lane, int w)
+{
+    const int kk = r.kk;
+    unsigned long long *wl = s.wl[w];
+    int nw = 0;
+    unsigned long long thr = 0ull;   // a full list's kk-th entry: only better entries can enter
+    const int64_t jf = (cb + r.mis) >> 3, jl = (ce - 1 + r.mis) >> 3;
+    for (int64_t base = jf + 32 * w; base <= jl; base += kThreads) {
+        const int64_t j = base + lane;
+        const uint4 q = j <= jl ? load_col_vec(r, j, cb, ce) : make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
+        const int64_t g0 = 8 * j - r.mis;
+#pragma unroll 1
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t raw = half_of(q, e);
+            const uint32_t key = order_key(raw);
+            unsigned long long cand = 0ull;
+            if (key != 0 && key >= T && key >= entry_key(thr)) {
+                uint32_t id = (uint32_t)(g0 + e - cb);
+                if (r.id_map) id = (uint32_t)__ldg(r.id_map + id);
+                cand = make_entry(key, id, raw);
+                if (cand < thr) cand = 0ull;
+            }
+            if (__ballot_sync(kFull, cand != 0ull)) {
+                nw = cta::list_merge32(wl, nw, cand, kk, lane);
+                thr = nw == kk ? wl[kk - 1] : 0ull;
+            }
+        }
+    }
+    if (lane == 0) s.wn[w] = nw;
+    merge_lists(s, kk, lane, w);
+}
+
+// Phase 2 for column c of run r (every thread of the CTA calls it): the
+// column's top-kk (draft: to the outputs; target: to verify).  shared: the
+// column's ticket is to be cleared for the next launch.  Every key of the
+// column is written (this CTA's own keys: before the barrier at entry).
+template <int U>
+__device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r, int64_t c, bool shared, Smem &s)
+{
+    constexpr int64_t B = 512 * U;
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int kk = r.kk;
+    const int64_t cb = c * r.V, ce = cb + r.V;
+    const int64_t bf = batch_of<U>(r, cb), bl = batch_of<U>(r, ce - 1);
+    const bool hin = elem_lo<U>(r, bf) < cb;   // the column starts inside batch bf: its keys there are in H
+    const int nb = (int)(bl - bf + 1);
+    const uint16_t *k0 = hin ? r.H + c * 512 + t : r.G + bf * 512 + t;
+    const uint16_t *kr = r.G + bf * 512 + t;   // keys of batch bf + i at kr[512 i] for i >= 1
+    const RunView rv = view_of(r);
+    __syncthreads();
+    if (t < kKeyRows) s.tiecnt[t] = 0u;
+
+    // 1. the column's group keys: sixteen loads in flight per thread, kept in
+    //    shared memory (the first kKeyRows batches); this thread's maximum
+    uint32_t mt = 0;
+    for (int i0 = 0; i0 < nb; i0 += 16) {
+        uint32_t kv[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) kv[q] = i0 + q < nb ? __ldcg(i0 + q == 0 ? k0 : kr + 512 * (i0 + q)) : 0u;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            mt = kv[q] > mt ? kv[q] : mt;
+            if (i0 + q < kKeyRows) s.keys[i0 + q][t] = (uint16_t)kv[q];
+        }
+    }
+    // 2. the bound T: the kk-th largest section maximum (sections of 8 threads)
+    uint32_t m8 = mt;
+#pragma unroll
+    for (int d = 1; d < 8; d <<= 1) {
+        const uint32_t o = __shfl_xor_sync(kFull, m8, d);
+        m8 = o > m8 ? o : m8;
+    }
+    if ((lane & 7) == 0) s.sec[4 * w + (lane >> 3)] = m8;
+    __syncthreads();
+    const uint32_t T = kth_of_64(s.sec[lane], s.sec[lane + 32], kk);
+    // 3. the groups to re-read: every group above T, and of the groups at T
+    //    (ties) -- with token ids, which grow batch by batch -- only those of
+    //    the first batches that hold kk of them (they hold kk elements at T,
+    //    all with smaller ids than any tie further on)
+    const bool cut_ties = r.id_map == nullptr && nb <= kKeyRows;
+    const bool any = __ballot_sync(kFull, mt != 0 && mt >= T) != 0u;   // this warp has groups reaching T
+    if (any) {
+#pragma unroll 1
+        for (int i = 0; i < nb; ++i) {
+            const uint32_t key = i < kKeyRows ? s.keys[i][t] : __ldcg(i == 0 ? k0 : kr + 512 * i);
+            const bool tie = key != 0 && key == T;
+            append_group(s, (key != 0 && key > T) || (tie && !cut_ties), ((uint32_t)i << 9) | (uint32_t)t, lane);
+            if (cut_ties) {
+                const uint32_t nt = (uint32_t)__popc(__ballot_sync(kFull, tie));
+                if (lane == 0 && nt) atomicAdd(&s.tiecnt[i], nt);
+            }
+        }
+    }
+    if (cut_ties) {
+        __syncthreads();
+        int upto = nb - 1, acc = 0;
+        for (int i = 0; i < nb; ++i) {
+            acc += (int)s.tiecnt[i];
+            if (acc >= kk) {
+                upto = i;
+                break;
+            }
+        }
+        if (any)
+#pragma unroll 1
+            for (int i = 0; i <= upto; ++i) {
+                const uint32_t key = s.keys[i][t];
+                append_group(s, key != 0 && key == T, ((uint32_t)i << 9) | (uint32_t)t, lane);
+            }
+    }
+    __syncthreads();
+    const int ng = (int)s.ngrp;
+    // 4. their elements >= T: one 16-byte vector per thread per pass, up to
+    //    four passes' loads in flight
+    if (ng <= kGroupCap) {
+        const int nv = ng * U;
+        for (int p0 = 0; p0 < nv; p0 += 4 * kThreads) {
+            uint4 q[4];
+            int64_t jv[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const int p = p0 + h * kThreads + t;
+                jv[h] = -1;
+                q[h] = make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
+                if (p < nv) {
+                    const uint32_t gid = s.grp[p / U];
+                    const int64_t j = (bf + (gid >> 9)) * B + (p % U) * 512 + (gid & 511u);
+                    if (j < r.NV) {
+                        jv[h] = j;
+                        q[h] = load_col_vec(rv, j, cb, ce);
+                    }
+                }
+            }
+#pragma unroll 1
+            for (int h = 0; h < 4; ++h) {
+                if (p0 + h * kThreads + 32 * w >= nv) break;   // this warp has no vector in the pass
+                const uint4 qh = h == 0 ? q[0] : h == 1 ? q[1] : h == 2 ? q[2] : q[3];
+                const int64_t g0 = 8 * (h == 0 ? jv[0] : h == 1 ? jv[1] : h == 2 ? jv[2] : jv[3]) - r.mis;
+                uint32_t mask = 0;   // this lane's elements >= T
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t key = order_key(half_of(qh, e));
+                    mask |= (key != 0 && key >= T) ? 1u << e : 0u;
+                }
+                int total;
+                const int excl = warp_exclusive_sum(__popc(mask), lane, total);
+                if (total == 0) continue;
+                uint32_t pos = 0;
+                if (lane == 0) pos = atomicAdd(&s.ncand, (uint32_t)total);
+                pos = __shfl_sync(kFull, pos, 0) + (uint32_t)excl;
+                for (uint32_t m = mask; m; m &= m - 1, ++pos) {
+                    const int e = __ffs(m) - 1;
+                    const uint32_t raw = half_of(qh, e);
+                    uint32_t id = (uint32_t)(g0 + e - cb);
+                    if (r.id_map) id = (uint32_t)__ldg(r.id_map + id);
+                    if (pos < (uint32_t)kCap) s.cand[pos] = make_entry(order_key(raw), id, raw);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    // 5. the kk best, in order
+    const int n = (int)s.ncand;
+    if (ng > kGroupCap || n > kCap) {
+        exact_scan(rv, cb, ce, T, s, lane, w);
+    } else if (n > kRankMax) {
+        select_many(n, kk, s, lane, w);
+    } else {
+        for (int i = t; i < n; i += kThreads) {
+            const unsigned long long e = s.cand[i];
+            int rank = 0;
+            for (int j = 0; j < n; ++j) rank += s.cand[j] > e ? 1 : 0;
+            if (rank < kk) s.wl[0][rank] = e;
+        }
+    }
+    __syncthreads();
+    if (r.draft) {
+        for (int i = t; i < kk; i += kThreads) {
+            const unsigned long long e = s.wl[0][i];
+            a.out_vals[c * kk + i] = entry_raw(e);
+            a.out_ids[c * kk + i] = (int32_t)entry_id(e);
+        }
+    } else if (w == 0) {
+        if (a.uniforms) sampled_column_done(a, c, s.wl[0], kk, lane);
+        else verify_column_done(a, c, (int32_t)entry_id(s.wl[0][0]), lane);
+    }
+    if (t == 0) {
+        s.ncand = 0u;
+        s.ngrp = 0u;
+        if (shared) r.ticket[c] = 0u;   // ready for the next launch
+    }
+    __syncthreads();
+}
+
+// Column c's CTAs: those owning its first and last batch.
+template <int U>
+__device__ __forceinline__ void column_owners(const GmRun &r, int64_t c, int64_t &wf, int64_t &wl)
+{
+    wf = owner_of(r, batch_of<U>(r, c * r.V));
+    wl = owner_of(r, batch_of<U>(r, (c + 1) * r.V - 1));
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const unsigned int *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Thread 0, at the end of the slice, for a shared column whose part here is
+// written (others = the number of other CTAs that share it): true if this
+// CTA is to finish the column.  If every other part is in already, it is,
+// with no atomic (its own keys need no release: only it reads them);
+// otherwise it takes the ticket, and finishes if it comes last.
+__device__ __forceinline__ uint32_t arrive_at_end(unsigned int *ticket, uint32_t others)
+{
+    if (ld_acquire(ticket) == others) return 1u;
+    return atom_add_acq_rel(ticket, 1u) == others ? 1u : 0u;
+}
+
+template <int U>
+__global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_constant__ RoundArgs a)
+{
+    constexpr int P = kLoads / U;
+    pdl_launch_dependents();
+    pdl_wait();
+    extern __shared__ __align__(16) unsigned char smem[];
+    Smem &s = *reinterpret_cast<Smem *>(smem);
+    const int b = blockIdx.x;
+    if (b >= a.d_units + a.t_units) return;
+    const bool draft = b < a.d_units;
+    const GmRun r = make_run<U>(a, draft);
+    const int bi = draft ? b : b - a.d_units;
+    const int64_t g0b = slice_lo(r, bi), g1b = slice_lo(r, bi + 1);
+    if (g1b <= g0b) return;
+    if (threadIdx.x == 0) {
+        s.ncand = 0u;
+        s.ngrp = 0u;
+    }
+    int64_t cn = elem_lo<U>(r, g0b) / r.V + 1;   // the column after the one in progress
+    int64_t cut = cn * r.V;                      // its first element
+    const int64_t cl = (elem_hi<U>(r, g1b - 1) - 1) / r.V;
+    int64_t cdone = cn - 1;      // the first column not yet handled
+    int64_t pend = -1;           // a shared column whose ticket this CTA took inside the stream
+    uint32_t pend_old = 0;       // (thread 0) that ticket's count before it
+    int64_t gb = g0b;
+    for (;;) {
+        if (gb < g1b) {
+            stream_step<U>(r, gb, g1b, cn, cut);
+            gb += P;
+        }
+        const bool ending = gb >= g1b;
+        const int64_t upto = ending ? cl + 1 : cn - 1;   // columns below it are complete here
+        while (cdone < upto || (ending && pend >= 0)) {
+            int64_t c, wf, wl;
+            bool fin;
+            if (cdone < upto) {
+                c = cdone++;
+                column_owners<U>(r, c, wf, wl);
+                fin = wf == wl;   // the column lies in this slice: finish it now
+                if (!fin) {
+                    __syncthreads();   // this CTA's keys of the column are written
+                    if (!ending) {
+                        // its part here ends inside the slice (the slice's first
+                        // column): take the ticket now, read it at the end
+                        if (threadIdx.x == 0) pend_old = atom_add_acq_rel(r.ticket + c, 1u);
+                        pend = c;
+                    } else {
+                        if (threadIdx.x == 0) s.last[0] = arrive_at_end(r.ticket + c, (uint32_t)(wl - wf));
+                        __syncthreads();
+                        fin = s.last[0] != 0u;
+                    }
+                }
+            } else {
+                c = pend;
+                pend = -1;
+                column_owners<U>(r, c, wf, wl);
+                __syncthreads();
+                if (threadIdx.x == 0) s.last[0] = pend_old == (uint32_t)(wl - wf) ? 1u : 0u;
+                __syncthreads();
+                fin = s.last[0] != 0u;
+            }
+            if (fin) finish_column<U>(a, r, c, wf != wl, s);
+            __syncthreads();   // s.last is read by every thread before it is written again
+        }
+        if (ending) break;
+    }
+}
+
+}  // namespace gm

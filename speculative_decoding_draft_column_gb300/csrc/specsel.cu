@@ -30,6 +30,7 @@
 #include "common.cuh"
 #include "round_cta.cuh"
 #include "round_warp.cuh"
+#include "round_gm.cuh"
 #include "head_q4.cuh"
 
 namespace {
@@ -72,6 +73,7 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 std::atomic<int64_t> g_launches{0};
 thread_local cudaStream_t t_stream = nullptr;
+thread_local int32_t t_last_kernel = SPEC_KERNEL_AUTO;
 thread_local std::string t_err;
 
 spec_status fail(spec_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
@@ -123,6 +125,12 @@ spec_status device_state(DeviceState **out)
                                                           cta::kSmemBytes);
         if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
         if (d.occ_c < 1) d.occ_c = 1;
+        void *kg[4] = {reinterpret_cast<void *>(gm::spec_round_kernel<1>), reinterpret_cast<void *>(gm::spec_round_kernel<2>),
+                       reinterpret_cast<void *>(gm::spec_round_kernel<4>), reinterpret_cast<void *>(gm::spec_round_kernel<8>)};
+        for (void *k : kg) {
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gm::kSmemBytes);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+        }
         d.init = true;
     }
     *out = &d;
@@ -240,21 +248,80 @@ void split_units(int64_t nv_d, int64_t nv_t, int64_t max_units, int64_t min_slic
 // a.t_units; a.pstride is set too).
 struct Plan {
     bool per_cta;
+    bool gm;          // the group-maxima kernel
+    int gm_u;         // its batch width: 16-byte vectors per thread per batch (1, 2, 4 or 8)
     int slots;        // per-warp kernel: 2 for k > 32 (finer seed groups)
     bool mapped;
     int64_t grid;     // CTAs
+    int64_t partials; // entries (u64) of the partials area the launch uses
 };
 
-Plan plan_round(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, bool mapped, int64_t max_partials)
+// The group-maxima kernel's plan: the batch width U and the CTAs of each run.
+// Every batch must touch two columns at most (V >= 8 * 512 * U).  Of the
+// widths that allow it, the widest unless a narrower one cuts the vectors
+// of the most loaded CTA by a third: a narrower batch balances small rounds
+// better but gives a column's finishing CTA more group keys to read.  False
+// if no width fits, or the group keys would not fit in max_partials entries.
+bool plan_gm(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, int64_t max_partials, Plan &p)
+{
+    int64_t vmin = INT64_MAX;
+    if (nv_d > 0) vmin = a.d_V < vmin ? a.d_V : vmin;
+    if (nv_t > 0) vmin = a.t_V < vmin ? a.t_V : vmin;
+    if (vmin < gm::kMinV) return false;
+    int32_t wd = 0, wt = 0;
+    split_units(nv_d, nv_t, d.sms, 512, 1, INT64_MAX / 4, &wd, &wt);
+    auto nbatches = [](int64_t nv, int64_t B) { return (nv + B - 1) / B; };
+    auto most = [&](int64_t nv, int64_t w, int64_t B) -> int64_t {
+        if (nv == 0) return 0;
+        const int64_t nb = nbatches(nv, B), ww = w < nb ? w : nb;
+        return (nb + ww - 1) / ww * B;
+    };
+    int best = 0;
+    int64_t best_cost = 0;
+    for (int u : {8, 4, 2, 1}) {
+        const int64_t B = 512 * (int64_t)u;
+        if (8 * B > vmin) continue;
+        const int64_t cd = most(nv_d, wd, B), ct = most(nv_t, wt, B);
+        const int64_t c = cd > ct ? cd : ct;
+        if (best == 0 || c * 3 < best_cost * 2) {
+            best = u;
+            best_cost = c;
+        }
+    }
+    if (best == 0) return false;
+    const int64_t B = 512 * (int64_t)best;
+    const int64_t nbd = nbatches(nv_d, B), nbt = nbatches(nv_t, B);
+    const int64_t bytes = (nbd + nbt + a.d_cols + a.t_cols) * 512 * 2;
+    const int64_t entries = (bytes + 7) / 8;
+    if (entries > max_partials) return false;
+    a.d_units = (int32_t)(nv_d > 0 ? (wd < nbd ? wd : nbd) : 0);
+    a.t_units = (int32_t)(nv_t > 0 ? (wt < nbt ? wt : nbt) : 0);
+    p.gm = true;
+    p.gm_u = best;
+    p.grid = (int64_t)a.d_units + a.t_units;
+    p.partials = entries;
+    return true;
+}
+
+// gm_max: the most partials entries the group-maxima kernel may use (the
+// area's present size while a graph is being captured); without room, or
+// with columns too short for it, the CTA kernel runs instead.
+Plan plan_round(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, bool mapped, int64_t max_partials,
+                int64_t gm_max = INT64_MAX)
 {
     Plan p;
     const int choice = g_kernel_choice.load(std::memory_order_relaxed);
-    p.per_cta = choice == SPEC_KERNEL_CTA ||
-                (choice == SPEC_KERNEL_AUTO && (nv_d + nv_t) * 16 <= kCtaMaxBytesPerSm * (int64_t)d.sms);
+    const bool small = (nv_d + nv_t) * 16 <= kCtaMaxBytesPerSm * (int64_t)d.sms;
+    p.gm = false;
+    p.gm_u = 0;
     p.mapped = mapped;
     const int kmax = a.k > a.t_k ? a.k : a.t_k;   // the larger list of the two runs
     p.slots = kmax > 32 ? 2 : 1;
     a.pstride = kmax + 2;
+    if ((choice == SPEC_KERNEL_GROUPMAX || (choice == SPEC_KERNEL_AUTO && small)) &&
+        plan_gm(d, a, nv_d, nv_t, max_partials < gm_max ? max_partials : gm_max, p))
+        return p;
+    p.per_cta = choice == SPEC_KERNEL_CTA || choice == SPEC_KERNEL_GROUPMAX || (choice == SPEC_KERNEL_AUTO && small);
     if (p.per_cta) {
         split_units(nv_d, nv_t, (int64_t)d.sms * d.occ_c, cta::kMinSliceVec, a.pstride, max_partials, &a.d_units,
                     &a.t_units);
@@ -264,11 +331,9 @@ Plan plan_round(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, 
         split_units(nv_d, nv_t, max_warps, wrp::kMinSliceVec, a.pstride, max_partials, &a.d_units, &a.t_units);
         p.grid = ((int64_t)a.d_units + a.t_units + wrp::kWarpsPerCta - 1) / wrp::kWarpsPerCta;
     }
+    p.partials = ((int64_t)a.d_units + a.t_units) * 2 * a.pstride;   // two lists per unit
     return p;
 }
-
-// Partial-list entries a plan needs (two lists per unit).
-int64_t plan_partials(const RoundArgs &a) { return ((int64_t)a.d_units + a.t_units) * 2 * a.pstride; }
 
 // Launch, with programmatic stream serialization when pdl: the kernel
 // signals its dependents at entry and waits for its predecessor before any
@@ -299,6 +364,14 @@ cudaError_t launch_pdl(K kernel, unsigned grid, unsigned block, size_t smem, cud
 cudaError_t launch_plan(const Plan &p, const RoundArgs &a, cudaStream_t stream, bool pdl = true)
 {
     const unsigned g = (unsigned)p.grid;
+    if (p.gm) {
+        switch (p.gm_u) {
+        case 8: return launch_pdl(gm::spec_round_kernel<8>, g, gm::kThreads, gm::kSmemBytes, stream, a, pdl);
+        case 4: return launch_pdl(gm::spec_round_kernel<4>, g, gm::kThreads, gm::kSmemBytes, stream, a, pdl);
+        case 2: return launch_pdl(gm::spec_round_kernel<2>, g, gm::kThreads, gm::kSmemBytes, stream, a, pdl);
+        default: return launch_pdl(gm::spec_round_kernel<1>, g, gm::kThreads, gm::kSmemBytes, stream, a, pdl);
+        }
+    }
     if (p.per_cta) return launch_pdl(cta::spec_round_kernel, g, cta::kThreads, cta::kSmemBytes, stream, a, pdl);
     const unsigned b = wrp::kThreads;
     const size_t m = wrp::kSmemBytes;
@@ -307,6 +380,8 @@ cudaError_t launch_plan(const Plan &p, const RoundArgs &a, cudaStream_t stream, 
     if (!p.mapped) return launch_pdl(wrp::spec_round_kernel<2, false>, g, b, m, stream, a, false);
     return launch_pdl(wrp::spec_round_kernel<2, true>, g, b, m, stream, a, false);
 }
+
+int32_t plan_kernel(const Plan &p) { return p.gm ? SPEC_KERNEL_GROUPMAX : p.per_cta ? SPEC_KERNEL_CTA : SPEC_KERNEL_WARP; }
 
 bool misaligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
 
@@ -372,20 +447,23 @@ spec_status launch_round_locked(const uint16_t *draft, int64_t cols, int64_t V, 
     a.temperature = smp.temperature;
     a.top_p = smp.top_p;
     a.uniforms = lanes ? smp.uniforms : nullptr;
-    const Plan plan = plan_round(*d, a, cols ? vectors_of(draft, cols * V) : 0,
-                                 lanes ? vectors_of(target, t_cols * tV) : 0, mapped, INT64_MAX / 4);
     cudaStream_t stream = t_stream;
-    const ScratchCaps need = {2 * (cols + t_cols), lanes, plan_partials(a)};
+    const Plan plan = plan_round(*d, a, cols ? vectors_of(draft, cols * V) : 0,
+                                 lanes ? vectors_of(target, t_cols * tV) : 0, mapped, INT64_MAX / 4,
+                                 stream_capturing(stream) ? d->cap_part : INT64_MAX);
+    const ScratchCaps need = {2 * (cols + t_cols), lanes, plan.partials};
     st = ensure_scratch(*d, need, stream);
     if (st != SPEC_OK) return st;
     const ScratchPtrs sp = scratch_ptrs(*d);
     a.partials = sp.partials;
+    a.gkeys = reinterpret_cast<uint16_t *>(sp.partials);
     a.col_ticket = sp.col_ticket;
     a.col_cert = sp.col_ticket + (cols + t_cols);
     a.lane_ticket = sp.lane_ticket;
     const cudaError_t e = launch_plan(plan, a, stream);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
+    t_last_kernel = plan_kernel(plan);
     return SPEC_OK;
 }
 
@@ -726,13 +804,16 @@ extern "C" {
 spec_status spec_set_kernel(int32_t which)
 {
     t_err.clear();
-    if (which != SPEC_KERNEL_AUTO && which != SPEC_KERNEL_WARP && which != SPEC_KERNEL_CTA)
+    if (which != SPEC_KERNEL_AUTO && which != SPEC_KERNEL_WARP && which != SPEC_KERNEL_CTA &&
+        which != SPEC_KERNEL_GROUPMAX)
         return fail(SPEC_ERR_ARG, "spec_set_kernel: unknown kernel %d", which);
     g_kernel_choice.store(which, std::memory_order_relaxed);
     return SPEC_OK;
 }
 
 int32_t spec_get_kernel(void) { return g_kernel_choice.load(std::memory_order_relaxed); }
+
+int32_t spec_last_kernel(void) { return t_last_kernel; }
 
 spec_status spec_set_stream(void *stream)
 {
@@ -905,6 +986,7 @@ extern "C" spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t 
     a.col_cert = a.col_ticket + (cols + t_cols);
     a.lane_ticket = reinterpret_cast<unsigned int *>(p + kNoAllocLaneTicket);
     a.partials = reinterpret_cast<unsigned long long *>(p + kNoAllocPart);
+    a.gkeys = reinterpret_cast<uint16_t *>(a.partials);
 
     cudaStream_t stream = t_stream;
     // the array keeps whatever the last call left: start every ticket at zero
@@ -913,5 +995,6 @@ extern "C" spec_status spec_round_noalloc(const uint16_t *draft_logits, int64_t 
     e = launch_plan(plan, a, stream, false);   // right after the ticket clear
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
+    t_last_kernel = plan_kernel(plan);
     return SPEC_OK;
 }

@@ -83,10 +83,10 @@ def test_stream_is_thread_local(sd):
 
 def test_kernel_choice(sd):
     assert sd.spec_get_kernel() == sd.SPEC_KERNEL_AUTO
-    for which in (sd.SPEC_KERNEL_WARP, sd.SPEC_KERNEL_CTA, sd.SPEC_KERNEL_AUTO):
+    for which in (sd.SPEC_KERNEL_WARP, sd.SPEC_KERNEL_CTA, sd.SPEC_KERNEL_GROUPMAX, sd.SPEC_KERNEL_AUTO):
         assert sd.lib.spec_set_kernel(which) == sd.SPEC_OK
         assert sd.spec_get_kernel() == which
-    for bad in (-1, 3, 99):
+    for bad in (-1, 4, 99):
         assert sd.lib.spec_set_kernel(bad) == sd.SPEC_ERR_ARG
         assert "unknown kernel" in sd.spec_last_error()
     assert sd.spec_get_kernel() == sd.SPEC_KERNEL_AUTO

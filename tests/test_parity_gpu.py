@@ -25,10 +25,11 @@ def _lib():
     return sd
 
 
-@pytest.fixture(autouse=True, params=[1, 2], ids=["warp", "cta"])
+@pytest.fixture(autouse=True, params=[1, 2, 3], ids=["warp", "cta", "gm"])
 def kernel(request, _lib):
-    """Every parity case runs on both streaming kernels (forced), whatever the
-    automatic choice would be for its size."""
+    """Every parity case runs on each streaming kernel (forced), whatever the
+    automatic choice would be for its size (the group-maxima kernel hands
+    columns shorter than 4096 to the CTA kernel)."""
     _lib.spec_set_kernel(request.param)
     yield request.param
     _lib.spec_set_kernel(_lib.SPEC_KERNEL_AUTO)
