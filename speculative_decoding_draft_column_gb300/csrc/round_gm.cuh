@@ -46,6 +46,7 @@ constexpr int kCap = 4096;            // phase 2 candidate elements
 constexpr int kGroupCap = 4096;       // phase 2 candidate groups
 constexpr int kKeyRows = 64;          // batches of a column whose keys phase 2 keeps in shared memory
 constexpr int kRankMax = 512;         // candidates ranked directly (more: sorted lists per warp)
+constexpr int kFewTies = 64;          // groups at the bound all re-read up to this many
 constexpr int64_t kMinV = 8 * 512;    // elements per column at least: a batch touches two columns at most
 
 struct Smem {
@@ -55,6 +56,7 @@ struct Smem {
     uint16_t keys[kKeyRows][512];                // the column's group keys, [batch - first batch][thread]
     uint32_t sec[64];                            // section maxima
     uint32_t tiecnt[kKeyRows];                   // groups at the bound, per batch
+    uint32_t wtie[kWarps];                       // groups at the bound, per warp
     int32_t wn[kWarps];
     uint32_t ncand, ngrp;
     uint32_t last[2];                            // the CTA completes its first / last column
@@ -62,6 +64,7 @@ struct Smem {
 
 constexpr size_t kSmemBytes = sizeof(Smem);
 static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM must fit");
+static_assert(kKeyRows <= 64, "phase 2 marks a thread's batches in a 64-bit mask");
 
 // One run (the draft or the target logits) on the 16-byte vector grid, as in
 // the other kernels: vector j holds elements [8j - mis, 8j - mis + 8) of the
@@ -221,6 +224,20 @@ __device__ __forceinline__ uint32_t kth_of_64(uint32_t v0, uint32_t v1, int kk)
         else hi = mid - 1;
     }
     return lo;
+}
+
+// Append the groups of this thread's rows in mask (bit i: batch i of the
+// column) to the group list, one shared atomic per warp.
+__device__ __forceinline__ void append_groups(Smem &s, unsigned long long mask, int lane)
+{
+    int total;
+    const int excl = warp_exclusive_sum(__popcll(mask), lane, total);
+    if (total == 0) return;
+    uint32_t pos = 0;
+    if (lane == 0) pos = atomicAdd(&s.ngrp, (uint32_t)total);
+    pos = __shfl_sync(kFull, pos, 0) + (uint32_t)excl;
+    for (unsigned long long m = mask; m; m &= m - 1, ++pos)
+        if (pos < (uint32_t)kGroupCap) s.grp[pos] = ((uint32_t)(__ffsll((long long)m) - 1) << 9) | (threadIdx.x & 511u);
 }
 
 // Append group id gid of this lane (if take) to the group list, one shared
@@ -385,41 +402,59 @@ __device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r
     __syncthreads();
     const uint32_t T = kth_of_64(s.sec[lane], s.sec[lane + 32], kk);
     // 3. the groups to re-read: every group above T, and of the groups at T
-    //    (ties) -- with token ids, which grow batch by batch -- only those of
-    //    the first batches that hold kk of them (they hold kk elements at T,
-    //    all with smaller ids than any tie further on)
-    const bool cut_ties = r.id_map == nullptr && nb <= kKeyRows;
-    const bool any = __ballot_sync(kFull, mt != 0 && mt >= T) != 0u;   // this warp has groups reaching T
-    if (any) {
+    //    (ties) -- with token ids, which grow batch by batch, and more than a
+    //    few of them -- only those of the first batches that hold kk of them
+    //    (they hold kk elements at T, all with smaller ids than any tie
+    //    further on).  Each thread marks its rows above / at T in two masks;
+    //    one shared atomic per warp appends a mask's groups.
+    if (nb > kKeyRows) {
+        // a column of more than kKeyRows batches: every group reaching T
+        if (__ballot_sync(kFull, mt != 0 && mt >= T) != 0u)
 #pragma unroll 1
-        for (int i = 0; i < nb; ++i) {
-            const uint32_t key = i < kKeyRows ? s.keys[i][t] : __ldcg(i == 0 ? k0 : kr + 512 * i);
-            const bool tie = key != 0 && key == T;
-            append_group(s, (key != 0 && key > T) || (tie && !cut_ties), ((uint32_t)i << 9) | (uint32_t)t, lane);
-            if (cut_ties) {
-                const uint32_t nt = (uint32_t)__popc(__ballot_sync(kFull, tie));
-                if (lane == 0 && nt) atomicAdd(&s.tiecnt[i], nt);
+            for (int i = 0; i < nb; ++i) {
+                const uint32_t key = i < kKeyRows ? s.keys[i][t] : __ldcg(i == 0 ? k0 : kr + 512 * i);
+                append_group(s, key != 0 && key >= T, ((uint32_t)i << 9) | (uint32_t)t, lane);
             }
-        }
-    }
-    if (cut_ties) {
         __syncthreads();
-        int upto = nb - 1, acc = 0;
-        for (int i = 0; i < nb; ++i) {
-            acc += (int)s.tiecnt[i];
-            if (acc >= kk) {
-                upto = i;
-                break;
-            }
-        }
-        if (any)
+    } else {
+        unsigned long long above = 0ull, tie = 0ull;
+        if (mt != 0 && mt >= T)
 #pragma unroll 1
-            for (int i = 0; i <= upto; ++i) {
+            for (int i = 0; i < nb; ++i) {
                 const uint32_t key = s.keys[i][t];
-                append_group(s, key != 0 && key == T, ((uint32_t)i << 9) | (uint32_t)t, lane);
+                above |= (unsigned long long)(key != 0 && key > T) << i;
+                tie |= (unsigned long long)(key != 0 && key == T) << i;
             }
+        append_groups(s, above, lane);
+        const uint32_t wt = __reduce_add_sync(kFull, (uint32_t)__popcll(tie));
+        if (lane == 0) s.wtie[w] = wt;
+        __syncthreads();
+        uint32_t nt = 0;
+#pragma unroll
+        for (int q = 0; q < kWarps; ++q) nt += s.wtie[q];
+        if (r.id_map != nullptr || nt <= (uint32_t)kFewTies) {
+            append_groups(s, tie, lane);
+        } else {
+            // many ties: groups at T per batch, then those of the first
+            // batches holding kk of them
+#pragma unroll 1
+            for (int i = 0; i < nb; ++i) {
+                const uint32_t ni = (uint32_t)__popc(__ballot_sync(kFull, (tie >> i) & 1ull));
+                if (lane == 0 && ni) atomicAdd(&s.tiecnt[i], ni);
+            }
+            __syncthreads();
+            int upto = nb - 1, acc = 0;
+            for (int i = 0; i < nb; ++i) {
+                acc += (int)s.tiecnt[i];
+                if (acc >= kk) {
+                    upto = i;
+                    break;
+                }
+            }
+            append_groups(s, upto >= 63 ? tie : tie & ((2ull << upto) - 1ull), lane);
+        }
+        __syncthreads();
     }
-    __syncthreads();
     const int ng = (int)s.ngrp;
     // 4. their elements >= T: one 16-byte vector per thread per pass, up to
     //    four passes' loads in flight
