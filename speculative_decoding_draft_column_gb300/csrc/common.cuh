@@ -464,11 +464,11 @@ __device__ __noinline__ void verify_column_done(const RoundArgs &a, int64_t c, i
 // (u = uniforms[ln][j][0]); otherwise -- and always at position gamma, the
 // bonus -- the token drawn is the first nucleus token (draft skipped) whose
 // running q exceeds uniforms[ln][j][1] times the total q without the draft.
-// The position's token (the draft, or the draw) goes to its commit id and
-// its acceptance bit to the lane's ticket word, as in verify_column_done.
-// Every lane computes the same sums (broadcast terms, same order).
-__device__ __noinline__ void sampled_column_done(const RoundArgs &a, int64_t c, const unsigned long long *lst, int n,
-                                                 int lane)
+// Returns whether the draft is accepted, and in token the position's token
+// (the draft, or the draw), in every lane: every lane computes the same sums
+// (broadcast terms, same order).
+__device__ __noinline__ bool sampled_decide(const RoundArgs &a, int64_t c, const unsigned long long *lst, int n,
+                                            int lane, int32_t &token_out)
 {
     const int gamma = a.gamma, gp1 = gamma + 1;
     const int64_t ln = c / gp1;
@@ -533,6 +533,21 @@ __device__ __noinline__ void sampled_column_done(const RoundArgs &a, int64_t c, 
         }
         token = pick >= 0 ? pick : last_tok;
     }
+    token_out = token;
+    return accepted;
+}
+
+// Sampled verify of target column c (as sampled_decide): the position's
+// token goes to its commit id and its acceptance bit to the lane's ticket
+// word, as in verify_column_done.
+__device__ __noinline__ void sampled_column_done(const RoundArgs &a, int64_t c, const unsigned long long *lst, int n,
+                                                 int lane)
+{
+    const int gamma = a.gamma, gp1 = gamma + 1;
+    const int64_t ln = c / gp1;
+    const int j = (int)(c - ln * gp1);
+    int32_t token;
+    const bool accepted = sampled_decide(a, c, lst, n, lane, token);
     uint32_t word = 0;
     if (lane == 0) {
         a.out_commit[ln * gp1 + j] = token;

@@ -358,6 +358,65 @@ __device__ __noinline__ void exact_scan(const RunView r, int64_t cb, int64_t ce,
     merge_lists(s, kk, lane, w);
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const unsigned int *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Target column c (position j of lane ln) is decided: its commit token and
+// whether draft j was accepted (greedy verify: the argmax and whether it
+// equals draft j; sampled verify: see sampled_decide).  Warp-wide.  No fence
+// anywhere: the column leaves token + 2 (never 0) in its slot of the lane
+// (the column-certificate words, zero between launches), then adds to the
+// lane's ticket word, relaxed: 1 (bits 0-7: positions done) and bit 8 + j
+// if accepted.  The last position's warp computes the accept length acc
+// from the word, reads every slot of the lane -- waiting (bounded) for one
+// that is not visible yet, since its column took the ticket after writing
+// it -- clears them, and writes all commit ids: each position's token up to
+// acc (below acc the accepted drafts), -1 after it.  A column's own commit
+// id is thus only ever written by the lane's last position.
+__device__ __forceinline__ void lane_done(const RoundArgs &a, int64_t c, int32_t token, bool accepted, int lane)
+{
+    const int gamma = a.gamma, gp1 = gamma + 1;
+    const int64_t ln = c / gp1;
+    const int j = (int)(c - ln * gp1);
+    unsigned int *slot = a.col_cert + a.d_cols + ln * gp1;
+    uint32_t word = 0;
+    if (lane == 0) {
+        asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(slot + j), "r"((uint32_t)token + 2u) : "memory");
+        const uint32_t add = 1u + ((accepted ? 1u : 0u) << (8 + j));
+        asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], %2;" : "=r"(word) : "l"(a.lane_ticket + ln), "r"(add)
+                     : "memory");
+        word += add;
+    }
+    word = __shfl_sync(kFull, word, 0);
+    if ((word & 0xFFu) != (uint32_t)gp1) return;
+    const uint32_t flags = (word >> 8) & ((1u << gamma) - 1u);
+    const int acc = __ffs(~flags) - 1 < gamma ? __ffs(~flags) - 1 : gamma;
+    if (lane < gp1) {
+        uint32_t v = ld_relaxed_u32(slot + lane);
+        if (v == 0u) {
+            const uint64_t t0 = global_ns();
+            while ((v = ld_relaxed_u32(slot + lane)) == 0u) {
+                if (global_ns() - t0 > kWaitLimitNs) {
+                    atomicOr(&g_wait_timeouts, 1u);
+                    v = 1u;   // commit id -1
+                    break;
+                }
+            }
+        }
+        slot[lane] = 0u;   // after the read of the column's value: ready for the next launch
+        a.out_commit[ln * gp1 + lane] = lane <= acc ? (int32_t)(v - 2u) : -1;
+    }
+    count_lane(a.counters, gamma, acc, lane);
+    if (lane == 0) {
+        a.out_accept[ln] = acc;
+        a.lane_ticket[ln] = 0u;   // ready for the next launch
+    }
+}
+
 // Phase 2 for column c of run r (every thread of the CTA calls it): the
 // column's top-kk (draft: to the outputs; target: to verify).  shared: the
 // column's ticket is to be cleared for the next launch.  Every key of the
@@ -375,6 +434,14 @@ __device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r
     const uint16_t *k0 = hin ? r.H + c * 512 + t : r.G + bf * 512 + t;
     const uint16_t *kr = r.G + bf * 512 + t;   // keys of batch bf + i at kr[512 i] for i >= 1
     const RunView rv = view_of(r);
+    // a target column's draft token (-2: none, the bonus position), early
+    int32_t draft_tok = -2;
+    if (!r.draft && t == 0) {
+        const int gp1 = a.gamma + 1;
+        const int64_t ln = c / gp1;
+        const int j = (int)(c - ln * gp1);
+        if (j < a.gamma) draft_tok = __ldg(a.drafts + ln * a.gamma + j);
+    }
     __syncthreads();
     if (t < kKeyRows) s.tiecnt[t] = 0u;
 
@@ -527,8 +594,11 @@ __device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r
             a.out_ids[c * kk + i] = (int32_t)entry_id(e);
         }
     } else if (w == 0) {
-        if (a.uniforms) sampled_column_done(a, c, s.wl[0], kk, lane);
-        else verify_column_done(a, c, (int32_t)entry_id(s.wl[0][0]), lane);
+        int32_t token = (int32_t)entry_id(s.wl[0][0]);
+        bool accepted;
+        if (a.uniforms) accepted = sampled_decide(a, c, s.wl[0], kk, lane, token);
+        else accepted = __shfl_sync(kFull, draft_tok, 0) == token;
+        lane_done(a, c, token, accepted, lane);
     }
     if (t == 0) {
         s.ncand = 0u;
