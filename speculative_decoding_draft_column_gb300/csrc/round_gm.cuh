@@ -421,18 +421,28 @@ __device__ __forceinline__ void lane_done(const RoundArgs &a, int64_t c, int32_t
 // column's top-kk (draft: to the outputs; target: to verify).  shared: the
 // column's ticket is to be cleared for the next launch.  Every key of the
 // column is written (this CTA's own keys: before the barrier at entry).
-template <int U>
+template <int U, bool COLS>
 __device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r, int64_t c, bool shared, Smem &s)
 {
     constexpr int64_t B = 512 * U;
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     const int kk = r.kk;
     const int64_t cb = c * r.V, ce = cb + r.V;
-    const int64_t bf = batch_of<U>(r, cb), bl = batch_of<U>(r, ce - 1);
-    const bool hin = elem_lo<U>(r, bf) < cb;   // the column starts inside batch bf: its keys there are in H
-    const int nb = (int)(bl - bf + 1);
-    const uint16_t *k0 = hin ? r.H + c * 512 + t : r.G + bf * 512 + t;
-    const uint16_t *kr = r.G + bf * 512 + t;   // keys of batch bf + i at kr[512 i] for i >= 1
+    // the column's groups: batch i (of nb), thread t' = vectors jbase + i B + u 512 + t'
+    int64_t jbase;
+    int nb;
+    const uint16_t *k0 = nullptr, *kr = nullptr;   // slice mode: keys of batch 0, and of batch i at kr[512 i]
+    if (COLS) {
+        jbase = (cb + r.mis) >> 3;
+        nb = (int)((((ce - 1 + r.mis) >> 3) - jbase) / B + 1);
+    } else {
+        const int64_t bf = batch_of<U>(r, cb), bl = batch_of<U>(r, ce - 1);
+        const bool hin = elem_lo<U>(r, bf) < cb;   // the column starts inside batch bf: its keys there are in H
+        jbase = bf * B;
+        nb = (int)(bl - bf + 1);
+        k0 = hin ? r.H + c * 512 + t : r.G + bf * 512 + t;
+        kr = r.G + bf * 512 + t;
+    }
     const RunView rv = view_of(r);
     // a target column's draft token (-2: none, the bonus position), early
     int32_t draft_tok = -2;
@@ -445,17 +455,25 @@ __device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r
     __syncthreads();
     if (t < kKeyRows) s.tiecnt[t] = 0u;
 
-    // 1. the column's group keys: sixteen loads in flight per thread, kept in
-    //    shared memory (the first kKeyRows batches); this thread's maximum
+    // 1. the column's group keys in shared memory (the first kKeyRows
+    //    batches; column mode: there already, from the stream; slice mode:
+    //    sixteen loads in flight per thread); this thread's maximum
     uint32_t mt = 0;
-    for (int i0 = 0; i0 < nb; i0 += 16) {
-        uint32_t kv[16];
+    if (COLS) {
+        for (int i = 0; i < nb; ++i) {
+            const uint32_t key = s.keys[i][t];
+            mt = key > mt ? key : mt;
+        }
+    } else {
+        for (int i0 = 0; i0 < nb; i0 += 16) {
+            uint32_t kv[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) kv[q] = i0 + q < nb ? __ldcg(i0 + q == 0 ? k0 : kr + 512 * (i0 + q)) : 0u;
+            for (int q = 0; q < 16; ++q) kv[q] = i0 + q < nb ? __ldcg(i0 + q == 0 ? k0 : kr + 512 * (i0 + q)) : 0u;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-            mt = kv[q] > mt ? kv[q] : mt;
-            if (i0 + q < kKeyRows) s.keys[i0 + q][t] = (uint16_t)kv[q];
+            for (int q = 0; q < 16; ++q) {
+                mt = kv[q] > mt ? kv[q] : mt;
+                if (i0 + q < kKeyRows) s.keys[i0 + q][t] = (uint16_t)kv[q];
+            }
         }
     }
     // 2. the bound T: the kk-th largest section maximum (sections of 8 threads)
@@ -537,7 +555,7 @@ __device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r
                 q[h] = make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
                 if (p < nv) {
                     const uint32_t gid = s.grp[p / U];
-                    const int64_t j = (bf + (gid >> 9)) * B + (p % U) * 512 + (gid & 511u);
+                    const int64_t j = jbase + (int64_t)(gid >> 9) * B + (p % U) * 512 + (gid & 511u);
                     if (j < r.NV) {
                         jv[h] = j;
                         q[h] = load_col_vec(rv, j, cb, ce);
@@ -634,7 +652,54 @@ __device__ __forceinline__ uint32_t arrive_at_end(unsigned int *ticket, uint32_t
     return atom_add_acq_rel(ticket, 1u) == others ? 1u : 0u;
 }
 
+// Column mode (U = 8): CTA b owns whole columns [floor(b cols / W),
+// floor((b + 1) cols / W)) of its run and streams them one by one in
+// batches counted from each column's first vector, writing the group keys
+// straight into shared memory; every column is finished right after its
+// last batch, by the CTA alone (no tickets, no keys in global memory).
 template <int U>
+__device__ __forceinline__ void stream_columns(const RoundArgs &a, const GmRun &r, int bi, Smem &s)
+{
+    constexpr int P = kLoads / U;
+    constexpr int64_t B = 512 * U;
+    const int t = threadIdx.x;
+    const int64_t cols = r.N / r.V;
+    const int64_t c0 = bi * cols / r.W, c1 = (bi + 1) * cols / r.W;
+    for (int64_t c = c0; c < c1; ++c) {
+        const int64_t cb = c * r.V, ce = cb + r.V;
+        const int64_t jf = (cb + r.mis) >> 3, jl = (ce - 1 + r.mis) >> 3;
+        const int nb = (int)((jl - jf) / B + 1);
+        for (int i0 = 0; i0 < nb; i0 += P) {
+            uint4 q[kLoads];
+#pragma unroll
+            for (int v = 0; v < kLoads; ++v) {
+                const int64_t j = jf + (int64_t)(i0 + v / U) * B + (v % U) * 512 + t;
+                q[v] = (i0 + v / U < nb && j > jf && j < jl && j >= r.jlo && j < r.jhi)
+                           ? __ldg(r.vb + j) : make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
+            }
+            if (i0 == 0 || i0 + P >= nb) {
+                // the column's first and last vectors, element by element
+#pragma unroll
+                for (int v = 0; v < kLoads; ++v) {
+                    const int64_t j = jf + (int64_t)(i0 + v / U) * B + (v % U) * 512 + t;
+                    if (i0 + v / U < nb && j <= jl && (j == jf || j == jl || j < r.jlo || j >= r.jhi))
+                        q[v] = load_edge(r.buf, j, r.mis, cb, ce);
+                }
+            }
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                if (i0 + p >= nb) break;
+                uint32_t m = kNaN2;
+#pragma unroll
+                for (int u = 0; u < U; ++u) m = bmax2(m, vmax(q[p * U + u]));
+                s.keys[i0 + p][t] = (uint16_t)key_of(m);
+            }
+        }
+        finish_column<U, true>(a, r, c, false, s);
+    }
+}
+
+template <int U, bool COLS>
 __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_constant__ RoundArgs a)
 {
     constexpr int P = kLoads / U;
@@ -647,12 +712,16 @@ __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_co
     const bool draft = b < a.d_units;
     const GmRun r = make_run<U>(a, draft);
     const int bi = draft ? b : b - a.d_units;
-    const int64_t g0b = slice_lo(r, bi), g1b = slice_lo(r, bi + 1);
-    if (g1b <= g0b) return;
     if (threadIdx.x == 0) {
         s.ncand = 0u;
         s.ngrp = 0u;
     }
+    if (COLS) {
+        stream_columns<U>(a, r, bi, s);
+        return;
+    }
+    const int64_t g0b = slice_lo(r, bi), g1b = slice_lo(r, bi + 1);
+    if (g1b <= g0b) return;
     int64_t cn = elem_lo<U>(r, g0b) / r.V + 1;   // the column after the one in progress
     int64_t cut = cn * r.V;                      // its first element
     const int64_t cl = (elem_hi<U>(r, g1b - 1) - 1) / r.V;
@@ -696,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_co
                 __syncthreads();
                 fin = s.last[0] != 0u;
             }
-            if (fin) finish_column<U>(a, r, c, wf != wl, s);
+            if (fin) finish_column<U, false>(a, r, c, wf != wl, s);
             __syncthreads();   // s.last is read by every thread before it is written again
         }
         if (ending) break;

@@ -125,8 +125,11 @@ spec_status device_state(DeviceState **out)
                                                           cta::kSmemBytes);
         if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
         if (d.occ_c < 1) d.occ_c = 1;
-        void *kg[4] = {reinterpret_cast<void *>(gm::spec_round_kernel<1>), reinterpret_cast<void *>(gm::spec_round_kernel<2>),
-                       reinterpret_cast<void *>(gm::spec_round_kernel<4>), reinterpret_cast<void *>(gm::spec_round_kernel<8>)};
+        void *kg[5] = {reinterpret_cast<void *>(gm::spec_round_kernel<1, false>),
+                       reinterpret_cast<void *>(gm::spec_round_kernel<2, false>),
+                       reinterpret_cast<void *>(gm::spec_round_kernel<4, false>),
+                       reinterpret_cast<void *>(gm::spec_round_kernel<8, false>),
+                       reinterpret_cast<void *>(gm::spec_round_kernel<8, true>)};
         for (void *k : kg) {
             e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gm::kSmemBytes);
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
@@ -250,6 +253,7 @@ struct Plan {
     bool per_cta;
     bool gm;          // the group-maxima kernel
     int gm_u;         // its batch width: 16-byte vectors per thread per batch (1, 2, 4 or 8)
+    bool gm_cols;     // its column mode: each CTA streams and finishes whole columns
     int slots;        // per-warp kernel: 2 for k > 32 (finer seed groups)
     bool mapped;
     int64_t grid;     // CTAs
@@ -268,6 +272,37 @@ bool plan_gm(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, int
     if (nv_d > 0) vmin = a.d_V < vmin ? a.d_V : vmin;
     if (nv_t > 0) vmin = a.t_V < vmin ? a.t_V : vmin;
     if (vmin < gm::kMinV) return false;
+    // Column mode: at least three quarters as many columns as SMs, every
+    // column at least one batch of U = 8 and at most the kKeyRows batches
+    // whose keys a CTA keeps in shared memory.  Each CTA then owns whole
+    // columns: no tickets, no keys in global memory.
+    const int64_t cols_all = (nv_d > 0 ? a.d_cols : 0) + (nv_t > 0 ? a.t_cols : 0);
+    int64_t vmax = 0;
+    if (nv_d > 0) vmax = a.d_V > vmax ? a.d_V : vmax;
+    if (nv_t > 0) vmax = a.t_V > vmax ? a.t_V : vmax;
+    if (4 * cols_all >= 3 * (int64_t)d.sms && vmin >= 8 * 512 * 8 && (vmax / 8 + 2) <= (int64_t)gm::kKeyRows * 512 * 8) {
+        const int64_t W = cols_all < d.sms ? cols_all : d.sms;
+        int64_t ud = 0, ut = 0;
+        if (nv_d > 0 && nv_t > 0) {
+            ud = (W * a.d_cols + cols_all / 2) / cols_all;
+            if (ud < 1) ud = 1;
+            if (ud > W - 1) ud = W - 1;
+            if (ud > a.d_cols) ud = a.d_cols;
+            ut = W - ud < a.t_cols ? W - ud : a.t_cols;
+        } else if (nv_d > 0) {
+            ud = W;
+        } else {
+            ut = W;
+        }
+        a.d_units = (int32_t)ud;
+        a.t_units = (int32_t)ut;
+        p.gm = true;
+        p.gm_u = 8;
+        p.gm_cols = true;
+        p.grid = ud + ut;
+        p.partials = 0;
+        return true;
+    }
     int32_t wd = 0, wt = 0;
     split_units(nv_d, nv_t, d.sms, 512, 1, INT64_MAX / 4, &wd, &wt);
     auto nbatches = [](int64_t nv, int64_t B) { return (nv + B - 1) / B; };
@@ -298,6 +333,7 @@ bool plan_gm(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, int
     a.t_units = (int32_t)(nv_t > 0 ? (wt < nbt ? wt : nbt) : 0);
     p.gm = true;
     p.gm_u = best;
+    p.gm_cols = false;
     p.grid = (int64_t)a.d_units + a.t_units;
     p.partials = entries;
     return true;
@@ -314,6 +350,7 @@ Plan plan_round(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, 
     const bool small = (nv_d + nv_t) * 16 <= kCtaMaxBytesPerSm * (int64_t)d.sms;
     p.gm = false;
     p.gm_u = 0;
+    p.gm_cols = false;
     p.mapped = mapped;
     const int kmax = a.k > a.t_k ? a.k : a.t_k;   // the larger list of the two runs
     p.slots = kmax > 32 ? 2 : 1;
@@ -365,11 +402,13 @@ cudaError_t launch_plan(const Plan &p, const RoundArgs &a, cudaStream_t stream, 
 {
     const unsigned g = (unsigned)p.grid;
     if (p.gm) {
+        const size_t m = gm::kSmemBytes;
+        if (p.gm_cols) return launch_pdl(gm::spec_round_kernel<8, true>, g, gm::kThreads, m, stream, a, pdl);
         switch (p.gm_u) {
-        case 8: return launch_pdl(gm::spec_round_kernel<8>, g, gm::kThreads, gm::kSmemBytes, stream, a, pdl);
-        case 4: return launch_pdl(gm::spec_round_kernel<4>, g, gm::kThreads, gm::kSmemBytes, stream, a, pdl);
-        case 2: return launch_pdl(gm::spec_round_kernel<2>, g, gm::kThreads, gm::kSmemBytes, stream, a, pdl);
-        default: return launch_pdl(gm::spec_round_kernel<1>, g, gm::kThreads, gm::kSmemBytes, stream, a, pdl);
+        case 8: return launch_pdl(gm::spec_round_kernel<8, false>, g, gm::kThreads, m, stream, a, pdl);
+        case 4: return launch_pdl(gm::spec_round_kernel<4, false>, g, gm::kThreads, m, stream, a, pdl);
+        case 2: return launch_pdl(gm::spec_round_kernel<2, false>, g, gm::kThreads, m, stream, a, pdl);
+        default: return launch_pdl(gm::spec_round_kernel<1, false>, g, gm::kThreads, m, stream, a, pdl);
         }
     }
     if (p.per_cta) return launch_pdl(cta::spec_round_kernel, g, cta::kThreads, cta::kSmemBytes, stream, a, pdl);
