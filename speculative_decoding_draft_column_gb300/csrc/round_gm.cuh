@@ -52,13 +52,14 @@ constexpr int64_t kMinV = 8 * 512;    // elements per column at least: a batch t
 struct Smem {
     unsigned long long cand[kCap];
     unsigned long long wl[kWarps][SPEC_MAX_K];   // sorted lists, one per warp; wl[0] ends as the column's list
-    uint32_t grp[kGroupCap];                     // candidate groups: (batch - first batch) << 9 | thread
+    uint32_t grp[kGroupCap];                     // candidate groups above the bound: (batch - first batch) << 9 | thread
+    uint32_t tgrp[kGroupCap];                    // candidate groups at the bound (ties), the same way
     uint16_t keys[kKeyRows][512];                // the column's group keys, [batch - first batch][thread]
     uint32_t sec[64];                            // section maxima
     uint32_t tiecnt[kKeyRows];                   // groups at the bound, per batch
     uint32_t wtie[kWarps];                       // groups at the bound, per warp
     int32_t wn[kWarps];
-    uint32_t ncand, ngrp;
+    uint32_t ncand, ngrp;                        // ngrp: groups above the bound (low 16 bits) and at it (high 16)
     uint32_t last[2];                            // the CTA completes its first / last column
 };
 
@@ -226,18 +227,24 @@ __device__ __forceinline__ uint32_t kth_of_64(uint32_t v0, uint32_t v1, int kk)
     return lo;
 }
 
-// Append the groups of this thread's rows in mask (bit i: batch i of the
-// column) to the group list, one shared atomic per warp.
-__device__ __forceinline__ void append_groups(Smem &s, unsigned long long mask, int lane)
+// Append the groups of this thread's rows in above and tie (bit i: batch i
+// of the column) to the two group lists, one shared atomic per warp on the
+// packed count (above: low 16 bits, ties: high 16 bits; at most 512 * 64 of
+// each).
+__device__ __forceinline__ void append_groups(Smem &s, unsigned long long above, unsigned long long tie, int lane)
 {
     int total;
-    const int excl = warp_exclusive_sum(__popcll(mask), lane, total);
+    const int excl = warp_exclusive_sum(__popcll(above) | (__popcll(tie) << 16), lane, total);
     if (total == 0) return;
-    uint32_t pos = 0;
-    if (lane == 0) pos = atomicAdd(&s.ngrp, (uint32_t)total);
-    pos = __shfl_sync(kFull, pos, 0) + (uint32_t)excl;
-    for (unsigned long long m = mask; m; m &= m - 1, ++pos)
-        if (pos < (uint32_t)kGroupCap) s.grp[pos] = ((uint32_t)(__ffsll((long long)m) - 1) << 9) | (threadIdx.x & 511u);
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(&s.ngrp, (uint32_t)total);
+    base = __shfl_sync(kFull, base, 0) + (uint32_t)excl;
+    uint32_t pa = base & 0xFFFFu, pt = base >> 16;
+    const uint32_t tid = threadIdx.x & 511u;
+    for (unsigned long long m = above; m; m &= m - 1, ++pa)
+        if (pa < (uint32_t)kGroupCap) s.grp[pa] = ((uint32_t)(__ffsll((long long)m) - 1) << 9) | tid;
+    for (unsigned long long m = tie; m; m &= m - 1, ++pt)
+        if (pt < (uint32_t)kGroupCap) s.tgrp[pt] = ((uint32_t)(__ffsll((long long)m) - 1) << 9) | tid;
 }
 
 // Append group id gid of this lane (if take) to the group list, one shared
@@ -492,8 +499,10 @@ __device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r
     //    (they hold kk elements at T, all with smaller ids than any tie
     //    further on).  Each thread marks its rows above / at T in two masks;
     //    one shared atomic per warp appends a mask's groups.
+    int upto = 1 << 30;   // groups at T taken from batches below upto only
     if (nb > kKeyRows) {
-        // a column of more than kKeyRows batches: every group reaching T
+        // a column of more than kKeyRows batches: every group reaching T, in
+        // the first list (a plain count)
         if (__ballot_sync(kFull, mt != 0 && mt >= T) != 0u)
 #pragma unroll 1
             for (int i = 0; i < nb; ++i) {
@@ -510,40 +519,39 @@ __device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r
                 above |= (unsigned long long)(key != 0 && key > T) << i;
                 tie |= (unsigned long long)(key != 0 && key == T) << i;
             }
-        append_groups(s, above, lane);
-        const uint32_t wt = __reduce_add_sync(kFull, (uint32_t)__popcll(tie));
-        if (lane == 0) s.wtie[w] = wt;
+        append_groups(s, above, tie, lane);
         __syncthreads();
-        uint32_t nt = 0;
-#pragma unroll
-        for (int q = 0; q < kWarps; ++q) nt += s.wtie[q];
-        if (r.id_map != nullptr || nt <= (uint32_t)kFewTies) {
-            append_groups(s, tie, lane);
-        } else {
-            // many ties: groups at T per batch, then those of the first
-            // batches holding kk of them
+        if (r.id_map == nullptr && (s.ngrp >> 16) > (uint32_t)kFewTies) {
+            // many ties: groups at T per batch, then the list of groups at T
+            // again, from the first batches holding kk of them only
 #pragma unroll 1
             for (int i = 0; i < nb; ++i) {
                 const uint32_t ni = (uint32_t)__popc(__ballot_sync(kFull, (tie >> i) & 1ull));
                 if (lane == 0 && ni) atomicAdd(&s.tiecnt[i], ni);
             }
             __syncthreads();
-            int upto = nb - 1, acc = 0;
+            int acc = 0;
             for (int i = 0; i < nb; ++i) {
                 acc += (int)s.tiecnt[i];
                 if (acc >= kk) {
-                    upto = i;
+                    upto = i + 1;
                     break;
                 }
             }
-            append_groups(s, upto >= 63 ? tie : tie & ((2ull << upto) - 1ull), lane);
+            const uint32_t keep_above = s.ngrp & 0xFFFFu;
+            __syncthreads();   // every thread has read the count
+            if (t == 0) s.ngrp = keep_above;
+            __syncthreads();
+            append_groups(s, 0ull, upto >= 64 ? tie : tie & ((1ull << upto) - 1ull), lane);
+            __syncthreads();
         }
-        __syncthreads();
     }
-    const int ng = (int)s.ngrp;
+    const int na = nb > kKeyRows ? (int)s.ngrp : (int)(s.ngrp & 0xFFFFu);
+    const int nt = nb > kKeyRows ? 0 : (int)(s.ngrp >> 16);
+    const int ng = na + nt;
     // 4. their elements >= T: one 16-byte vector per thread per pass, up to
     //    four passes' loads in flight
-    if (ng <= kGroupCap) {
+    if (na <= kGroupCap && nt <= kGroupCap) {
         const int nv = ng * U;
         for (int p0 = 0; p0 < nv; p0 += 4 * kThreads) {
             uint4 q[4];
@@ -553,8 +561,9 @@ __device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r
                 const int p = p0 + h * kThreads + t;
                 jv[h] = -1;
                 q[h] = make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
-                if (p < nv) {
-                    const uint32_t gid = s.grp[p / U];
+                const bool at_t = p / U >= na;   // a group at T: only from the batches below upto
+                const uint32_t gid = p < nv ? (at_t ? s.tgrp[p / U - na] : s.grp[p / U]) : 0u;
+                if (p < nv && (!at_t || (int)(gid >> 9) < upto)) {
                     const int64_t j = jbase + (int64_t)(gid >> 9) * B + (p % U) * 512 + (gid & 511u);
                     if (j < r.NV) {
                         jv[h] = j;
@@ -592,7 +601,7 @@ __device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r
     __syncthreads();
     // 5. the kk best, in order
     const int n = (int)s.ncand;
-    if (ng > kGroupCap || n > kCap) {
+    if (na > kGroupCap || nt > kGroupCap || n > kCap) {
         exact_scan(rv, cb, ce, T, s, lane, w);
     } else if (n > kRankMax) {
         select_many(n, kk, s, lane, w);
