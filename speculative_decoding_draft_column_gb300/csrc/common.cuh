@@ -464,9 +464,34 @@ __device__ __noinline__ void verify_column_done(const RoundArgs &a, int64_t c, i
 // (u = uniforms[ln][j][0]); otherwise -- and always at position gamma, the
 // bonus -- the token drawn is the first nucleus token (draft skipped) whose
 // running q exceeds uniforms[ln][j][1] times the total q without the draft.
+// Sums of doubles over the warp: the total in every lane, and the
+// inclusive prefix (lane order) in each lane.
+__device__ __forceinline__ double warp_sum_d(double v)
+{
+#pragma unroll
+    for (int d = 16; d; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
+    return v;
+}
+
+__device__ __forceinline__ double warp_scan_d(double v, int lane)
+{
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const double y = __shfl_up_sync(kFull, v, d);
+        if (lane >= d) v += y;
+    }
+    return v;
+}
+
 // Returns whether the draft is accepted, and in token the position's token
-// (the draft, or the draw), in every lane: every lane computes the same sums
-// (broadcast terms, same order).
+// (the draft, or the draw), in every lane.  List entry t sits in lane t
+// (t < 32) or lane t - 32.  The sums over the list are warp trees and the
+// running sums warp scans, and p and q are products with one reciprocal:
+// their rounding differs from sums in list order by about 1e-16 relative,
+// so a decision can differ from one made in list order only within that
+// distance of its boundary.  FP64 runs at a small fraction of the FP32
+// rate on this GPU: about 80 double instructions per column instead of
+// the 150 of four serial loops of broadcasts.
 __device__ __noinline__ bool sampled_decide(const RoundArgs &a, int64_t c, const unsigned long long *lst, int n,
                                             int lane, int32_t &token_out)
 {
@@ -474,64 +499,61 @@ __device__ __noinline__ bool sampled_decide(const RoundArgs &a, int64_t c, const
     const int64_t ln = c / gp1;
     const int j = (int)(c - ln * gp1);
     const double T = a.temperature;
-    const unsigned long long ea_ = lane < n ? lst[lane] : 0ull, eb_ = lane + 32 < n ? lst[lane + 32] : 0ull;
+    const bool ha = lane < n, hb = lane + 32 < n;
+    const unsigned long long ea_ = ha ? lst[lane] : 0ull, eb_ = hb ? lst[lane + 32] : 0ull;
     const double z0 = (double)bf16_as_float(entry_raw(lst[0])) / T;
-    const double ea = lane < n ? exp((double)bf16_as_float(entry_raw(ea_)) / T - z0) : 0.0;
-    const double eb = lane + 32 < n ? exp((double)bf16_as_float(entry_raw(eb_)) / T - z0) : 0.0;
-    const int32_t ida = lane < n ? (int32_t)entry_id(ea_) : -1, idb = lane + 32 < n ? (int32_t)entry_id(eb_) : -1;
-    double S = 0.0;
-    for (int t = 0; t < n; ++t) {
-        const double va = __shfl_sync(kFull, ea, t & 31), vb = __shfl_sync(kFull, eb, t & 31);
-        S += t < 32 ? va : vb;
+    const double ea = ha ? exp((double)bf16_as_float(entry_raw(ea_)) / T - z0) : 0.0;
+    const double eb = hb ? exp((double)bf16_as_float(entry_raw(eb_)) / T - z0) : 0.0;
+    const int32_t ida = ha ? (int32_t)entry_id(ea_) : -1, idb = hb ? (int32_t)entry_id(eb_) : -1;
+    const double inv = 1.0 / warp_sum_d(ea + eb);
+    const double pa = ea * inv, pb = eb * inv;
+    // the nucleus: the shortest prefix whose running sum reaches top_p
+    const double ca = warp_scan_d(pa, lane);
+    const double cb = __shfl_sync(kFull, ca, 31) + warp_scan_d(pb, lane);
+    const uint32_t ra = __ballot_sync(kFull, ha && ca >= a.top_p), rb = __ballot_sync(kFull, hb && cb >= a.top_p);
+    int last;
+    double C;
+    if (ra) {
+        last = __ffs(ra) - 1;
+        C = __shfl_sync(kFull, ca, last);
+    } else if (rb) {
+        last = 32 + __ffs(rb) - 1;
+        C = __shfl_sync(kFull, cb, last - 32);
+    } else {
+        last = n - 1;
+        C = n > 32 ? __shfl_sync(kFull, cb, (n - 33) & 31) : __shfl_sync(kFull, ca, (n - 1) & 31);
     }
-    const double pa = ea / S, pb = eb / S;
-    double cum = 0.0, C = 0.0;
-    int last = n - 1;
-    bool found = false;
-    for (int t = 0; t < n; ++t) {
-        const double va = __shfl_sync(kFull, pa, t & 31), vb = __shfl_sync(kFull, pb, t & 31);
-        cum += t < 32 ? va : vb;
-        if (!found && cum >= a.top_p) {
-            found = true;
-            last = t;
-            C = cum;
-        }
-    }
-    if (!found) C = cum;
-    const double qa = lane <= last ? pa / C : 0.0, qb = lane + 32 <= last ? pb / C : 0.0;
+    const double invC = 1.0 / C;
+    const double qa = lane <= last ? pa * invC : 0.0, qb = lane + 32 <= last ? pb * invC : 0.0;
     const int32_t draft = j < gamma ? __ldg(a.drafts + ln * gamma + j) : -1;
     const double u = a.uniforms[(ln * gp1 + j) * 2], u2 = a.uniforms[(ln * gp1 + j) * 2 + 1];
     // q of the draft (0 outside the nucleus)
-    const uint32_t ha = __ballot_sync(kFull, lane <= last && ida == draft && draft >= 0);
-    const uint32_t hb = __ballot_sync(kFull, lane + 32 <= last && idb == draft && draft >= 0);
+    const uint32_t da = __ballot_sync(kFull, lane <= last && ida == draft && draft >= 0);
+    const uint32_t db = __ballot_sync(kFull, lane + 32 <= last && idb == draft && draft >= 0);
     double qd = 0.0;
     {
-        const double xa = __shfl_sync(kFull, qa, ha ? __ffs(ha) - 1 : 0);
-        const double xb = __shfl_sync(kFull, qb, hb ? __ffs(hb) - 1 : 0);
-        qd = ha ? xa : (hb ? xb : 0.0);
+        const double xa = __shfl_sync(kFull, qa, da ? __ffs(da) - 1 : 0);
+        const double xb = __shfl_sync(kFull, qb, db ? __ffs(db) - 1 : 0);
+        qd = da ? xa : (db ? xb : 0.0);
     }
     const bool accepted = j < gamma && u < qd;
     int32_t token = draft;
     if (!accepted) {
-        double W = 0.0;
-        for (int t = 0; t <= last; ++t) {
-            const double va = __shfl_sync(kFull, qa, t & 31), vb = __shfl_sync(kFull, qb, t & 31);
-            const int32_t ia = __shfl_sync(kFull, ida, t & 31), ib = __shfl_sync(kFull, idb, t & 31);
-            if ((t < 32 ? ia : ib) != draft) W += t < 32 ? va : vb;
-        }
-        const double target = u2 * W;
-        double run = 0.0;
-        int32_t pick = -1, last_tok = -1;
-        for (int t = 0; t <= last; ++t) {
-            const double va = __shfl_sync(kFull, qa, t & 31), vb = __shfl_sync(kFull, qb, t & 31);
-            const int32_t ia = __shfl_sync(kFull, ida, t & 31), ib = __shfl_sync(kFull, idb, t & 31);
-            const int32_t tok = t < 32 ? ia : ib;
-            if (tok == draft) continue;
-            last_tok = tok;
-            run += t < 32 ? va : vb;
-            if (pick < 0 && run > target) pick = tok;
-        }
-        token = pick >= 0 ? pick : last_tok;
+        // a draw from q without the draft: the first kept token (list order,
+        // the draft skipped) whose running weight exceeds u2 times the total
+        const bool ka = lane <= last && ida != draft, kb = lane + 32 <= last && idb != draft;
+        const double wa = ka ? qa : 0.0, wb = kb ? qb : 0.0;
+        const double target = u2 * warp_sum_d(wa + wb);
+        const double sa = warp_scan_d(wa, lane);
+        const double sb = __shfl_sync(kFull, sa, 31) + warp_scan_d(wb, lane);
+        const uint32_t xa = __ballot_sync(kFull, ka && sa > target), xb = __ballot_sync(kFull, kb && sb > target);
+        const int32_t pa_id = __shfl_sync(kFull, ida, xa ? __ffs(xa) - 1 : 0);
+        const int32_t pb_id = __shfl_sync(kFull, idb, xb ? __ffs(xb) - 1 : 0);
+        // none exceeds it (rounding left the target at the very end): the last kept token
+        const uint32_t la = __ballot_sync(kFull, ka), lb = __ballot_sync(kFull, kb);
+        const int32_t last_a = __shfl_sync(kFull, ida, la ? 31 - __clz((int)la) : 0);
+        const int32_t last_b = __shfl_sync(kFull, idb, lb ? 31 - __clz((int)lb) : 0);
+        token = xa ? pa_id : xb ? pb_id : lb ? last_b : last_a;
     }
     token_out = token;
     return accepted;
