@@ -277,27 +277,32 @@ spec_status spec_shortlist_topk(const uint16_t *hidden, int64_t cols, int64_t d,
 
 /* Which streaming kernel runs a round.  All compute the same results (every
  * output is the unique exact answer); they differ only in speed:
- *   SPEC_KERNEL_GROUPMAX -- two phases in one launch.  The CTAs of a full-GPU
- *                       grid stream their slices keeping only the maximum of
- *                       each thread's group of 8-64 elements (2 bytes of
- *                       scratch per group); the last CTA done with a column
- *                       takes the k-th largest of its threads' maxima as a
- *                       bound, re-reads the few groups that reach it and
- *                       ranks their elements.  Needs V >= 4096 and scratch
- *                       of about 2 bytes per 8-64 logits (the CTA kernel runs
- *                       instead when either is missing, e.g. inside a graph
- *                       capture that the scratch does not yet cover -- one
- *                       call of the same sizes before capturing makes room).
- *                       Fastest while each SM streams a few columns at most.
+ *   SPEC_KERNEL_GROUPMAX -- two phases in one launch.  The stream keeps only
+ *                       the maximum of each thread's group of 64 logits
+ *                       (a 2-byte key); per column, the k-th largest of
+ *                       those maxima bounds the top-k, and only the few
+ *                       groups that reach it are read again and ranked.
+ *                       Column mode (at least 3/4 as many columns as SMs,
+ *                       columns of 32,768 to ~393,000 logits): each CTA
+ *                       owns whole columns and keeps their keys in shared
+ *                       memory; from 1.5 columns per SM on, four of its
+ *                       warps finish one column while twelve stream the
+ *                       next.  Slice mode (otherwise, V >= 4096): CTAs own
+ *                       equal slices and meet per column through tickets,
+ *                       with scratch of about 2 bytes per 8-64 logits (the
+ *                       CTA kernel runs instead inside a graph capture that
+ *                       the scratch does not yet cover -- one call of the
+ *                       same sizes before capturing makes room).
  *   SPEC_KERNEL_CTA  -- the CTAs of a full-GPU grid each stream a contiguous
  *                       slice in 60 KiB chunks; per column one threshold per
  *                       CTA (the k-th best the CTA has seen), kept by a
  *                       merging warp.
  *   SPEC_KERNEL_WARP -- every warp streams its own slice with its own ring,
  *                       buffer and threshold; no coordination inside the
- *                       stream.  Fastest for large rounds.
- *   SPEC_KERNEL_AUTO -- (default) GROUPMAX (else CTA) while the round's
- *                       logits are at most 6 MiB per SM, WARP above.
+ *                       stream.
+ *   SPEC_KERNEL_AUTO -- (default) GROUPMAX in column mode at any size; else,
+ *                       up to 6 MiB of logits per SM, GROUPMAX in slice mode
+ *                       (or CTA where it cannot run); else WARP.
  * The choice is process-wide; SPEC_ERR_ARG for any other value. */
 #define SPEC_KERNEL_AUTO 0
 #define SPEC_KERNEL_WARP 1

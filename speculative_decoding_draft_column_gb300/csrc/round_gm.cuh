@@ -56,6 +56,7 @@ struct Smem {
     uint32_t tgrp[kGroupCap];                    // candidate groups at the bound (ties), the same way
     uint16_t keys[kKeyRows][512];                // the column's group keys, [batch - first batch][thread]
     uint32_t sec[64];                            // section maxima
+    uint32_t smax[512];                          // the group-key maxima of the threads (or slots)
     uint32_t tiecnt[kKeyRows];                   // groups at the bound, per batch
     uint32_t wtie[kWarps];                       // groups at the bound, per warp
     int32_t wn[kWarps];
@@ -247,6 +248,34 @@ __device__ __forceinline__ void append_groups(Smem &s, unsigned long long above,
         if (pt < (uint32_t)kGroupCap) s.tgrp[pt] = ((uint32_t)(__ffsll((long long)m) - 1) << 9) | tid;
 }
 
+// The kk-th largest of the n values v[0 .. n) (n a multiple of 32, at most
+// 512), in every lane of the warp: a bisection between the smallest and the
+// largest.  For kk above 8, where 64 section maxima bound too loosely.
+__device__ __forceinline__ uint32_t kth_of_smem(const uint32_t *v, int n, int kk, int lane)
+{
+    uint32_t x[16];
+    uint32_t lo = 0xFFFFFFFFu, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        x[i] = i * 32 < n ? v[i * 32 + lane] : 0u;
+        if (i * 32 < n) {
+            lo = x[i] < lo ? x[i] : lo;
+            hi = x[i] > hi ? x[i] : hi;
+        }
+    }
+    lo = __reduce_min_sync(kFull, lo);   // all n values reach it
+    hi = __reduce_max_sync(kFull, hi);
+    while (lo < hi) {
+        const uint32_t mid = (lo + hi + 1) >> 1;
+        uint32_t cnt = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) cnt += (i * 32 < n && x[i] >= mid) ? 1u : 0u;
+        if ((int)__reduce_add_sync(kFull, cnt) >= kk) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
 // Append group id gid of this lane (if take) to the group list, one shared
 // atomic per warp.
 __device__ __forceinline__ void append_group(Smem &s, bool take, uint32_t gid, int lane)
@@ -295,14 +324,24 @@ __device__ __forceinline__ unsigned long long make_entry(uint32_t key, uint32_t 
     return ((unsigned long long)key << 48) | ((unsigned long long)(~id) << 16) | raw;
 }
 
-// Warp 0 merges the sixteen warps' sorted lists (s.wl[w][0 .. s.wn[w])) into
-// s.wl[0]: the kk best of all of them.  Every thread of the CTA must call it.
+// A barrier of a team of NW warps: the CTA (id 0) or a named barrier.
+template <int NW, int BAR>
+__device__ __forceinline__ void team_sync()
+{
+    if constexpr (BAR == 0) __syncthreads();
+    else asm volatile("bar.sync %0, %1;" ::"n"(BAR), "n"(NW * 32) : "memory");
+}
+
+// Warp 0 of a team of NW warps merges the team's sorted lists (s.wl[w][0 ..
+// s.wn[w]), w the warp within the team) into s.wl[0]: the kk best of all of
+// them.  Every thread of the team must call it.
+template <int NW, int BAR>
 __device__ __forceinline__ void merge_lists(Smem &s, int kk, int lane, int w)
 {
-    __syncthreads();
+    team_sync<NW, BAR>();
     if (w != 0) return;
     int n0 = s.wn[0];
-    for (int q = 1; q < kWarps; ++q) {
+    for (int q = 1; q < NW; ++q) {
         const int nq = s.wn[q];
         for (int b2 = 0; b2 < nq; b2 += 32) {
             unsigned long long e = b2 + lane < nq ? s.wl[q][b2 + lane] : 0ull;
@@ -313,26 +352,28 @@ __device__ __forceinline__ void merge_lists(Smem &s, int kk, int lane, int w)
 }
 
 // The kk best of the n candidates in s.cand (many of them: ties at the
-// bound), into s.wl[0]: every warp folds a share into its own sorted list,
-// behind the list's kk-th entry, then the lists are merged.
+// bound), into s.wl[0]: every warp of the team folds a share into its own
+// sorted list, behind the list's kk-th entry, then the lists are merged.
+template <int NW, int BAR>
 __device__ __noinline__ void select_many(int n, int kk, Smem &s, int lane, int w)
 {
     unsigned long long *wl = s.wl[w];
     int nw = 0;
-    for (int base = 32 * w; base < n; base += kThreads) {
+    for (int base = 32 * w; base < n; base += NW * 32) {
         unsigned long long e = base + lane < n ? s.cand[base + lane] : 0ull;
         if (nw == kk && e < wl[kk - 1]) e = 0ull;
         nw = cta::list_merge32(wl, nw, e, kk, lane);
     }
     if (lane == 0) s.wn[w] = nw;
-    merge_lists(s, kk, lane, w);
+    merge_lists<NW, BAR>(s, kk, lane, w);
 }
 
 // Exact top-kk of column [cb, ce) among its elements >= T, for any input
 // (the path for massive ties): every warp scans a share of the column's
 // vectors into its own sorted list, keeping only entries above the list's
-// kk-th; the lists are then merged into s.wl[0].  Every thread of the CTA
-// must call it.
+// kk-th; the lists are then merged into s.wl[0].  Every thread of the team
+// (NW warps) must call it.
+template <int NW, int BAR>
 __device__ __noinline__ void exact_scan(const RunView r, int64_t cb, int64_t ce, uint32_t T, Smem &s, int lane, int w)
 {
     const int kk = r.kk;
@@ -340,7 +381,7 @@ __device__ __noinline__ void exact_scan(const RunView r, int64_t cb, int64_t ce,
     int nw = 0;
     unsigned long long thr = 0ull;   // a full list's kk-th entry: only better entries can enter
     const int64_t jf = (cb + r.mis) >> 3, jl = (ce - 1 + r.mis) >> 3;
-    for (int64_t base = jf + 32 * w; base <= jl; base += kThreads) {
+    for (int64_t base = jf + 32 * w; base <= jl; base += NW * 32) {
         const int64_t j = base + lane;
         const uint4 q = j <= jl ? load_col_vec(r, j, cb, ce) : make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
         const int64_t g0 = 8 * j - r.mis;
@@ -362,7 +403,7 @@ __device__ __noinline__ void exact_scan(const RunView r, int64_t cb, int64_t ce,
         }
     }
     if (lane == 0) s.wn[w] = nw;
-    merge_lists(s, kk, lane, w);
+    merge_lists<NW, BAR>(s, kk, lane, w);
 }
 
 __device__ __forceinline__ uint32_t ld_relaxed_u32(const unsigned int *p)
@@ -424,12 +465,20 @@ __device__ __forceinline__ void lane_done(const RoundArgs &a, int64_t c, int32_t
     }
 }
 
-// Phase 2 for column c of run r (every thread of the CTA calls it): the
-// column's top-kk (draft: to the outputs; target: to verify).  shared: the
-// column's ticket is to be cleared for the next launch.  Every key of the
-// column is written (this CTA's own keys: before the barrier at entry).
+// What the candidate steps of phase 2 leave for the last one.
+struct Sel {
+    uint32_t T;          // the bound
+    int upto;            // groups at T taken from batches below upto only
+    bool lost;           // a list overflowed: scan the column instead
+    int32_t draft_tok;   // (thread 0) a target column's draft token; -2: none
+};
+
+// Phase 2 up to the candidates of column c (every thread of the CTA calls
+// it), over the column's first `rows` batches: the bound, the groups that
+// can hold a winner, and their elements >= T in the candidate buffer.  The
+// caller adds the candidates of later batches, if any, and calls rank_emit.
 template <int U, bool COLS>
-__device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r, int64_t c, bool shared, Smem &s)
+__device__ __forceinline__ Sel select_candidates(const RoundArgs &a, const GmRun &r, int64_t c, int rows, Smem &s)
 {
     constexpr int64_t B = 512 * U;
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
@@ -450,6 +499,7 @@ __device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r
         k0 = hin ? r.H + c * 512 + t : r.G + bf * 512 + t;
         kr = r.G + bf * 512 + t;
     }
+    if (nb > rows) nb = rows;
     const RunView rv = view_of(r);
     // a target column's draft token (-2: none, the bonus position), early
     int32_t draft_tok = -2;
@@ -491,8 +541,11 @@ __device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r
         m8 = o > m8 ? o : m8;
     }
     if ((lane & 7) == 0) s.sec[4 * w + (lane >> 3)] = m8;
+    s.smax[t] = mt;
     __syncthreads();
-    const uint32_t T = kth_of_64(s.sec[lane], s.sec[lane + 32], kk);
+    // T: the kk-th largest of 64 section maxima (kk <= 8) or of the 512
+    // threads' maxima; either is the key of kk distinct groups
+    const uint32_t T = kk <= 8 ? kth_of_64(s.sec[lane], s.sec[lane + 32], kk) : kth_of_smem(s.smax, kThreads, kk, lane);
     // 3. the groups to re-read: every group above T, and of the groups at T
     //    (ties) -- with token ids, which grow batch by batch, and more than a
     //    few of them -- only those of the first batches that hold kk of them
@@ -598,13 +651,28 @@ __device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r
             }
         }
     }
+    return Sel{T, upto, na > kGroupCap || nt > kGroupCap, draft_tok};
+}
+
+// Phase 2, the last step for column c: the kk best of the candidates, in
+// order, to the outputs (draft) or to verify (target); the column's ticket
+// cleared if shared.  Every thread of the CTA calls it.
+template <int U>
+__device__ __forceinline__ void rank_emit(const RoundArgs &a, const GmRun &r, int64_t c, bool shared, const Sel &sel,
+                                          Smem &s)
+{
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int kk = r.kk;
+    const int64_t cb = c * r.V, ce = cb + r.V;
+    const uint32_t T = sel.T;
+    const int32_t draft_tok = sel.draft_tok;
+    const RunView rv = view_of(r);
     __syncthreads();
-    // 5. the kk best, in order
     const int n = (int)s.ncand;
-    if (na > kGroupCap || nt > kGroupCap || n > kCap) {
-        exact_scan(rv, cb, ce, T, s, lane, w);
+    if (sel.lost || n > kCap) {
+        exact_scan<kWarps, 0>(rv, cb, ce, T, s, lane, w);
     } else if (n > kRankMax) {
-        select_many(n, kk, s, lane, w);
+        select_many<kWarps, 0>(n, kk, s, lane, w);
     } else {
         for (int i = t; i < n; i += kThreads) {
             const unsigned long long e = s.cand[i];
@@ -633,6 +701,17 @@ __device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r
         if (shared) r.ticket[c] = 0u;   // ready for the next launch
     }
     __syncthreads();
+}
+
+// Phase 2 for column c of run r, all of it (every thread of the CTA calls
+// it).  shared: the column's ticket is to be cleared for the next launch.
+// Every key of the column is written (this CTA's own keys: before the
+// barrier at entry).
+template <int U, bool COLS>
+__device__ __forceinline__ void finish_column(const RoundArgs &a, const GmRun &r, int64_t c, bool shared, Smem &s)
+{
+    const Sel sel = select_candidates<U, COLS>(a, r, c, 1 << 30, s);
+    rank_emit<U>(a, r, c, shared, sel, s);
 }
 
 // Column c's CTAs: those owning its first and last batch.
@@ -671,6 +750,7 @@ __device__ __forceinline__ void stream_columns(const RoundArgs &a, const GmRun &
 {
     constexpr int P = kLoads / U;
     constexpr int64_t B = 512 * U;
+    static_assert(P == 1, "column mode: one batch per step");
     const int t = threadIdx.x;
     const int64_t cols = r.N / r.V;
     const int64_t c0 = bi * cols / r.W, c1 = (bi + 1) * cols / r.W;
@@ -708,7 +788,275 @@ __device__ __forceinline__ void stream_columns(const RoundArgs &a, const GmRun &
     }
 }
 
-template <int U, bool COLS>
+// ---- column mode with finishing warps ----------------------------------------
+//
+// For rounds with several columns per CTA: warps 0-11 stream (384 key slots
+// a batch, two batches of eight loads per thread in flight), warps 12-15
+// finish, one column behind.  The streamers write a column's group keys into
+// one of two shared-memory buffers and arrive on its "full" barrier; the
+// finishing warps wait there, finish the column from the buffer while the
+// streamers fill the other one, and arrive on the buffer's "free" barrier,
+// which the streamers wait on before they fill it again.  A column's finish
+// then costs no stream time as long as the CTA has columns left to stream.
+
+constexpr int kStreamWarps = 12;
+constexpr int kStreamThreads = kStreamWarps * 32;           // key slots of a batch
+constexpr int kFinWarps = kWarps - kStreamWarps;
+constexpr int kFinThreads = kFinWarps * 32;
+constexpr int kSlotsPer = kStreamThreads / kFinThreads;     // slots per finishing thread
+constexpr int kTeamRows = 16;                               // batches of a column at most
+constexpr int kBarTeam = 1, kBarFree = 2, kBarFull = 4;     // named barriers (free and full: + buffer)
+static_assert(kSlotsPer * kFinThreads == kStreamThreads && kSlotsPer * kTeamRows <= 64, "slot masks");
+static_assert(2 * kTeamRows * kStreamThreads <= kKeyRows * 512, "the two key buffers fit in s.keys");
+
+__device__ __forceinline__ void bar_sync_id(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void bar_arrive_id(int id, int n) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+// Key buffer b: [batch][slot].
+__device__ __forceinline__ uint16_t *team_keys(Smem &s, int b)
+{
+    return &s.keys[0][0] + (size_t)b * kTeamRows * kStreamThreads;
+}
+
+// The streamers' part: every column of [c0, c1), one after the other.
+template <int U>
+__device__ __forceinline__ void team_stream(const GmRun &r, int64_t c0, int64_t c1, Smem &s)
+{
+    constexpr int64_t B = (int64_t)kStreamThreads * U;
+    constexpr int P = 16 / U;   // batches a step
+    const int st = threadIdx.x;
+    for (int64_t c = c0; c < c1; ++c) {
+        const int n = (int)(c - c0), b = n & 1;
+        if (n >= 2) bar_sync_id(kBarFree + b, kThreads);   // the finishing warps are done with buffer b
+        uint16_t *keys = team_keys(s, b);
+        const int64_t cb = c * r.V, ce = cb + r.V;
+        const int64_t jf = (cb + r.mis) >> 3, jl = (ce - 1 + r.mis) >> 3;
+        const int nb = (int)((jl - jf) / B + 1);
+        for (int i0 = 0; i0 < nb; i0 += P) {
+            uint4 q[16];
+#pragma unroll
+            for (int v = 0; v < 16; ++v) {
+                const int64_t j = jf + (int64_t)(i0 + v / U) * B + (v % U) * kStreamThreads + st;
+                q[v] = (i0 + v / U < nb && j > jf && j < jl && j >= r.jlo && j < r.jhi)
+                           ? __ldg(r.vb + j) : make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
+            }
+            if (i0 == 0 || i0 + P >= nb) {
+                // the column's first and last vectors, element by element
+#pragma unroll
+                for (int v = 0; v < 16; ++v) {
+                    const int64_t j = jf + (int64_t)(i0 + v / U) * B + (v % U) * kStreamThreads + st;
+                    if (i0 + v / U < nb && j <= jl && (j == jf || j == jl || j < r.jlo || j >= r.jhi))
+                        q[v] = load_edge(r.buf, j, r.mis, cb, ce);
+                }
+            }
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                if (i0 + p >= nb) break;
+                uint32_t m = kNaN2;
+#pragma unroll
+                for (int u = 0; u < U; ++u) m = bmax2(m, vmax(q[p * U + u]));
+                keys[(i0 + p) * kStreamThreads + st] = (uint16_t)key_of(m);
+            }
+        }
+        bar_arrive_id(kBarFull + b, kThreads);   // buffer b holds column c's keys
+    }
+}
+
+// Append the groups of a finishing thread's slots in above and tie (bit
+// 16 q + i: batch i of slot ft + 128 q) to the two group lists, one shared
+// atomic per warp on the packed count (as append_groups).
+__device__ __forceinline__ void team_append_groups(Smem &s, unsigned long long above, unsigned long long tie, int ft,
+                                                   int lane)
+{
+    int total;
+    const int excl = warp_exclusive_sum(__popcll(above) | (__popcll(tie) << 16), lane, total);
+    if (total == 0) return;
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(&s.ngrp, (uint32_t)total);
+    base = __shfl_sync(kFull, base, 0) + (uint32_t)excl;
+    uint32_t pa = base & 0xFFFFu, pt = base >> 16;
+    for (unsigned long long m = above; m; m &= m - 1, ++pa) {
+        const int k = __ffsll((long long)m) - 1;
+        if (pa < (uint32_t)kGroupCap) s.grp[pa] = ((uint32_t)(k & 15) << 9) | (uint32_t)(ft + kFinThreads * (k >> 4));
+    }
+    for (unsigned long long m = tie; m; m &= m - 1, ++pt) {
+        const int k = __ffsll((long long)m) - 1;
+        if (pt < (uint32_t)kGroupCap) s.tgrp[pt] = ((uint32_t)(k & 15) << 9) | (uint32_t)(ft + kFinThreads * (k >> 4));
+    }
+}
+
+// The finishing warps' part for column c, whose keys are in buffer b:
+// phase 2 as in select_candidates and rank_emit, by 128 threads of three
+// key slots each (sections: two threads, six slots), on named barrier 1.
+template <int U>
+__device__ __forceinline__ void team_finish(const RoundArgs &a, const GmRun &r, int64_t c, int b, Smem &s)
+{
+    constexpr int64_t B = (int64_t)kStreamThreads * U;
+    constexpr int NW = kFinWarps, BAR = kBarTeam;
+    const int ft = threadIdx.x - kStreamThreads, lane = ft & 31, w = ft >> 5;
+    const int kk = r.kk;
+    const int64_t cb = c * r.V, ce = cb + r.V;
+    const int64_t jf = (cb + r.mis) >> 3, jl = (ce - 1 + r.mis) >> 3;
+    const int nb = (int)((jl - jf) / B + 1);
+    const uint16_t *keys = team_keys(s, b);
+    const RunView rv = view_of(r);
+    int32_t draft_tok = -2;   // (thread 0) a target column's draft token; -2: none
+    if (!r.draft && ft == 0) {
+        const int gp1 = a.gamma + 1;
+        const int64_t ln = c / gp1;
+        const int j = (int)(c - ln * gp1);
+        if (j < a.gamma) draft_tok = __ldg(a.drafts + ln * a.gamma + j);
+    }
+    if (ft < kKeyRows) s.tiecnt[ft] = 0u;
+    // 1. this thread's slots: their maxima
+    uint32_t ms[kSlotsPer], mt = 0;
+#pragma unroll
+    for (int q = 0; q < kSlotsPer; ++q) {
+        ms[q] = 0;
+        for (int i = 0; i < nb; ++i) {
+            const uint32_t key = keys[i * kStreamThreads + ft + kFinThreads * q];
+            ms[q] = key > ms[q] ? key : ms[q];
+        }
+        mt = ms[q] > mt ? ms[q] : mt;
+    }
+    // 2. the bound: the kk-th largest of 64 section maxima (kk <= 8) or of
+    //    the 384 slot maxima
+    const uint32_t o = __shfl_xor_sync(kFull, mt, 1);
+    if ((lane & 1) == 0) s.sec[ft >> 1] = o > mt ? o : mt;
+#pragma unroll
+    for (int q = 0; q < kSlotsPer; ++q) s.smax[ft + kFinThreads * q] = ms[q];
+    team_sync<NW, BAR>();
+    const uint32_t T = kk <= 8 ? kth_of_64(s.sec[lane], s.sec[lane + 32], kk)
+                               : kth_of_smem(s.smax, kStreamThreads, kk, lane);
+    // 3. the groups above T and at it (bit 16 q + i: batch i of slot q)
+    unsigned long long above = 0ull, tie = 0ull;
+#pragma unroll
+    for (int q = 0; q < kSlotsPer; ++q)
+        if (ms[q] != 0 && ms[q] >= T)
+            for (int i = 0; i < nb; ++i) {
+                const uint32_t key = keys[i * kStreamThreads + ft + kFinThreads * q];
+                above |= (unsigned long long)(key != 0 && key > T) << (16 * q + i);
+                tie |= (unsigned long long)(key != 0 && key == T) << (16 * q + i);
+            }
+    team_append_groups(s, above, tie, ft, lane);
+    team_sync<NW, BAR>();
+    if (r.id_map == nullptr && (s.ngrp >> 16) > (uint32_t)kFewTies) {
+        // many ties: groups at T per batch; again, from the first batches holding kk
+#pragma unroll 1
+        for (int i = 0; i < nb; ++i) {
+            uint32_t ni = 0;
+#pragma unroll
+            for (int q = 0; q < kSlotsPer; ++q) ni += (uint32_t)__popc(__ballot_sync(kFull, (tie >> (16 * q + i)) & 1ull));
+            if (lane == 0 && ni) atomicAdd(&s.tiecnt[i], ni);
+        }
+        team_sync<NW, BAR>();
+        int acc = 0, upto = 16;
+        for (int i = 0; i < nb; ++i) {
+            acc += (int)s.tiecnt[i];
+            if (acc >= kk) {
+                upto = i + 1;
+                break;
+            }
+        }
+        const uint32_t keep_above = s.ngrp & 0xFFFFu;
+        team_sync<NW, BAR>();
+        if (ft == 0) s.ngrp = keep_above;
+        team_sync<NW, BAR>();
+        const unsigned long long rows = upto >= 16 ? 0xFFFFull : (1ull << upto) - 1ull;
+        team_append_groups(s, 0ull, tie & (rows | rows << 16 | rows << 32), ft, lane);
+        team_sync<NW, BAR>();
+    }
+    const int na = (int)(s.ngrp & 0xFFFFu), nt = (int)(s.ngrp >> 16);
+    const bool lost = na > kGroupCap || nt > kGroupCap;
+    // 4. their elements >= T: one 16-byte vector per thread per pass
+    if (!lost) {
+        const int nv = (na + nt) * U;
+        for (int p0 = 0; p0 < nv; p0 += kFinThreads) {
+            const int p = p0 + ft;
+            uint4 qv = make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
+            int64_t j = 0;
+            if (p < nv) {
+                const uint32_t gid = p / U < na ? s.grp[p / U] : s.tgrp[p / U - na];
+                j = jf + (int64_t)(gid >> 9) * B + (p % U) * kStreamThreads + (gid & 511u);
+                if (j < r.NV) qv = load_col_vec(rv, j, cb, ce);
+            }
+            uint32_t mask = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t key = order_key(half_of(qv, e));
+                mask |= (key != 0 && key >= T) ? 1u << e : 0u;
+            }
+            int total;
+            const int excl = warp_exclusive_sum(__popc(mask), lane, total);
+            if (total == 0) continue;
+            uint32_t pos = 0;
+            if (lane == 0) pos = atomicAdd(&s.ncand, (uint32_t)total);
+            pos = __shfl_sync(kFull, pos, 0) + (uint32_t)excl;
+            for (uint32_t m = mask; m; m &= m - 1, ++pos) {
+                const int e = __ffs(m) - 1;
+                const uint32_t raw = half_of(qv, e);
+                uint32_t id = (uint32_t)(8 * j - r.mis - cb + e);
+                if (r.id_map) id = (uint32_t)__ldg(r.id_map + id);
+                if (pos < (uint32_t)kCap) s.cand[pos] = make_entry(order_key(raw), id, raw);
+            }
+        }
+    }
+    team_sync<NW, BAR>();
+    // 5. the kk best, in order
+    const int n = (int)s.ncand;
+    if (lost || n > kCap) {
+        exact_scan<NW, BAR>(rv, cb, ce, T, s, lane, w);
+    } else if (n > kRankMax) {
+        select_many<NW, BAR>(n, kk, s, lane, w);
+    } else {
+        for (int i = ft; i < n; i += kFinThreads) {
+            const unsigned long long e = s.cand[i];
+            int rank = 0;
+            for (int jj = 0; jj < n; ++jj) rank += s.cand[jj] > e ? 1 : 0;
+            if (rank < kk) s.wl[0][rank] = e;
+        }
+    }
+    team_sync<NW, BAR>();
+    if (r.draft) {
+        for (int i = ft; i < kk; i += kFinThreads) {
+            const unsigned long long e = s.wl[0][i];
+            a.out_vals[c * kk + i] = entry_raw(e);
+            a.out_ids[c * kk + i] = (int32_t)entry_id(e);
+        }
+    } else if (w == 0) {
+        int32_t token = (int32_t)entry_id(s.wl[0][0]);
+        bool accepted;
+        if (a.uniforms) accepted = sampled_decide(a, c, s.wl[0], kk, lane, token);
+        else accepted = __shfl_sync(kFull, draft_tok, 0) == token;
+        lane_done(a, c, token, accepted, lane);
+    }
+    if (ft == 0) {
+        s.ncand = 0u;
+        s.ngrp = 0u;
+    }
+    team_sync<NW, BAR>();
+}
+
+// The finishing warps' part: every column of [c0, c1), one column behind
+// the streamers.
+template <int U>
+__device__ __forceinline__ void team_finish_all(const RoundArgs &a, const GmRun &r, int64_t c0, int64_t c1, Smem &s)
+{
+    if (threadIdx.x == kStreamThreads) {
+        s.ncand = 0u;
+        s.ngrp = 0u;
+    }
+    team_sync<kFinWarps, kBarTeam>();
+    for (int64_t c = c0; c < c1; ++c) {
+        const int n = (int)(c - c0), b = n & 1;
+        bar_sync_id(kBarFull + b, kThreads);   // buffer b holds column c's keys
+        team_finish<U>(a, r, c, b, s);
+        if (c + 2 < c1) bar_arrive_id(kBarFree + b, kThreads);   // the streamers may fill buffer b again
+    }
+}
+
+// MODE 0: slice mode; 1: column mode; 2: column mode with finishing warps.
+template <int U, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_constant__ RoundArgs a)
 {
     constexpr int P = kLoads / U;
@@ -725,8 +1073,15 @@ __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_co
         s.ncand = 0u;
         s.ngrp = 0u;
     }
-    if (COLS) {
+    if constexpr (MODE == 1) {
         stream_columns<U>(a, r, bi, s);
+        return;
+    }
+    if constexpr (MODE == 2) {
+        const int64_t cols = r.N / r.V;
+        const int64_t c0 = bi * cols / r.W, c1 = (bi + 1) * cols / r.W;
+        if (threadIdx.x < kStreamThreads) team_stream<U>(r, c0, c1, s);
+        else team_finish_all<U>(a, r, c0, c1, s);
         return;
     }
     const int64_t g0b = slice_lo(r, bi), g1b = slice_lo(r, bi + 1);

@@ -125,11 +125,12 @@ spec_status device_state(DeviceState **out)
                                                           cta::kSmemBytes);
         if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
         if (d.occ_c < 1) d.occ_c = 1;
-        void *kg[5] = {reinterpret_cast<void *>(gm::spec_round_kernel<1, false>),
-                       reinterpret_cast<void *>(gm::spec_round_kernel<2, false>),
-                       reinterpret_cast<void *>(gm::spec_round_kernel<4, false>),
-                       reinterpret_cast<void *>(gm::spec_round_kernel<8, false>),
-                       reinterpret_cast<void *>(gm::spec_round_kernel<8, true>)};
+        void *kg[6] = {reinterpret_cast<void *>(gm::spec_round_kernel<1, 0>),
+                       reinterpret_cast<void *>(gm::spec_round_kernel<2, 0>),
+                       reinterpret_cast<void *>(gm::spec_round_kernel<4, 0>),
+                       reinterpret_cast<void *>(gm::spec_round_kernel<8, 0>),
+                       reinterpret_cast<void *>(gm::spec_round_kernel<8, 1>),
+                       reinterpret_cast<void *>(gm::spec_round_kernel<8, 2>)};
         for (void *k : kg) {
             e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gm::kSmemBytes);
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
@@ -253,7 +254,7 @@ struct Plan {
     bool per_cta;
     bool gm;          // the group-maxima kernel
     int gm_u;         // its batch width: 16-byte vectors per thread per batch (1, 2, 4 or 8)
-    bool gm_cols;     // its column mode: each CTA streams and finishes whole columns
+    int gm_mode;      // its mode: 0 slices, 1 whole columns per CTA, 2 whole columns with finishing warps
     int slots;        // per-warp kernel: 2 for k > 32 (finer seed groups)
     bool mapped;
     int64_t grid;     // CTAs
@@ -266,7 +267,8 @@ struct Plan {
 // of the most loaded CTA by a third: a narrower batch balances small rounds
 // better but gives a column's finishing CTA more group keys to read.  False
 // if no width fits, or the group keys would not fit in max_partials entries.
-bool plan_gm(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, int64_t max_partials, Plan &p)
+bool plan_gm(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, int64_t max_partials, bool slices,
+             Plan &p)
 {
     int64_t vmin = INT64_MAX;
     if (nv_d > 0) vmin = a.d_V < vmin ? a.d_V : vmin;
@@ -280,6 +282,11 @@ bool plan_gm(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, int
     int64_t vmax = 0;
     if (nv_d > 0) vmax = a.d_V > vmax ? a.d_V : vmax;
     if (nv_t > 0) vmax = a.t_V > vmax ? a.t_V : vmax;
+    // With at least 1.5 columns per SM and columns of at most kTeamRows
+    // batches of 384 x 8 vectors, finishing warps take the columns' finish
+    // off the stream.
+    const bool team = 2 * cols_all >= 3 * (int64_t)d.sms &&
+                      (vmax / 8 + 2) <= (int64_t)gm::kTeamRows * gm::kStreamThreads * 8;
     if (4 * cols_all >= 3 * (int64_t)d.sms && vmin >= 8 * 512 * 8 && (vmax / 8 + 2) <= (int64_t)gm::kKeyRows * 512 * 8) {
         const int64_t W = cols_all < d.sms ? cols_all : d.sms;
         int64_t ud = 0, ut = 0;
@@ -298,11 +305,12 @@ bool plan_gm(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, int
         a.t_units = (int32_t)ut;
         p.gm = true;
         p.gm_u = 8;
-        p.gm_cols = true;
+        p.gm_mode = team ? 2 : 1;
         p.grid = ud + ut;
         p.partials = 0;
         return true;
     }
+    if (!slices) return false;
     int32_t wd = 0, wt = 0;
     split_units(nv_d, nv_t, d.sms, 512, 1, INT64_MAX / 4, &wd, &wt);
     auto nbatches = [](int64_t nv, int64_t B) { return (nv + B - 1) / B; };
@@ -333,7 +341,7 @@ bool plan_gm(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, int
     a.t_units = (int32_t)(nv_t > 0 ? (wt < nbt ? wt : nbt) : 0);
     p.gm = true;
     p.gm_u = best;
-    p.gm_cols = false;
+    p.gm_mode = 0;
     p.grid = (int64_t)a.d_units + a.t_units;
     p.partials = entries;
     return true;
@@ -350,13 +358,16 @@ Plan plan_round(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, 
     const bool small = (nv_d + nv_t) * 16 <= kCtaMaxBytesPerSm * (int64_t)d.sms;
     p.gm = false;
     p.gm_u = 0;
-    p.gm_cols = false;
+    p.gm_mode = 0;
     p.mapped = mapped;
     const int kmax = a.k > a.t_k ? a.k : a.t_k;   // the larger list of the two runs
     p.slots = kmax > 32 ? 2 : 1;
     a.pstride = kmax + 2;
-    if ((choice == SPEC_KERNEL_GROUPMAX || (choice == SPEC_KERNEL_AUTO && small)) &&
-        plan_gm(d, a, nv_d, nv_t, max_partials < gm_max ? max_partials : gm_max, p))
+    // The group-maxima kernel: its column modes at any size, its slice mode
+    // up to 6 MiB of logits per SM (its group keys live in scratch).
+    if ((choice == SPEC_KERNEL_GROUPMAX || choice == SPEC_KERNEL_AUTO) &&
+        plan_gm(d, a, nv_d, nv_t, max_partials < gm_max ? max_partials : gm_max,
+                choice == SPEC_KERNEL_GROUPMAX || small, p))
         return p;
     p.per_cta = choice == SPEC_KERNEL_CTA || choice == SPEC_KERNEL_GROUPMAX || (choice == SPEC_KERNEL_AUTO && small);
     if (p.per_cta) {
@@ -403,12 +414,13 @@ cudaError_t launch_plan(const Plan &p, const RoundArgs &a, cudaStream_t stream, 
     const unsigned g = (unsigned)p.grid;
     if (p.gm) {
         const size_t m = gm::kSmemBytes;
-        if (p.gm_cols) return launch_pdl(gm::spec_round_kernel<8, true>, g, gm::kThreads, m, stream, a, pdl);
+        if (p.gm_mode == 2) return launch_pdl(gm::spec_round_kernel<8, 2>, g, gm::kThreads, m, stream, a, pdl);
+        if (p.gm_mode == 1) return launch_pdl(gm::spec_round_kernel<8, 1>, g, gm::kThreads, m, stream, a, pdl);
         switch (p.gm_u) {
-        case 8: return launch_pdl(gm::spec_round_kernel<8, false>, g, gm::kThreads, m, stream, a, pdl);
-        case 4: return launch_pdl(gm::spec_round_kernel<4, false>, g, gm::kThreads, m, stream, a, pdl);
-        case 2: return launch_pdl(gm::spec_round_kernel<2, false>, g, gm::kThreads, m, stream, a, pdl);
-        default: return launch_pdl(gm::spec_round_kernel<1, false>, g, gm::kThreads, m, stream, a, pdl);
+        case 8: return launch_pdl(gm::spec_round_kernel<8, 0>, g, gm::kThreads, m, stream, a, pdl);
+        case 4: return launch_pdl(gm::spec_round_kernel<4, 0>, g, gm::kThreads, m, stream, a, pdl);
+        case 2: return launch_pdl(gm::spec_round_kernel<2, 0>, g, gm::kThreads, m, stream, a, pdl);
+        default: return launch_pdl(gm::spec_round_kernel<1, 0>, g, gm::kThreads, m, stream, a, pdl);
         }
     }
     if (p.per_cta) return launch_pdl(cta::spec_round_kernel, g, cta::kThreads, cta::kSmemBytes, stream, a, pdl);
