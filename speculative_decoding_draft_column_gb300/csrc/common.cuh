@@ -483,6 +483,81 @@ __device__ __forceinline__ double warp_scan_d(double v, int lane)
     return v;
 }
 
+__device__ __forceinline__ float warp_sum_f(float v)
+{
+#pragma unroll
+    for (int d = 16; d; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
+    return v;
+}
+
+__device__ __forceinline__ float warp_scan_f(float v, int lane)
+{
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float y = __shfl_up_sync(kFull, v, d);
+        if (lane >= d) v += y;
+    }
+    return v;
+}
+
+// The decisions of sampled_decide in float32, where each is certain.  Each
+// term e_t = exp((v_t - v_0) / T) is computed with an absolute error below
+// 3e-7 (the difference of two bf16 values, one multiplication by 1/T and
+// expf each round once, and |x| e^x <= 1/e bounds what a relative error in
+// the exponent does), so the probabilities p_t, their running sums and,
+// with a nucleus sum of at least 1/4, the q_t and their running sums are
+// off by less than 1e-4.  A decision whose float32 margin is at least 2e-4
+// is therefore the one float64 takes.  Returns false -- nothing decided,
+// float64 decides -- when a margin is smaller, the nucleus sum is below
+// 1/4, or the list is longer than 32.
+__device__ __forceinline__ bool sampled_decide_f32(const RoundArgs &a, const unsigned long long *lst, int n, int lane,
+                                                   bool has_draft, int32_t draft, double u, double u2, bool &accepted,
+                                                   int32_t &token)
+{
+    constexpr float kSure = 2e-4f;
+    if (n > 32) return false;
+    const float invT = (float)(1.0 / a.temperature);
+    const bool h = lane < n;
+    const unsigned long long e_ = h ? lst[lane] : 0ull;
+    const float v0 = bf16_as_float(entry_raw(lst[0]));
+    const float e = h ? expf((bf16_as_float(entry_raw(e_)) - v0) * invT) : 0.0f;
+    const int32_t id = h ? (int32_t)entry_id(e_) : -1;
+    const float p = e / warp_sum_f(e);
+    const float cp = warp_scan_f(p, lane);
+    const float top_p = (float)a.top_p;
+    const uint32_t reach = __ballot_sync(kFull, h && cp >= top_p);
+    const int last = reach ? __ffs(reach) - 1 : n - 1;
+    // the nucleus cut: the running sum at it clears top_p (when it reaches
+    // it at all) and the one before falls short of it, both by kSure
+    const float c_last = __shfl_sync(kFull, cp, last);
+    const float c_prev = __shfl_sync(kFull, cp, last > 0 ? last - 1 : 0);
+    if (reach && c_last - top_p < kSure) return false;
+    if (last > 0 && top_p - c_prev < kSure) return false;
+    if (!(c_last >= 0.25f)) return false;   // also a NaN (a column topped by -Inf)
+    const float q = lane <= last ? p / c_last : 0.0f;
+    const uint32_t dm = __ballot_sync(kFull, lane <= last && id == draft && has_draft);
+    const float qd = dm ? __shfl_sync(kFull, q, __ffs(dm) - 1) : 0.0f;
+    if (has_draft && dm && fabs(u - (double)qd) < (double)kSure) return false;
+    accepted = has_draft && u < (double)qd;
+    if (accepted) {
+        token = draft;
+        return true;
+    }
+    // the draw: the first kept token (the draft skipped) whose running
+    // weight exceeds u2 times the total
+    const bool k = lane <= last && !(has_draft && id == draft);
+    const float wgt = k ? q : 0.0f;
+    const float target = (float)u2 * warp_sum_f(wgt);
+    const float run = warp_scan_f(wgt, lane);
+    const uint32_t x = __ballot_sync(kFull, k && run > target);
+    if (!x) return false;
+    const int pick = __ffs(x) - 1;
+    const float r_pick = __shfl_sync(kFull, run, pick), r_prev = __shfl_sync(kFull, run - wgt, pick);
+    if (r_pick - target < kSure || target - r_prev < kSure) return false;
+    token = __shfl_sync(kFull, id, pick);
+    return true;
+}
+
 // Returns whether the draft is accepted, and in token the position's token
 // (the draft, or the draw), in every lane.  List entry t sits in lane t
 // (t < 32) or lane t - 32.  The sums over the list are warp trees and the
@@ -498,6 +573,16 @@ __device__ __noinline__ bool sampled_decide(const RoundArgs &a, int64_t c, const
     const int gamma = a.gamma, gp1 = gamma + 1;
     const int64_t ln = c / gp1;
     const int j = (int)(c - ln * gp1);
+    const int32_t draft = j < gamma ? __ldg(a.drafts + ln * gamma + j) : -1;
+    const double u = a.uniforms[(ln * gp1 + j) * 2], u2 = a.uniforms[(ln * gp1 + j) * 2 + 1];
+    {
+        bool acc32;
+        int32_t tok32;
+        if (sampled_decide_f32(a, lst, n, lane, j < gamma, draft, u, u2, acc32, tok32)) {
+            token_out = tok32;
+            return acc32;
+        }
+    }
     const double T = a.temperature;
     const bool ha = lane < n, hb = lane + 32 < n;
     const unsigned long long ea_ = ha ? lst[lane] : 0ull, eb_ = hb ? lst[lane + 32] : 0ull;
@@ -525,8 +610,6 @@ __device__ __noinline__ bool sampled_decide(const RoundArgs &a, int64_t c, const
     }
     const double invC = 1.0 / C;
     const double qa = lane <= last ? pa * invC : 0.0, qb = lane + 32 <= last ? pb * invC : 0.0;
-    const int32_t draft = j < gamma ? __ldg(a.drafts + ln * gamma + j) : -1;
-    const double u = a.uniforms[(ln * gp1 + j) * 2], u2 = a.uniforms[(ln * gp1 + j) * 2 + 1];
     // q of the draft (0 outside the nucleus)
     const uint32_t da = __ballot_sync(kFull, lane <= last && ida == draft && draft >= 0);
     const uint32_t db = __ballot_sync(kFull, lane + 32 <= last && idb == draft && draft >= 0);

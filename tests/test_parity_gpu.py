@@ -363,6 +363,47 @@ def test_sampled_verify_full_vocabulary():
     gu.assert_verify_equal(gu.run_verify_sampled(r.target, r.drafts, 1.0, 0.95, 20, u), (wa, wc), "sampled C2")
 
 
+def _near_boundary_round(seed, lanes, gamma, V, delta, top_k=20, top_p=0.95):
+    """Drafts and uniforms that put every decision `delta` from its boundary:
+    draft j is the second token of its column's nucleus; u = q(draft) +/-
+    delta (alternating), and where that rejects, u2 puts the draw's target
+    delta above or below the running weight after the first kept token."""
+    t = synth._draft_block(seed, lanes * (gamma + 1), V, 3.0)
+    vals, ids = oracle.topk(t, top_k)
+    drafts = np.empty((lanes, gamma), dtype=np.int32)
+    u = np.empty((lanes, gamma + 1, 2))
+    g = synth.rng(seed + 1, 0)
+    for ln in range(lanes):
+        for j in range(gamma + 1):
+            kept, q = oracle.sampled_column(vals[ln * (gamma + 1) + j], ids[ln * (gamma + 1) + j], 1.0, top_p)
+            sign = 1.0 if (ln + j) % 2 else -1.0
+            if j < gamma:
+                d = kept[1] if len(kept) > 1 else kept[0]
+                drafts[ln, j] = d
+                u[ln, j, 0] = min(max(q[kept.index(d)] + sign * delta, 0.0), 1.0 - 1e-12)
+            else:
+                d = None
+                u[ln, j, 0] = g.random()
+            w = [qt for tok, qt in zip(kept, q) if tok != d]
+            W = float(np.sum(np.array(w, dtype=np.float64))) if w else 1.0
+            r1 = w[0] if w else 0.5
+            u[ln, j, 1] = min(max((r1 - sign * delta) / W, 0.0), 1.0 - 1e-12)
+    return t, drafts, u
+
+
+@pytest.mark.parametrize("delta", [5e-5, 3e-6])
+def test_sampled_decisions_near_boundaries(delta):
+    """Every acceptance and draw lies `delta` from its boundary -- inside the
+    float32 path's margin, so the kernels decide these in float64 -- and
+    must agree with the oracle."""
+    lanes, gamma, V = 6, 7, 50_021
+    t, drafts, u = _near_boundary_round(970 + int(delta * 1e7), lanes, gamma, V, delta)
+    wa, wc, margin = oracle.sampled_verify(t, drafts, 1.0, 0.95, 20, u)
+    assert 1e-9 < margin <= delta * 1.01
+    gu.assert_verify_equal(gu.run_verify_sampled(t.reshape(lanes, gamma + 1, V), drafts, 1.0, 0.95, 20, u),
+                           (wa, wc), f"sampled near boundaries delta={delta}")
+
+
 def test_round_sampled_is_topk_plus_sampled_verify():
     import torch
     sd = gu.sd_module()
