@@ -790,45 +790,54 @@ __device__ __forceinline__ void stream_columns(const RoundArgs &a, const GmRun &
 
 // ---- column mode with finishing warps ----------------------------------------
 //
-// For rounds with several columns per CTA: warps 0-11 stream (384 key slots
-// a batch, two batches of eight loads per thread in flight), warps 12-15
-// finish, one column behind.  The streamers write a column's group keys into
+// For rounds with several columns per CTA: warps 0 .. kStreamWarps-1 stream
+// (one key slot a thread, two batches of eight loads per thread in
+// flight), the other warps finish, one column behind.  The streamers write a column's group keys into
 // one of two shared-memory buffers and arrive on its "full" barrier; the
 // finishing warps wait there, finish the column from the buffer while the
 // streamers fill the other one, and arrive on the buffer's "free" barrier,
 // which the streamers wait on before they fill it again.  A column's finish
 // then costs no stream time as long as the CTA has columns left to stream.
 
-constexpr int kStreamWarps = 12;
-constexpr int kStreamThreads = kStreamWarps * 32;           // key slots of a batch
-constexpr int kFinWarps = kWarps - kStreamWarps;
-constexpr int kFinThreads = kFinWarps * 32;
-constexpr int kSlotsPer = kStreamThreads / kFinThreads;     // slots per finishing thread
-constexpr int kTeamRows = 16;                               // batches of a column at most
+// The split of a CTA's warps in this mode: SW stream, the others finish.
+template <int SW>
+struct Team {
+    static constexpr int kStreamWarps = SW;
+    static constexpr int kStreamThreads = SW * 32;                      // key slots of a batch
+    static constexpr int kFinWarps = kWarps - SW;
+    static constexpr int kFinThreads = kFinWarps * 32;
+    static constexpr int kSlotsPer = kStreamThreads / kFinThreads;      // slots per finishing thread
+    static constexpr int kTeamRows = 64 / kSlotsPer < 24 ? 64 / kSlotsPer : 24;   // batches of a column at most
+    static constexpr int kSecThreads = kFinThreads / 64;                // finishing threads a section
+    static_assert(kSlotsPer * kFinThreads == kStreamThreads && kSlotsPer * kTeamRows <= 64, "slot masks");
+    static_assert(kSecThreads * 64 == kFinThreads && kStreamThreads <= 512, "sections, slot ids in 9 bits");
+    static_assert(2 * kTeamRows * kStreamThreads <= kKeyRows * 512, "the two key buffers fit in s.keys");
+};
 constexpr int kBarTeam = 1, kBarFree = 2, kBarFull = 4;     // named barriers (free and full: + buffer)
-static_assert(kSlotsPer * kFinThreads == kStreamThreads && kSlotsPer * kTeamRows <= 64, "slot masks");
-static_assert(2 * kTeamRows * kStreamThreads <= kKeyRows * 512, "the two key buffers fit in s.keys");
 
 __device__ __forceinline__ void bar_sync_id(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void bar_arrive_id(int id, int n) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
 // Key buffer b: [batch][slot].
+template <int SW>
 __device__ __forceinline__ uint16_t *team_keys(Smem &s, int b)
 {
-    return &s.keys[0][0] + (size_t)b * kTeamRows * kStreamThreads;
+    using TM = Team<SW>;
+    return &s.keys[0][0] + (size_t)b * TM::kTeamRows * TM::kStreamThreads;
 }
 
 // The streamers' part: every column of [c0, c1), one after the other.
-template <int U>
+template <int U, int SW>
 __device__ __forceinline__ void team_stream(const GmRun &r, int64_t c0, int64_t c1, Smem &s)
 {
-    constexpr int64_t B = (int64_t)kStreamThreads * U;
+    using TM = Team<SW>;
+    constexpr int64_t B = (int64_t)TM::kStreamThreads * U;
     constexpr int P = 16 / U;   // batches a step
     const int st = threadIdx.x;
     for (int64_t c = c0; c < c1; ++c) {
         const int n = (int)(c - c0), b = n & 1;
         if (n >= 2) bar_sync_id(kBarFree + b, kThreads);   // the finishing warps are done with buffer b
-        uint16_t *keys = team_keys(s, b);
+        uint16_t *keys = team_keys<SW>(s, b);
         const int64_t cb = c * r.V, ce = cb + r.V;
         const int64_t jf = (cb + r.mis) >> 3, jl = (ce - 1 + r.mis) >> 3;
         const int nb = (int)((jl - jf) / B + 1);
@@ -836,7 +845,7 @@ __device__ __forceinline__ void team_stream(const GmRun &r, int64_t c0, int64_t 
             uint4 q[16];
 #pragma unroll
             for (int v = 0; v < 16; ++v) {
-                const int64_t j = jf + (int64_t)(i0 + v / U) * B + (v % U) * kStreamThreads + st;
+                const int64_t j = jf + (int64_t)(i0 + v / U) * B + (v % U) * TM::kStreamThreads + st;
                 q[v] = (i0 + v / U < nb && j > jf && j < jl && j >= r.jlo && j < r.jhi)
                            ? __ldg(r.vb + j) : make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
             }
@@ -844,7 +853,7 @@ __device__ __forceinline__ void team_stream(const GmRun &r, int64_t c0, int64_t 
                 // the column's first and last vectors, element by element
 #pragma unroll
                 for (int v = 0; v < 16; ++v) {
-                    const int64_t j = jf + (int64_t)(i0 + v / U) * B + (v % U) * kStreamThreads + st;
+                    const int64_t j = jf + (int64_t)(i0 + v / U) * B + (v % U) * TM::kStreamThreads + st;
                     if (i0 + v / U < nb && j <= jl && (j == jf || j == jl || j < r.jlo || j >= r.jhi))
                         q[v] = load_edge(r.buf, j, r.mis, cb, ce);
                 }
@@ -855,7 +864,7 @@ __device__ __forceinline__ void team_stream(const GmRun &r, int64_t c0, int64_t 
                 uint32_t m = kNaN2;
 #pragma unroll
                 for (int u = 0; u < U; ++u) m = bmax2(m, vmax(q[p * U + u]));
-                keys[(i0 + p) * kStreamThreads + st] = (uint16_t)key_of(m);
+                keys[(i0 + p) * TM::kStreamThreads + st] = (uint16_t)key_of(m);
             }
         }
         bar_arrive_id(kBarFull + b, kThreads);   // buffer b holds column c's keys
@@ -863,11 +872,13 @@ __device__ __forceinline__ void team_stream(const GmRun &r, int64_t c0, int64_t 
 }
 
 // Append the groups of a finishing thread's slots in above and tie (bit
-// 16 q + i: batch i of slot ft + 128 q) to the two group lists, one shared
-// atomic per warp on the packed count (as append_groups).
+// TM::kTeamRows q + i: batch i of slot ft + TM::kFinThreads q) to the two group
+// lists, one shared atomic per warp on the packed count (as append_groups).
+template <int SW>
 __device__ __forceinline__ void team_append_groups(Smem &s, unsigned long long above, unsigned long long tie, int ft,
                                                    int lane)
 {
+    using TM = Team<SW>;
     int total;
     const int excl = warp_exclusive_sum(__popcll(above) | (__popcll(tie) << 16), lane, total);
     if (total == 0) return;
@@ -877,28 +888,32 @@ __device__ __forceinline__ void team_append_groups(Smem &s, unsigned long long a
     uint32_t pa = base & 0xFFFFu, pt = base >> 16;
     for (unsigned long long m = above; m; m &= m - 1, ++pa) {
         const int k = __ffsll((long long)m) - 1;
-        if (pa < (uint32_t)kGroupCap) s.grp[pa] = ((uint32_t)(k & 15) << 9) | (uint32_t)(ft + kFinThreads * (k >> 4));
+        if (pa < (uint32_t)kGroupCap)
+            s.grp[pa] = ((uint32_t)(k % TM::kTeamRows) << 9) | (uint32_t)(ft + TM::kFinThreads * (k / TM::kTeamRows));
     }
     for (unsigned long long m = tie; m; m &= m - 1, ++pt) {
         const int k = __ffsll((long long)m) - 1;
-        if (pt < (uint32_t)kGroupCap) s.tgrp[pt] = ((uint32_t)(k & 15) << 9) | (uint32_t)(ft + kFinThreads * (k >> 4));
+        if (pt < (uint32_t)kGroupCap)
+            s.tgrp[pt] = ((uint32_t)(k % TM::kTeamRows) << 9) | (uint32_t)(ft + TM::kFinThreads * (k / TM::kTeamRows));
     }
 }
 
 // The finishing warps' part for column c, whose keys are in buffer b:
-// phase 2 as in select_candidates and rank_emit, by 128 threads of three
-// key slots each (sections: two threads, six slots), on named barrier 1.
-template <int U>
+// phase 2 as in select_candidates and rank_emit, by TM::kFinThreads threads of
+// TM::kSlotsPer key slots each (64 sections of TM::kSecThreads threads), on named
+// barrier 1.
+template <int U, int SW>
 __device__ __forceinline__ void team_finish(const RoundArgs &a, const GmRun &r, int64_t c, int b, Smem &s)
 {
-    constexpr int64_t B = (int64_t)kStreamThreads * U;
-    constexpr int NW = kFinWarps, BAR = kBarTeam;
-    const int ft = threadIdx.x - kStreamThreads, lane = ft & 31, w = ft >> 5;
+    using TM = Team<SW>;
+    constexpr int64_t B = (int64_t)TM::kStreamThreads * U;
+    constexpr int NW = TM::kFinWarps, BAR = kBarTeam;
+    const int ft = threadIdx.x - TM::kStreamThreads, lane = ft & 31, w = ft >> 5;
     const int kk = r.kk;
     const int64_t cb = c * r.V, ce = cb + r.V;
     const int64_t jf = (cb + r.mis) >> 3, jl = (ce - 1 + r.mis) >> 3;
     const int nb = (int)((jl - jf) / B + 1);
-    const uint16_t *keys = team_keys(s, b);
+    const uint16_t *keys = team_keys<SW>(s, b);
     const RunView rv = view_of(r);
     int32_t draft_tok = -2;   // (thread 0) a target column's draft token; -2: none
     if (!r.draft && ft == 0) {
@@ -909,36 +924,41 @@ __device__ __forceinline__ void team_finish(const RoundArgs &a, const GmRun &r, 
     }
     if (ft < kKeyRows) s.tiecnt[ft] = 0u;
     // 1. this thread's slots: their maxima
-    uint32_t ms[kSlotsPer], mt = 0;
+    uint32_t ms[TM::kSlotsPer], mt = 0;
 #pragma unroll
-    for (int q = 0; q < kSlotsPer; ++q) {
+    for (int q = 0; q < TM::kSlotsPer; ++q) {
         ms[q] = 0;
         for (int i = 0; i < nb; ++i) {
-            const uint32_t key = keys[i * kStreamThreads + ft + kFinThreads * q];
+            const uint32_t key = keys[i * TM::kStreamThreads + ft + TM::kFinThreads * q];
             ms[q] = key > ms[q] ? key : ms[q];
         }
         mt = ms[q] > mt ? ms[q] : mt;
     }
     // 2. the bound: the kk-th largest of 64 section maxima (kk <= 8) or of
-    //    the 384 slot maxima
-    const uint32_t o = __shfl_xor_sync(kFull, mt, 1);
-    if ((lane & 1) == 0) s.sec[ft >> 1] = o > mt ? o : mt;
+    //    the slot maxima
+    uint32_t msec = mt;
 #pragma unroll
-    for (int q = 0; q < kSlotsPer; ++q) s.smax[ft + kFinThreads * q] = ms[q];
+    for (int d = 1; d < TM::kSecThreads; d <<= 1) {
+        const uint32_t o = __shfl_xor_sync(kFull, msec, d);
+        msec = o > msec ? o : msec;
+    }
+    if ((lane & (TM::kSecThreads - 1)) == 0) s.sec[ft / TM::kSecThreads] = msec;
+#pragma unroll
+    for (int q = 0; q < TM::kSlotsPer; ++q) s.smax[ft + TM::kFinThreads * q] = ms[q];
     team_sync<NW, BAR>();
     const uint32_t T = kk <= 8 ? kth_of_64(s.sec[lane], s.sec[lane + 32], kk)
-                               : kth_of_smem(s.smax, kStreamThreads, kk, lane);
-    // 3. the groups above T and at it (bit 16 q + i: batch i of slot q)
+                               : kth_of_smem(s.smax, TM::kStreamThreads, kk, lane);
+    // 3. the groups above T and at it (bit TM::kTeamRows q + i: batch i of slot q)
     unsigned long long above = 0ull, tie = 0ull;
 #pragma unroll
-    for (int q = 0; q < kSlotsPer; ++q)
+    for (int q = 0; q < TM::kSlotsPer; ++q)
         if (ms[q] != 0 && ms[q] >= T)
             for (int i = 0; i < nb; ++i) {
-                const uint32_t key = keys[i * kStreamThreads + ft + kFinThreads * q];
-                above |= (unsigned long long)(key != 0 && key > T) << (16 * q + i);
-                tie |= (unsigned long long)(key != 0 && key == T) << (16 * q + i);
+                const uint32_t key = keys[i * TM::kStreamThreads + ft + TM::kFinThreads * q];
+                above |= (unsigned long long)(key != 0 && key > T) << (TM::kTeamRows * q + i);
+                tie |= (unsigned long long)(key != 0 && key == T) << (TM::kTeamRows * q + i);
             }
-    team_append_groups(s, above, tie, ft, lane);
+    team_append_groups<SW>(s, above, tie, ft, lane);
     team_sync<NW, BAR>();
     if (r.id_map == nullptr && (s.ngrp >> 16) > (uint32_t)kFewTies) {
         // many ties: groups at T per batch; again, from the first batches holding kk
@@ -946,11 +966,12 @@ __device__ __forceinline__ void team_finish(const RoundArgs &a, const GmRun &r, 
         for (int i = 0; i < nb; ++i) {
             uint32_t ni = 0;
 #pragma unroll
-            for (int q = 0; q < kSlotsPer; ++q) ni += (uint32_t)__popc(__ballot_sync(kFull, (tie >> (16 * q + i)) & 1ull));
+            for (int q = 0; q < TM::kSlotsPer; ++q)
+                ni += (uint32_t)__popc(__ballot_sync(kFull, (tie >> (TM::kTeamRows * q + i)) & 1ull));
             if (lane == 0 && ni) atomicAdd(&s.tiecnt[i], ni);
         }
         team_sync<NW, BAR>();
-        int acc = 0, upto = 16;
+        int acc = 0, upto = TM::kTeamRows;
         for (int i = 0; i < nb; ++i) {
             acc += (int)s.tiecnt[i];
             if (acc >= kk) {
@@ -962,42 +983,57 @@ __device__ __forceinline__ void team_finish(const RoundArgs &a, const GmRun &r, 
         team_sync<NW, BAR>();
         if (ft == 0) s.ngrp = keep_above;
         team_sync<NW, BAR>();
-        const unsigned long long rows = upto >= 16 ? 0xFFFFull : (1ull << upto) - 1ull;
-        team_append_groups(s, 0ull, tie & (rows | rows << 16 | rows << 32), ft, lane);
+        const unsigned long long rows = (1ull << upto) - 1ull;   // upto <= TM::kTeamRows <= 24
+        unsigned long long keep = 0ull;
+#pragma unroll
+        for (int q = 0; q < TM::kSlotsPer; ++q) keep |= rows << (TM::kTeamRows * q);
+        team_append_groups<SW>(s, 0ull, tie & keep, ft, lane);
         team_sync<NW, BAR>();
     }
     const int na = (int)(s.ngrp & 0xFFFFu), nt = (int)(s.ngrp >> 16);
     const bool lost = na > kGroupCap || nt > kGroupCap;
-    // 4. their elements >= T: one 16-byte vector per thread per pass
+    // 4. their elements >= T: one 16-byte vector per thread per pass, four
+    //    passes' loads in flight
     if (!lost) {
         const int nv = (na + nt) * U;
-        for (int p0 = 0; p0 < nv; p0 += kFinThreads) {
-            const int p = p0 + ft;
-            uint4 qv = make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
-            int64_t j = 0;
-            if (p < nv) {
-                const uint32_t gid = p / U < na ? s.grp[p / U] : s.tgrp[p / U - na];
-                j = jf + (int64_t)(gid >> 9) * B + (p % U) * kStreamThreads + (gid & 511u);
-                if (j < r.NV) qv = load_col_vec(rv, j, cb, ce);
-            }
-            uint32_t mask = 0;
+        for (int p0 = 0; p0 < nv; p0 += 4 * TM::kFinThreads) {
+            uint4 qv[4];
+            int64_t jv[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint32_t key = order_key(half_of(qv, e));
-                mask |= (key != 0 && key >= T) ? 1u << e : 0u;
+            for (int h = 0; h < 4; ++h) {
+                const int p = p0 + h * TM::kFinThreads + ft;
+                qv[h] = make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
+                jv[h] = 0;
+                if (p < nv) {
+                    const uint32_t gid = p / U < na ? s.grp[p / U] : s.tgrp[p / U - na];
+                    jv[h] = jf + (int64_t)(gid >> 9) * B + (p % U) * TM::kStreamThreads + (gid & 511u);
+                    if (jv[h] < r.NV) qv[h] = load_col_vec(rv, jv[h], cb, ce);
+                }
             }
-            int total;
-            const int excl = warp_exclusive_sum(__popc(mask), lane, total);
-            if (total == 0) continue;
-            uint32_t pos = 0;
-            if (lane == 0) pos = atomicAdd(&s.ncand, (uint32_t)total);
-            pos = __shfl_sync(kFull, pos, 0) + (uint32_t)excl;
-            for (uint32_t m = mask; m; m &= m - 1, ++pos) {
-                const int e = __ffs(m) - 1;
-                const uint32_t raw = half_of(qv, e);
-                uint32_t id = (uint32_t)(8 * j - r.mis - cb + e);
-                if (r.id_map) id = (uint32_t)__ldg(r.id_map + id);
-                if (pos < (uint32_t)kCap) s.cand[pos] = make_entry(order_key(raw), id, raw);
+#pragma unroll 1
+            for (int h = 0; h < 4; ++h) {
+                if (p0 + h * TM::kFinThreads + 32 * w >= nv) break;   // this warp has no vector in the pass
+                const uint4 q = h == 0 ? qv[0] : h == 1 ? qv[1] : h == 2 ? qv[2] : qv[3];
+                const int64_t j = h == 0 ? jv[0] : h == 1 ? jv[1] : h == 2 ? jv[2] : jv[3];
+                uint32_t mask = 0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t key = order_key(half_of(q, e));
+                    mask |= (key != 0 && key >= T) ? 1u << e : 0u;
+                }
+                int total;
+                const int excl = warp_exclusive_sum(__popc(mask), lane, total);
+                if (total == 0) continue;
+                uint32_t pos = 0;
+                if (lane == 0) pos = atomicAdd(&s.ncand, (uint32_t)total);
+                pos = __shfl_sync(kFull, pos, 0) + (uint32_t)excl;
+                for (uint32_t m = mask; m; m &= m - 1, ++pos) {
+                    const int e = __ffs(m) - 1;
+                    const uint32_t raw = half_of(q, e);
+                    uint32_t id = (uint32_t)(8 * j - r.mis - cb + e);
+                    if (r.id_map) id = (uint32_t)__ldg(r.id_map + id);
+                    if (pos < (uint32_t)kCap) s.cand[pos] = make_entry(order_key(raw), id, raw);
+                }
             }
         }
     }
@@ -1009,7 +1045,7 @@ __device__ __forceinline__ void team_finish(const RoundArgs &a, const GmRun &r, 
     } else if (n > kRankMax) {
         select_many<NW, BAR>(n, kk, s, lane, w);
     } else {
-        for (int i = ft; i < n; i += kFinThreads) {
+        for (int i = ft; i < n; i += TM::kFinThreads) {
             const unsigned long long e = s.cand[i];
             int rank = 0;
             for (int jj = 0; jj < n; ++jj) rank += s.cand[jj] > e ? 1 : 0;
@@ -1018,7 +1054,7 @@ __device__ __forceinline__ void team_finish(const RoundArgs &a, const GmRun &r, 
     }
     team_sync<NW, BAR>();
     if (r.draft) {
-        for (int i = ft; i < kk; i += kFinThreads) {
+        for (int i = ft; i < kk; i += TM::kFinThreads) {
             const unsigned long long e = s.wl[0][i];
             a.out_vals[c * kk + i] = entry_raw(e);
             a.out_ids[c * kk + i] = (int32_t)entry_id(e);
@@ -1039,23 +1075,25 @@ __device__ __forceinline__ void team_finish(const RoundArgs &a, const GmRun &r, 
 
 // The finishing warps' part: every column of [c0, c1), one column behind
 // the streamers.
-template <int U>
+template <int U, int SW>
 __device__ __forceinline__ void team_finish_all(const RoundArgs &a, const GmRun &r, int64_t c0, int64_t c1, Smem &s)
 {
-    if (threadIdx.x == kStreamThreads) {
+    using TM = Team<SW>;
+    if (threadIdx.x == TM::kStreamThreads) {
         s.ncand = 0u;
         s.ngrp = 0u;
     }
-    team_sync<kFinWarps, kBarTeam>();
+    team_sync<TM::kFinWarps, kBarTeam>();
     for (int64_t c = c0; c < c1; ++c) {
         const int n = (int)(c - c0), b = n & 1;
         bar_sync_id(kBarFull + b, kThreads);   // buffer b holds column c's keys
-        team_finish<U>(a, r, c, b, s);
+        team_finish<U, SW>(a, r, c, b, s);
         if (c + 2 < c1) bar_arrive_id(kBarFree + b, kThreads);   // the streamers may fill buffer b again
     }
 }
 
-// MODE 0: slice mode; 1: column mode; 2: column mode with finishing warps.
+// MODE 0: slice mode; 1: column mode; 2 and 3: column mode with finishing
+// warps, 12 (2) or 8 (3) of the 16 streaming.
 template <int U, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_constant__ RoundArgs a)
 {
@@ -1077,11 +1115,12 @@ __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_co
         stream_columns<U>(a, r, bi, s);
         return;
     }
-    if constexpr (MODE == 2) {
+    if constexpr (MODE == 2 || MODE == 3) {
+        constexpr int SW = MODE == 2 ? 12 : 8;
         const int64_t cols = r.N / r.V;
         const int64_t c0 = bi * cols / r.W, c1 = (bi + 1) * cols / r.W;
-        if (threadIdx.x < kStreamThreads) team_stream<U>(r, c0, c1, s);
-        else team_finish_all<U>(a, r, c0, c1, s);
+        if (threadIdx.x < Team<SW>::kStreamThreads) team_stream<U, SW>(r, c0, c1, s);
+        else team_finish_all<U, SW>(a, r, c0, c1, s);
         return;
     }
     const int64_t g0b = slice_lo(r, bi), g1b = slice_lo(r, bi + 1);

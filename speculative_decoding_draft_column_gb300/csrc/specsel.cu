@@ -125,7 +125,8 @@ spec_status device_state(DeviceState **out)
                                                           cta::kSmemBytes);
         if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
         if (d.occ_c < 1) d.occ_c = 1;
-        void *kg[6] = {reinterpret_cast<void *>(gm::spec_round_kernel<1, 0>),
+        void *kg[7] = {reinterpret_cast<void *>(gm::spec_round_kernel<8, 3>),
+                       reinterpret_cast<void *>(gm::spec_round_kernel<1, 0>),
                        reinterpret_cast<void *>(gm::spec_round_kernel<2, 0>),
                        reinterpret_cast<void *>(gm::spec_round_kernel<4, 0>),
                        reinterpret_cast<void *>(gm::spec_round_kernel<8, 0>),
@@ -282,11 +283,16 @@ bool plan_gm(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, int
     int64_t vmax = 0;
     if (nv_d > 0) vmax = a.d_V > vmax ? a.d_V : vmax;
     if (nv_t > 0) vmax = a.t_V > vmax ? a.t_V : vmax;
-    // With at least 1.5 columns per SM and columns of at most kTeamRows
-    // batches of 384 x 8 vectors, finishing warps take the columns' finish
-    // off the stream.
-    const bool team = 2 * cols_all >= 3 * (int64_t)d.sms &&
-                      (vmax / 8 + 2) <= (int64_t)gm::kTeamRows * gm::kStreamThreads * 8;
+    // With at least 1.5 columns per SM, finishing warps take the columns'
+    // finish off the stream: 4 of the 16 warps, or 8 where a column's finish
+    // outweighs its stream (k above 8 on columns of at most 192 K logits:
+    // GB300, C5s at k = 20 / 64: 196 / 288 us with 4, 177 / 197 with 8; C4
+    // and C5 at k = 8 faster with 4).  Columns must fit kTeamRows batches.
+    const int kmax = a.k > a.t_k ? a.k : a.t_k;
+    const bool eight = kmax > 8 && vmax <= 192 * 1024 &&
+                       (vmax / 8 + 2) <= (int64_t)gm::Team<8>::kTeamRows * gm::Team<8>::kStreamThreads * 8;
+    const bool four = (vmax / 8 + 2) <= (int64_t)gm::Team<12>::kTeamRows * gm::Team<12>::kStreamThreads * 8;
+    const bool team = 2 * cols_all >= 3 * (int64_t)d.sms && (eight || four);
     if (4 * cols_all >= 3 * (int64_t)d.sms && vmin >= 8 * 512 * 8 && (vmax / 8 + 2) <= (int64_t)gm::kKeyRows * 512 * 8) {
         const int64_t W = cols_all < d.sms ? cols_all : d.sms;
         int64_t ud = 0, ut = 0;
@@ -305,7 +311,7 @@ bool plan_gm(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, int
         a.t_units = (int32_t)ut;
         p.gm = true;
         p.gm_u = 8;
-        p.gm_mode = team ? 2 : 1;
+        p.gm_mode = !team ? 1 : eight ? 3 : 2;
         p.grid = ud + ut;
         p.partials = 0;
         return true;
@@ -414,6 +420,7 @@ cudaError_t launch_plan(const Plan &p, const RoundArgs &a, cudaStream_t stream, 
     const unsigned g = (unsigned)p.grid;
     if (p.gm) {
         const size_t m = gm::kSmemBytes;
+        if (p.gm_mode == 3) return launch_pdl(gm::spec_round_kernel<8, 3>, g, gm::kThreads, m, stream, a, pdl);
         if (p.gm_mode == 2) return launch_pdl(gm::spec_round_kernel<8, 2>, g, gm::kThreads, m, stream, a, pdl);
         if (p.gm_mode == 1) return launch_pdl(gm::spec_round_kernel<8, 1>, g, gm::kThreads, m, stream, a, pdl);
         switch (p.gm_u) {
