@@ -404,6 +404,22 @@ def test_sampled_decisions_near_boundaries(delta):
                            (wa, wc), f"sampled near boundaries delta={delta}")
 
 
+@pytest.mark.parametrize("V", [248_046, 131_072])
+def test_sampled_verify_many_columns(V):
+    """Sampled verify over 40 lanes x 8 target columns: enough columns for
+    the group-maxima kernel's finishing warps (12 + 4 warps at the full
+    vocabulary; 8 + 8 for top_k 20 on shortlist-length columns)."""
+    lanes, gamma = 40, 7
+    t = synth._draft_block(990 + V % 97, lanes * (gamma + 1), V, 3.0)
+    _, top = oracle.topk(t, 1)   # drafts: each position's most likely token, so some are accepted
+    drafts = np.ascontiguousarray(top[:, 0].reshape(lanes, gamma + 1)[:, :gamma], dtype=np.int32)
+    u = synth.rng(992, 0).random((lanes, gamma + 1, 2))
+    wa, wc, margin = oracle.sampled_verify(t, drafts, 1.0, 0.95, 20, u)
+    assert margin > 1e-9
+    gu.assert_verify_equal(gu.run_verify_sampled(t.reshape(lanes, gamma + 1, V), drafts, 1.0, 0.95, 20, u),
+                           (wa, wc), f"sampled many columns V={V}")
+
+
 def test_round_sampled_is_topk_plus_sampled_verify():
     import torch
     sd = gu.sd_module()
