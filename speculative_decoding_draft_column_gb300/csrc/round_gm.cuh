@@ -368,13 +368,14 @@ __device__ __noinline__ void select_many(int n, int kk, Smem &s, int lane, int w
     merge_lists<NW, BAR>(s, kk, lane, w);
 }
 
-// Exact top-kk of column [cb, ce) among its elements >= T, for any input
-// (the path for massive ties): every warp scans a share of the column's
-// vectors into its own sorted list, keeping only entries above the list's
-// kk-th; the lists are then merged into s.wl[0].  Every thread of the team
-// (NW warps) must call it.
+// Exact top-kk of the elements [cb, ce) of a column (its ids counted from
+// element idb) among those >= T, for any input (the path for massive ties):
+// every warp scans a share of the range's vectors into its own sorted list,
+// keeping only entries above the list's kk-th; the lists are then merged
+// into s.wl[0].  Every thread of the team (NW warps) must call it.
 template <int NW, int BAR>
-__device__ __noinline__ void exact_scan(const RunView r, int64_t cb, int64_t ce, uint32_t T, Smem &s, int lane, int w)
+__device__ __noinline__ void exact_scan(const RunView r, int64_t cb, int64_t ce, int64_t idb, uint32_t T, Smem &s,
+                                        int lane, int w)
 {
     const int kk = r.kk;
     unsigned long long *wl = s.wl[w];
@@ -391,7 +392,7 @@ __device__ __noinline__ void exact_scan(const RunView r, int64_t cb, int64_t ce,
             const uint32_t key = order_key(raw);
             unsigned long long cand = 0ull;
             if (key != 0 && key >= T && key >= entry_key(thr)) {
-                uint32_t id = (uint32_t)(g0 + e - cb);
+                uint32_t id = (uint32_t)(g0 + e - idb);
                 if (r.id_map) id = (uint32_t)__ldg(r.id_map + id);
                 cand = make_entry(key, id, raw);
                 if (cand < thr) cand = 0ull;
@@ -670,7 +671,7 @@ __device__ __forceinline__ void rank_emit(const RoundArgs &a, const GmRun &r, in
     __syncthreads();
     const int n = (int)s.ncand;
     if (sel.lost || n > kCap) {
-        exact_scan<kWarps, 0>(rv, cb, ce, T, s, lane, w);
+        exact_scan<kWarps, 0>(rv, cb, ce, cb, T, s, lane, w);
     } else if (n > kRankMax) {
         select_many<kWarps, 0>(n, kk, s, lane, w);
     } else {
@@ -1041,7 +1042,7 @@ __device__ __forceinline__ void team_finish(const RoundArgs &a, const GmRun &r, 
     // 5. the kk best, in order
     const int n = (int)s.ncand;
     if (lost || n > kCap) {
-        exact_scan<NW, BAR>(rv, cb, ce, T, s, lane, w);
+        exact_scan<NW, BAR>(rv, cb, ce, cb, T, s, lane, w);
     } else if (n > kRankMax) {
         select_many<NW, BAR>(n, kk, s, lane, w);
     } else {
@@ -1092,12 +1093,267 @@ __device__ __forceinline__ void team_finish_all(const RoundArgs &a, const GmRun 
     }
 }
 
+// ---- one pass: every CTA's slice in its registers ---------------------------
+//
+// Rounds small enough for each CTA's slice to fit in its registers at once
+// (at most 512 L vectors, L loads per thread).  The CTAs of a run are dealt
+// out to its columns, as evenly as they go (each column at least one), and
+// a column's CTAs split its vectors evenly: CTA b of W works on column
+// floor(b cols / W).  A CTA loads its slice, then selects the top-kk of it
+// by itself: the bound over its own section (or thread) maxima, its
+// elements that reach it, ranked.  No group key goes to global memory and
+// nothing is read twice.  A column with one CTA is finished right there;
+// otherwise every CTA publishes its sorted list and the one that takes the
+// column's ticket last merges them.
+
+constexpr int kVecCap = (int)(sizeof(Smem::keys) / sizeof(uint4));   // vectors staged in s.keys
+static_assert(kVecCap <= kGroupCap, "their positions go to s.grp");
+
+// q (elements [g0, g0 + 8), counted like lo and hi) with its elements
+// outside [lo, hi) masked
+__device__ __forceinline__ uint4 mask_vec(const uint4 &q, int g0, int lo, int hi)
+{
+    const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const int p = g0 + 2 * h;
+        const bool in0 = p >= lo && p < hi, in1 = p + 1 >= lo && p + 1 < hi;
+        o[h] = (in0 ? (wd[h] & 0xFFFFu) : 0x7FFFu) | (in1 ? (wd[h] & 0xFFFF0000u) : 0x7FFF0000u);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// The sorted top-kk of the part [lo, hi) of the column starting at element
+// cb, from this CTA's slice (vectors j0 + u 512 + t in q[u]), into s.wl[0];
+// returns its length, min(kk, the part's elements).  Every thread calls it.
+// Positions inside the slice are counted from its vector j0's first
+// element, e0 = 8 j0 - mis, in 32 bits.
+template <int L>
+__device__ __forceinline__ int pass_list(const GmRun &r, const uint4 (&q)[L], int64_t j0, int64_t cb, int64_t lo,
+                                         int64_t hi, Smem &s)
+{
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int kk = r.kk;
+    const int64_t e0 = 8 * j0 - r.mis;
+    const int lr = (int)(lo - e0), hr = (int)(hi - e0);   // the part, from e0
+    const int idb = (int)(e0 - cb);                        // id of position 0
+    // 1. this thread's maximum over the part
+    uint32_t m2 = kNaN2;
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        const int g0 = 8 * (u * 512 + t);
+        if (g0 >= lr && g0 + 8 <= hr) m2 = bmax2(m2, vmax(q[u]));
+        else if (g0 + 8 > lr && g0 < hr) m2 = bmax2(m2, vmax(mask_vec(q[u], g0, lr, hr)));
+    }
+    const uint32_t mt = key_of(m2);
+    // 2. the bound T: the kk-th largest section maximum (kk <= 8) or thread
+    //    maximum (larger kk, or a part in fewer than kk sections); 0 when
+    //    fewer than kk threads hold an element of the part -- then every
+    //    element is a candidate, and there are fewer than 8 kk
+    uint32_t m8 = mt;
+#pragma unroll
+    for (int d = 1; d < 8; d <<= 1) {
+        const uint32_t o = __shfl_xor_sync(kFull, m8, d);
+        m8 = o > m8 ? o : m8;
+    }
+    if ((lane & 7) == 0) s.sec[4 * w + (lane >> 3)] = m8;
+    s.smax[t] = mt;
+    __syncthreads();
+    uint32_t T = kk <= 8 ? kth_of_64(s.sec[lane], s.sec[lane + 32], kk) : 0u;
+    if (T == 0u) T = kth_of_smem(s.smax, kThreads, kk, lane);
+    // 3. the vectors whose maximum reaches T (elements outside the part
+    //    masked) to shared memory, from the warps holding one; then their
+    //    elements >= T, one per thread, to the candidates
+    uint4 *vq = reinterpret_cast<uint4 *>(&s.keys[0][0]);
+    if (__any_sync(kFull, mt != 0 && mt >= T)) {
+        const bool mine = mt != 0 && mt >= T;
+#pragma unroll
+        for (int u = 0; u < L; ++u) {
+            const int g0 = 8 * (u * 512 + t);
+            const bool full = g0 >= lr && g0 + 8 <= hr;
+            const uint4 v = full ? q[u] : mask_vec(q[u], g0, lr, hr);
+            const bool take = mine && (full || (g0 + 8 > lr && g0 < hr)) && key_of(vmax(v)) >= T;
+            const uint32_t bal = __ballot_sync(kFull, take);
+            if (bal) {
+                uint32_t base = 0;
+                if (lane == 0) base = atomicAdd(&s.ngrp, (uint32_t)__popc(bal));
+                base = __shfl_sync(kFull, base, 0);
+                const uint32_t pos = base + (uint32_t)__popc(bal & lanemask_lt());
+                if (take && pos < (uint32_t)kVecCap) {
+                    vq[pos] = v;
+                    s.grp[pos] = (uint32_t)g0;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    const int nvec = (int)s.ngrp;
+    if (nvec <= kVecCap)
+        for (int i0 = 0; i0 < 8 * nvec; i0 += kThreads) {
+            const int i = i0 + t;
+            unsigned long long ent = 0ull;
+            if (i < 8 * nvec) {
+                const uint32_t raw = half_of(vq[i >> 3], i & 7);
+                const uint32_t key = order_key(raw);
+                if (key != 0 && key >= T) {   // masked elements: key 0
+                    uint32_t id = (uint32_t)((int)s.grp[i >> 3] + (i & 7) + idb);
+                    if (r.id_map) id = (uint32_t)__ldg(r.id_map + id);
+                    ent = make_entry(key, id, raw);
+                }
+            }
+            const uint32_t bal = __ballot_sync(kFull, ent != 0ull);
+            if (bal) {
+                uint32_t base = 0;
+                if (lane == 0) base = atomicAdd(&s.ncand, (uint32_t)__popc(bal));
+                base = __shfl_sync(kFull, base, 0);
+                const uint32_t pos = base + (uint32_t)__popc(bal & lanemask_lt());
+                if (ent != 0ull && pos < (uint32_t)kCap) s.cand[pos] = ent;
+            }
+        }
+    __syncthreads();
+    // 4. ranked (value desc, id asc); many: sorted lists per warp; more than
+    //    the buffers hold (massive ties): the part scanned exactly
+    const int n = nvec > kVecCap ? kCap + 1 : (int)s.ncand;
+    if (n > kCap) {
+        exact_scan<kWarps, 0>(view_of(r), lo, hi, cb, T, s, lane, w);
+    } else if (n > kRankMax) {
+        select_many<kWarps, 0>(n, kk, s, lane, w);
+    } else {
+        for (int i = t; i < n; i += kThreads) {
+            const unsigned long long e = s.cand[i];
+            int rank = 0;
+            for (int j = 0; j < n; ++j) rank += s.cand[j] > e ? 1 : 0;
+            if (rank < kk) s.wl[0][rank] = e;
+        }
+    }
+    __syncthreads();
+    if (t == 0) {
+        s.ncand = 0u;
+        s.ngrp = 0u;
+    }
+    return n < kk ? n : kk;
+}
+
+// Column c's list, s.wl[0][0 .. kk), to its outputs (draft) or to verify
+// (target; draft_tok: thread 0's copy of the column's draft token, -2 for
+// the bonus position).  Every thread calls it.
+__device__ __forceinline__ void pass_emit(const RoundArgs &a, const GmRun &r, int64_t c, int32_t draft_tok, Smem &s)
+{
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int kk = r.kk;
+    if (r.draft) {
+        for (int i = t; i < kk; i += kThreads) {
+            const unsigned long long e = s.wl[0][i];
+            a.out_vals[c * kk + i] = entry_raw(e);
+            a.out_ids[c * kk + i] = (int32_t)entry_id(e);
+        }
+    } else if (w == 0) {
+        int32_t token = (int32_t)entry_id(s.wl[0][0]);
+        bool accepted;
+        if (a.uniforms) accepted = sampled_decide(a, c, s.wl[0], kk, lane, token);
+        else accepted = __shfl_sync(kFull, draft_tok, 0) == token;
+        lane_done(a, c, token, accepted, lane);
+    }
+}
+
+// The CTA that came last to column c (its nc CTAs: units u0, u0 + 1, ...):
+// every CTA's published list (kk entries, 0 for none), merged, then
+// emitted; the ticket cleared for the next launch.  At most kCap entries.
+__device__ __forceinline__ void pass_merge(const RoundArgs &a, const GmRun &r, int64_t c, int64_t u0, int nc,
+                                           int32_t draft_tok, Smem &s)
+{
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int kk = r.kk;
+    const int n_all = nc * kk;
+    for (int i0 = 0; i0 < n_all; i0 += kThreads) {
+        const int i = i0 + t;
+        const unsigned long long e =
+            i < n_all ? __ldcg(a.partials + (u0 + i / kk) * a.pstride + i % kk) : 0ull;
+        const uint32_t bal = __ballot_sync(kFull, e != 0ull);
+        if (bal) {
+            uint32_t base = 0;
+            if (lane == 0) base = atomicAdd(&s.ncand, (uint32_t)__popc(bal));
+            base = __shfl_sync(kFull, base, 0);
+            const uint32_t pos = base + (uint32_t)__popc(bal & lanemask_lt());
+            if (e != 0ull && pos < (uint32_t)kCap) s.cand[pos] = e;
+        }
+    }
+    __syncthreads();
+    const int n = (int)s.ncand < kCap ? (int)s.ncand : kCap;
+    if (n > kRankMax) {
+        select_many<kWarps, 0>(n, kk, s, lane, w);
+    } else {
+        for (int i = t; i < n; i += kThreads) {
+            const unsigned long long e = s.cand[i];
+            int rank = 0;
+            for (int j = 0; j < n; ++j) rank += s.cand[j] > e ? 1 : 0;
+            if (rank < kk) s.wl[0][rank] = e;
+        }
+    }
+    __syncthreads();
+    if (t == 0) r.ticket[c] = 0u;   // ready for the next launch
+    pass_emit(a, r, c, draft_tok, s);
+}
+
+// One-pass mode, all of it, for CTA bi of run r.
+template <int L>
+__device__ __forceinline__ void one_pass(const RoundArgs &a, const GmRun &r, int bi, Smem &s)
+{
+    const int t = threadIdx.x;
+    const int64_t cols = r.N / r.V;
+    const int64_t c = (int64_t)bi * cols / r.W;                        // this CTA's column
+    const int64_t f = (c * r.W + cols - 1) / cols;                     // its first CTA
+    const int nc = (int)(((c + 1) * r.W + cols - 1) / cols - f);       // and how many
+    const int64_t cb = c * r.V, ce = cb + r.V;
+    const int64_t jf = (cb + r.mis) >> 3, nvc = ((ce - 1 + r.mis) >> 3) - jf + 1;
+    const int64_t j0 = jf + (bi - f) * nvc / nc, j1 = jf + (bi - f + 1) * nvc / nc;
+    // Plain (L2-cached) loads, not read-only ones: a read-only load may be
+    // issued again at a later use instead of being kept in registers.
+    uint4 q[L];
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        const int64_t j = j0 + u * 512 + t;
+        q[u] = (j < j1 && j >= r.jlo && j < r.jhi) ? __ldcg(r.vb + j) : make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
+    }
+    if (j0 < r.jlo || j1 > r.jhi) {
+        // the buffer's edge vectors (at most one at each end), element by element
+#pragma unroll
+        for (int u = 0; u < L; ++u) {
+            const int64_t j = j0 + u * 512 + t;
+            if (j < j1 && (j < r.jlo || j >= r.jhi)) q[u] = load_edge(r.buf, j, r.mis, 0, r.N);
+        }
+    }
+    // a target column's draft token (thread 0), early
+    int32_t dtok = -2;
+    if (!r.draft && t == 0) {
+        const int gp1 = a.gamma + 1;
+        const int64_t ln = c / gp1;
+        const int j = (int)(c - ln * gp1);
+        if (j < a.gamma) dtok = __ldg(a.drafts + ln * a.gamma + j);
+    }
+    const int64_t e0 = 8 * j0 - r.mis, e1 = 8 * j1 - r.mis;
+    const int len = pass_list<L>(r, q, j0, cb, e0 > cb ? e0 : cb, e1 < ce ? e1 : ce, s);
+    if (nc == 1) {
+        pass_emit(a, r, c, dtok, s);
+        return;
+    }
+    const int64_t unit0 = r.draft ? 0 : a.d_units;
+    unsigned long long *slot = a.partials + (unit0 + bi) * a.pstride;
+    if (t < r.kk) __stcg(slot + t, t < len ? s.wl[0][t] : 0ull);
+    __syncthreads();   // the list is written
+    if (t == 0) s.last[0] = arrive_at_end(r.ticket + c, (uint32_t)(nc - 1));
+    __syncthreads();
+    if (s.last[0] != 0u) pass_merge(a, r, c, unit0 + f, nc, dtok, s);
+}
+
 // MODE 0: slice mode; 1: column mode; 2 and 3: column mode with finishing
-// warps, 12 (2) or 8 (3) of the 16 streaming.
+// warps, 12 (2) or 8 (3) of the 16 streaming; 4: one pass, U loads per
+// thread.
 template <int U, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_constant__ RoundArgs a)
 {
-    constexpr int P = kLoads / U;
+    constexpr int P = MODE == 0 ? kLoads / U : 1;
     pdl_launch_dependents();
     pdl_wait();
     extern __shared__ __align__(16) unsigned char smem[];
@@ -1111,6 +1367,10 @@ __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_co
         s.ncand = 0u;
         s.ngrp = 0u;
     }
+    if constexpr (MODE == 4) {
+        one_pass<U>(a, r, bi, s);
+        return;
+    }
     if constexpr (MODE == 1) {
         stream_columns<U>(a, r, bi, s);
         return;
@@ -1123,55 +1383,57 @@ __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_co
         else team_finish_all<U, SW>(a, r, c0, c1, s);
         return;
     }
-    const int64_t g0b = slice_lo(r, bi), g1b = slice_lo(r, bi + 1);
-    if (g1b <= g0b) return;
-    int64_t cn = elem_lo<U>(r, g0b) / r.V + 1;   // the column after the one in progress
-    int64_t cut = cn * r.V;                      // its first element
-    const int64_t cl = (elem_hi<U>(r, g1b - 1) - 1) / r.V;
-    int64_t cdone = cn - 1;      // the first column not yet handled
-    int64_t pend = -1;           // a shared column whose ticket this CTA took inside the stream
-    uint32_t pend_old = 0;       // (thread 0) that ticket's count before it
-    int64_t gb = g0b;
-    for (;;) {
-        if (gb < g1b) {
-            stream_step<U>(r, gb, g1b, cn, cut);
-            gb += P;
-        }
-        const bool ending = gb >= g1b;
-        const int64_t upto = ending ? cl + 1 : cn - 1;   // columns below it are complete here
-        while (cdone < upto || (ending && pend >= 0)) {
-            int64_t c, wf, wl;
-            bool fin;
-            if (cdone < upto) {
-                c = cdone++;
-                column_owners<U>(r, c, wf, wl);
-                fin = wf == wl;   // the column lies in this slice: finish it now
-                if (!fin) {
-                    __syncthreads();   // this CTA's keys of the column are written
-                    if (!ending) {
-                        // its part here ends inside the slice (the slice's first
-                        // column): take the ticket now, read it at the end
-                        if (threadIdx.x == 0) pend_old = atom_add_acq_rel(r.ticket + c, 1u);
-                        pend = c;
-                    } else {
-                        if (threadIdx.x == 0) s.last[0] = arrive_at_end(r.ticket + c, (uint32_t)(wl - wf));
-                        __syncthreads();
-                        fin = s.last[0] != 0u;
-                    }
-                }
-            } else {
-                c = pend;
-                pend = -1;
-                column_owners<U>(r, c, wf, wl);
-                __syncthreads();
-                if (threadIdx.x == 0) s.last[0] = pend_old == (uint32_t)(wl - wf) ? 1u : 0u;
-                __syncthreads();
-                fin = s.last[0] != 0u;
+    if constexpr (MODE == 0) {
+        const int64_t g0b = slice_lo(r, bi), g1b = slice_lo(r, bi + 1);
+        if (g1b <= g0b) return;
+        int64_t cn = elem_lo<U>(r, g0b) / r.V + 1;   // the column after the one in progress
+        int64_t cut = cn * r.V;                      // its first element
+        const int64_t cl = (elem_hi<U>(r, g1b - 1) - 1) / r.V;
+        int64_t cdone = cn - 1;      // the first column not yet handled
+        int64_t pend = -1;           // a shared column whose ticket this CTA took inside the stream
+        uint32_t pend_old = 0;       // (thread 0) that ticket's count before it
+        int64_t gb = g0b;
+        for (;;) {
+            if (gb < g1b) {
+                stream_step<U>(r, gb, g1b, cn, cut);
+                gb += P;
             }
-            if (fin) finish_column<U, false>(a, r, c, wf != wl, s);
-            __syncthreads();   // s.last is read by every thread before it is written again
+            const bool ending = gb >= g1b;
+            const int64_t upto = ending ? cl + 1 : cn - 1;   // columns below it are complete here
+            while (cdone < upto || (ending && pend >= 0)) {
+                int64_t c, wf, wl;
+                bool fin;
+                if (cdone < upto) {
+                    c = cdone++;
+                    column_owners<U>(r, c, wf, wl);
+                    fin = wf == wl;   // the column lies in this slice: finish it now
+                    if (!fin) {
+                        __syncthreads();   // this CTA's keys of the column are written
+                        if (!ending) {
+                            // its part here ends inside the slice (the slice's first
+                            // column): take the ticket now, read it at the end
+                            if (threadIdx.x == 0) pend_old = atom_add_acq_rel(r.ticket + c, 1u);
+                            pend = c;
+                        } else {
+                            if (threadIdx.x == 0) s.last[0] = arrive_at_end(r.ticket + c, (uint32_t)(wl - wf));
+                            __syncthreads();
+                            fin = s.last[0] != 0u;
+                        }
+                    }
+                } else {
+                    c = pend;
+                    pend = -1;
+                    column_owners<U>(r, c, wf, wl);
+                    __syncthreads();
+                    if (threadIdx.x == 0) s.last[0] = pend_old == (uint32_t)(wl - wf) ? 1u : 0u;
+                    __syncthreads();
+                    fin = s.last[0] != 0u;
+                }
+                if (fin) finish_column<U, false>(a, r, c, wf != wl, s);
+                __syncthreads();   // s.last is read by every thread before it is written again
+            }
+            if (ending) break;
         }
-        if (ending) break;
     }
 }
 

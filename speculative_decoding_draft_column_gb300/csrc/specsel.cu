@@ -125,7 +125,9 @@ spec_status device_state(DeviceState **out)
                                                           cta::kSmemBytes);
         if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
         if (d.occ_c < 1) d.occ_c = 1;
-        void *kg[7] = {reinterpret_cast<void *>(gm::spec_round_kernel<8, 3>),
+        void *kg[9] = {reinterpret_cast<void *>(gm::spec_round_kernel<8, 3>),
+                       reinterpret_cast<void *>(gm::spec_round_kernel<8, 4>),
+                       reinterpret_cast<void *>(gm::spec_round_kernel<16, 4>),
                        reinterpret_cast<void *>(gm::spec_round_kernel<1, 0>),
                        reinterpret_cast<void *>(gm::spec_round_kernel<2, 0>),
                        reinterpret_cast<void *>(gm::spec_round_kernel<4, 0>),
@@ -254,8 +256,9 @@ void split_units(int64_t nv_d, int64_t nv_t, int64_t max_units, int64_t min_slic
 struct Plan {
     bool per_cta;
     bool gm;          // the group-maxima kernel
-    int gm_u;         // its batch width: 16-byte vectors per thread per batch (1, 2, 4 or 8)
-    int gm_mode;      // its mode: 0 slices, 1 whole columns per CTA, 2 whole columns with finishing warps
+    int gm_u;         // its batch width: 16-byte vectors per thread per batch (1, 2, 4 or 8; one pass: 8 or 16)
+    int gm_mode;      // its mode: 0 slices, 1 whole columns per CTA, 2 / 3 whole columns with finishing warps,
+                      // 4 one pass (gm_u: loads per thread)
     int slots;        // per-warp kernel: 2 for k > 32 (finer seed groups)
     bool mapped;
     int64_t grid;     // CTAs
@@ -274,6 +277,33 @@ bool plan_gm(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, int
     int64_t vmin = INT64_MAX;
     if (nv_d > 0) vmin = a.d_V < vmin ? a.d_V : vmin;
     if (nv_t > 0) vmin = a.t_V < vmin ? a.t_V : vmin;
+    // One pass: the CTAs of each run dealt out to its columns (every column
+    // at least one, every CTA at least one vector), every CTA's slice at
+    // most 512 L vectors (L = 8 loads per thread, else 16) so that it holds
+    // the slice in registers, and a column's lists fitting the merge buffer.
+    for (int L : {8, 16}) {
+        int32_t wd = 0, wt = 0;
+        split_units(nv_d, nv_t, d.sms, 512, a.pstride, max_partials, &wd, &wt);   // 8 KB a CTA at least
+        auto fits = [L](int64_t nv, int64_t cols, int64_t w, int64_t V, int kk) {
+            if (nv == 0) return true;
+            if (w < cols) return false;
+            const int64_t nmin = w / cols, nmax = (w + cols - 1) / cols;
+            const int64_t nvc = V / 8 + 2;   // a column's vectors, at most
+            return (nvc + nmin - 1) / nmin <= 512 * (int64_t)L && V / 8 >= nmax && nmax * kk <= (int64_t)gm::kCap;
+        };
+        const int64_t units = (nv_d > 0 ? wd : 0) + (nv_t > 0 ? wt : 0);
+        if (!fits(nv_d, a.d_cols, wd, a.d_V, a.k) || !fits(nv_t, a.t_cols, wt, a.t_V, a.t_k) ||
+            units * a.pstride > max_partials)
+            continue;
+        a.d_units = nv_d > 0 ? wd : 0;
+        a.t_units = nv_t > 0 ? wt : 0;
+        p.gm = true;
+        p.gm_u = L;
+        p.gm_mode = 4;
+        p.grid = units;
+        p.partials = units * a.pstride;
+        return true;
+    }
     if (vmin < gm::kMinV) return false;
     // Column mode: at least three quarters as many columns as SMs, every
     // column at least one batch of U = 8 and at most the kKeyRows batches
@@ -420,6 +450,9 @@ cudaError_t launch_plan(const Plan &p, const RoundArgs &a, cudaStream_t stream, 
     const unsigned g = (unsigned)p.grid;
     if (p.gm) {
         const size_t m = gm::kSmemBytes;
+        if (p.gm_mode == 4 && p.gm_u == 16)
+            return launch_pdl(gm::spec_round_kernel<16, 4>, g, gm::kThreads, m, stream, a, pdl);
+        if (p.gm_mode == 4) return launch_pdl(gm::spec_round_kernel<8, 4>, g, gm::kThreads, m, stream, a, pdl);
         if (p.gm_mode == 3) return launch_pdl(gm::spec_round_kernel<8, 3>, g, gm::kThreads, m, stream, a, pdl);
         if (p.gm_mode == 2) return launch_pdl(gm::spec_round_kernel<8, 2>, g, gm::kThreads, m, stream, a, pdl);
         if (p.gm_mode == 1) return launch_pdl(gm::spec_round_kernel<8, 1>, g, gm::kThreads, m, stream, a, pdl);
