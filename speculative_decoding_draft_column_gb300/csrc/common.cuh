@@ -117,6 +117,16 @@ __device__ __forceinline__ bool any_ge(uint32_t a, uint32_t t2)
     return r != 0;
 }
 
+// a / b for a >= 0, b > 0: the 32-bit divide when both fit in 32 bits (a
+// handful of instructions), the 64-bit routine (several times longer) only
+// otherwise.  The indices divided here (columns, lanes, CTAs, vectors of
+// rounds below 2^32 of them) nearly always fit.
+__device__ __forceinline__ int64_t udiv(int64_t a, int64_t b)
+{
+    if ((((uint64_t)a | (uint64_t)b) >> 32) == 0) return (int64_t)((uint32_t)a / (uint32_t)b);
+    return a / b;
+}
+
 __device__ __forceinline__ float bf16_as_float(uint32_t raw16) { return __uint_as_float(raw16 << 16); }
 
 // element e (0..7) of a 16-byte vector, widened exactly to float
@@ -407,8 +417,8 @@ struct Run {
     bool draft;
 };
 
-__device__ __forceinline__ int64_t slice_start(const Run &r, int64_t w) { return w * r.NV / r.W; }
-__device__ __forceinline__ int64_t owner(const Run &r, int64_t j) { return ((j + 1) * r.W - 1) / r.NV; }
+__device__ __forceinline__ int64_t slice_start(const Run &r, int64_t w) { return udiv(w * r.NV, r.W); }
+__device__ __forceinline__ int64_t owner(const Run &r, int64_t j) { return udiv((j + 1) * r.W - 1, r.NV); }
 __device__ __forceinline__ int64_t first_elem(const Run &r, int64_t w)
 {
     const int64_t g = 8 * slice_start(r, w) - r.mis;
@@ -419,7 +429,7 @@ __device__ __forceinline__ int64_t first_elem(const Run &r, int64_t w)
 // slice, else 1 (a slice holds part of at most two columns that it shares).
 __device__ __forceinline__ unsigned long long *list_slot(const RoundArgs &a, const Run &r, int64_t w, int64_t c)
 {
-    const int sl = (c == first_elem(r, w) / r.V) ? 0 : 1;
+    const int sl = (c == udiv(first_elem(r, w), r.V)) ? 0 : 1;
     return a.partials + ((int64_t)(r.gw0 + w) * 2 + sl) * a.pstride;
 }
 
@@ -433,7 +443,7 @@ __device__ __forceinline__ unsigned long long *list_slot(const RoundArgs &a, con
 __device__ __noinline__ void verify_column_done(const RoundArgs &a, int64_t c, int32_t arg, int lane)
 {
     const int gamma = a.gamma, gp1 = gamma + 1;
-    const int64_t ln = c / gp1;
+    const int64_t ln = udiv(c, gp1);
     const int j = (int)(c - ln * gp1);
     uint32_t word = 0;
     if (lane == 0) {
@@ -571,7 +581,7 @@ __device__ __noinline__ bool sampled_decide(const RoundArgs &a, int64_t c, const
                                             int lane, int32_t &token_out)
 {
     const int gamma = a.gamma, gp1 = gamma + 1;
-    const int64_t ln = c / gp1;
+    const int64_t ln = udiv(c, gp1);
     const int j = (int)(c - ln * gp1);
     const int32_t draft = j < gamma ? __ldg(a.drafts + ln * gamma + j) : -1;
     const double u = a.uniforms[(ln * gp1 + j) * 2], u2 = a.uniforms[(ln * gp1 + j) * 2 + 1];
@@ -649,7 +659,7 @@ __device__ __noinline__ void sampled_column_done(const RoundArgs &a, int64_t c, 
                                                  int lane)
 {
     const int gamma = a.gamma, gp1 = gamma + 1;
-    const int64_t ln = c / gp1;
+    const int64_t ln = udiv(c, gp1);
     const int j = (int)(c - ln * gp1);
     int32_t token;
     const bool accepted = sampled_decide(a, c, lst, n, lane, token);

@@ -414,7 +414,7 @@ __device__ __noinline__ void merge_slice(const RoundArgs &a, const Run &r, int64
                                          CtaSmem &s, int lane)
 {
     const int64_t nch = (J1 - J0 + kChunkVec - 1) / kChunkVec;
-    int64_t c = first_elem(r, bi) / r.V;
+    int64_t c = udiv(first_elem(r, bi), r.V);
     int sg = 0, n = 0;
     for (int64_t i = 0; i < nch; ++i) {
         const Chunk k = chunk_of(r, J0, J1, i);
@@ -531,7 +531,7 @@ __device__ __forceinline__ void stream_slice(const RoundArgs &a, const Run &r, i
 {
     const int64_t nch = (J1 - J0 + kChunkVec - 1) / kChunkVec;
     const int kk = r.kk;
-    int64_t c = first_elem(r, bi) / r.V;       // current column
+    int64_t c = udiv(first_elem(r, bi), r.V);       // current column
     int64_t seen = 0;                          // elements of column c this CTA has scanned
     uint32_t tprev = 0;                        // best seed of column c from an earlier chunk
     int sg = 0, nseed = 0;

@@ -77,6 +77,7 @@ struct GmRun {
     const uint16_t *buf;
     const uint4 *vb;
     int64_t V, N, NV, jlo, jhi, NB;
+    int64_t cols;            // N / V
     uint16_t *G;             // [NB][512]: group keys of each batch's first column
     uint16_t *H;             // [cols][512]: group keys of a column starting inside a batch, in that batch
     unsigned int *ticket;    // [cols]
@@ -102,6 +103,7 @@ __device__ __forceinline__ GmRun make_run(const RoundArgs &a, bool draft)
     r.buf = draft ? a.draft : a.target;
     r.V = draft ? a.d_V : a.t_V;
     const int64_t cols = draft ? a.d_cols : a.t_cols;
+    r.cols = cols;
     r.N = cols * r.V;
     r.W = draft ? a.d_units : a.t_units;
     r.kk = draft ? a.k : a.t_k;
@@ -137,8 +139,8 @@ __device__ __forceinline__ int64_t elem_hi(const GmRun &r, int64_t g)
 template <int U>
 __device__ __forceinline__ int64_t batch_of(const GmRun &r, int64_t e) { return ((e + r.mis) >> 3) / (512 * U); }
 
-__device__ __forceinline__ int64_t slice_lo(const GmRun &r, int64_t b) { return b * r.NB / r.W; }
-__device__ __forceinline__ int64_t owner_of(const GmRun &r, int64_t g) { return ((g + 1) * r.W - 1) / r.NB; }
+__device__ __forceinline__ int64_t slice_lo(const GmRun &r, int64_t b) { return udiv(b * r.NB, r.W); }
+__device__ __forceinline__ int64_t owner_of(const GmRun &r, int64_t g) { return udiv((g + 1) * r.W - 1, r.NB); }
 
 __device__ __forceinline__ uint32_t key_of(uint32_t m2) { return order_key(hmax_splat(m2) & 0xFFFFu); }
 
@@ -219,6 +221,7 @@ __device__ __forceinline__ uint32_t kth_of_64(uint32_t v0, uint32_t v1, int kk)
 {
     uint32_t lo = __reduce_min_sync(kFull, v0 < v1 ? v0 : v1);   // all 64 reach it
     uint32_t hi = __reduce_max_sync(kFull, v0 > v1 ? v0 : v1);
+    if (kk == 1) return hi;
     while (lo < hi) {
         const uint32_t mid = (lo + hi + 1) >> 1;
         const int n = __popc(__ballot_sync(kFull, v0 >= mid)) + __popc(__ballot_sync(kFull, v1 >= mid));
@@ -322,6 +325,31 @@ __device__ __forceinline__ uint32_t half_of(const uint4 &q, int e)
 __device__ __forceinline__ unsigned long long make_entry(uint32_t key, uint32_t id, uint32_t raw)
 {
     return ((unsigned long long)key << 48) | ((unsigned long long)(~id) << 16) | raw;
+}
+
+// Rank each of the n candidates in s.cand (n <= kRankMax, all distinct)
+// among them, value desc, id asc, and put those ranked below kk into
+// s.wl[0] in order.  Thread t of a team of nt threads; the candidates are
+// compared four at a time (two 16-byte shared loads, four independent
+// counts).
+__device__ __forceinline__ void rank_into_list(Smem &s, int n, int kk, int t, int nt)
+{
+    const ulonglong2 *c2 = reinterpret_cast<const ulonglong2 *>(s.cand);
+    for (int i = t; i < n; i += nt) {
+        const unsigned long long e = s.cand[i];
+        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+        int j = 0;
+        for (; j + 4 <= n; j += 4) {
+            const ulonglong2 a = c2[j >> 1], b = c2[(j >> 1) + 1];
+            r0 += a.x > e ? 1 : 0;
+            r1 += a.y > e ? 1 : 0;
+            r2 += b.x > e ? 1 : 0;
+            r3 += b.y > e ? 1 : 0;
+        }
+        for (; j < n; ++j) r0 += s.cand[j] > e ? 1 : 0;
+        const int rank = r0 + r1 + r2 + r3;
+        if (rank < kk) s.wl[0][rank] = e;
+    }
 }
 
 // A barrier of a team of NW warps: the CTA (id 0) or a named barrier.
@@ -429,7 +457,7 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const unsigned int *p)
 __device__ __forceinline__ void lane_done(const RoundArgs &a, int64_t c, int32_t token, bool accepted, int lane)
 {
     const int gamma = a.gamma, gp1 = gamma + 1;
-    const int64_t ln = c / gp1;
+    const int64_t ln = udiv(c, gp1);
     const int j = (int)(c - ln * gp1);
     unsigned int *slot = a.col_cert + a.d_cols + ln * gp1;
     uint32_t word = 0;
@@ -506,7 +534,7 @@ __device__ __forceinline__ Sel select_candidates(const RoundArgs &a, const GmRun
     int32_t draft_tok = -2;
     if (!r.draft && t == 0) {
         const int gp1 = a.gamma + 1;
-        const int64_t ln = c / gp1;
+        const int64_t ln = udiv(c, gp1);
         const int j = (int)(c - ln * gp1);
         if (j < a.gamma) draft_tok = __ldg(a.drafts + ln * a.gamma + j);
     }
@@ -675,12 +703,7 @@ __device__ __forceinline__ void rank_emit(const RoundArgs &a, const GmRun &r, in
     } else if (n > kRankMax) {
         select_many<kWarps, 0>(n, kk, s, lane, w);
     } else {
-        for (int i = t; i < n; i += kThreads) {
-            const unsigned long long e = s.cand[i];
-            int rank = 0;
-            for (int j = 0; j < n; ++j) rank += s.cand[j] > e ? 1 : 0;
-            if (rank < kk) s.wl[0][rank] = e;
-        }
+        rank_into_list(s, n, kk, t, kThreads);
     }
     __syncthreads();
     if (r.draft) {
@@ -753,8 +776,8 @@ __device__ __forceinline__ void stream_columns(const RoundArgs &a, const GmRun &
     constexpr int64_t B = 512 * U;
     static_assert(P == 1, "column mode: one batch per step");
     const int t = threadIdx.x;
-    const int64_t cols = r.N / r.V;
-    const int64_t c0 = bi * cols / r.W, c1 = (bi + 1) * cols / r.W;
+    const int64_t cols = r.cols;
+    const int64_t c0 = udiv(bi * cols, r.W), c1 = udiv((bi + 1) * cols, r.W);
     for (int64_t c = c0; c < c1; ++c) {
         const int64_t cb = c * r.V, ce = cb + r.V;
         const int64_t jf = (cb + r.mis) >> 3, jl = (ce - 1 + r.mis) >> 3;
@@ -919,7 +942,7 @@ __device__ __forceinline__ void team_finish(const RoundArgs &a, const GmRun &r, 
     int32_t draft_tok = -2;   // (thread 0) a target column's draft token; -2: none
     if (!r.draft && ft == 0) {
         const int gp1 = a.gamma + 1;
-        const int64_t ln = c / gp1;
+        const int64_t ln = udiv(c, gp1);
         const int j = (int)(c - ln * gp1);
         if (j < a.gamma) draft_tok = __ldg(a.drafts + ln * a.gamma + j);
     }
@@ -1046,12 +1069,7 @@ __device__ __forceinline__ void team_finish(const RoundArgs &a, const GmRun &r, 
     } else if (n > kRankMax) {
         select_many<NW, BAR>(n, kk, s, lane, w);
     } else {
-        for (int i = ft; i < n; i += TM::kFinThreads) {
-            const unsigned long long e = s.cand[i];
-            int rank = 0;
-            for (int jj = 0; jj < n; ++jj) rank += s.cand[jj] > e ? 1 : 0;
-            if (rank < kk) s.wl[0][rank] = e;
-        }
+        rank_into_list(s, n, kk, ft, TM::kFinThreads);
     }
     team_sync<NW, BAR>();
     if (r.draft) {
@@ -1106,9 +1124,6 @@ __device__ __forceinline__ void team_finish_all(const RoundArgs &a, const GmRun 
 // otherwise every CTA publishes its sorted list and the one that takes the
 // column's ticket last merges them.
 
-constexpr int kVecCap = (int)(sizeof(Smem::keys) / sizeof(uint4));   // vectors staged in s.keys
-static_assert(kVecCap <= kGroupCap, "their positions go to s.grp");
-
 // q (elements [g0, g0 + 8), counted like lo and hi) with its elements
 // outside [lo, hi) masked
 __device__ __forceinline__ uint4 mask_vec(const uint4 &q, int g0, int lo, int hi)
@@ -1124,29 +1139,47 @@ __device__ __forceinline__ uint4 mask_vec(const uint4 &q, int g0, int lo, int hi
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// The sorted top-kk of the part [lo, hi) of the column starting at element
-// cb, from this CTA's slice (vectors j0 + u 512 + t in q[u]), into s.wl[0];
-// returns its length, min(kk, the part's elements).  Every thread calls it.
-// Positions inside the slice are counted from its vector j0's first
-// element, e0 = 8 j0 - mis, in 32 bits.
+// Vector u of a thread's registers, u not known at compile time (selects:
+// a short, branch-free sequence instead of a copy of the caller's code per
+// vector).
 template <int L>
-__device__ __forceinline__ int pass_list(const GmRun &r, const uint4 (&q)[L], int64_t j0, int64_t cb, int64_t lo,
-                                         int64_t hi, Smem &s)
+__device__ __forceinline__ uint4 pick(const uint4 (&q)[L], int u)
+{
+    uint4 v = q[0];
+#pragma unroll
+    for (int i = 1; i < L; ++i)
+        if (i == u) v = q[i];
+    return v;
+}
+
+// The candidates of the part of a column held by this CTA's slice (vectors
+// j0 + u 512 + t in q[u], every element outside the part already the mask
+// value; cb the column's first element): its elements that reach the bound
+// T, unranked, in s.cand; returns how many (more than kCap: only the first
+// kCap kept).  With kk = 1 and no id map, just the part's best element
+// (none for an empty part).  Every thread calls it.  Positions inside the
+// slice are counted from its vector j0's first element, e0 = 8 j0 - mis, in
+// 32 bits.  The code is kept short (rolled loops over the few vectors that
+// matter): it runs once per launch, so each new stretch of it is an
+// instruction-cache miss.
+template <int L>
+__device__ __forceinline__ int pass_cands(const GmRun &r, const uint4 (&q)[L], int64_t j0, int64_t cb, Smem &s,
+                                          uint32_t &T_out)
 {
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     const int kk = r.kk;
-    const int64_t e0 = 8 * j0 - r.mis;
-    const int lr = (int)(lo - e0), hr = (int)(hi - e0);   // the part, from e0
-    const int idb = (int)(e0 - cb);                        // id of position 0
-    // 1. this thread's maximum over the part
-    uint32_t m2 = kNaN2;
+    const int idb = (int)(8 * j0 - r.mis - cb);   // id of position 0
+    // 1. the key of every vector's maximum, two to a word, and this
+    //    thread's maximum
+    uint32_t vk[(L + 1) / 2];
+    uint32_t mt = 0;
 #pragma unroll
     for (int u = 0; u < L; ++u) {
-        const int g0 = 8 * (u * 512 + t);
-        if (g0 >= lr && g0 + 8 <= hr) m2 = bmax2(m2, vmax(q[u]));
-        else if (g0 + 8 > lr && g0 < hr) m2 = bmax2(m2, vmax(mask_vec(q[u], g0, lr, hr)));
+        const uint32_t key = key_of(vmax(q[u]));
+        mt = key > mt ? key : mt;
+        if (u & 1) vk[u >> 1] |= key << 16;
+        else vk[u >> 1] = key;
     }
-    const uint32_t mt = key_of(m2);
     // 2. the bound T: the kk-th largest section maximum (kk <= 8) or thread
     //    maximum (larger kk, or a part in fewer than kk sections); 0 when
     //    fewer than kk threads hold an element of the part -- then every
@@ -1159,79 +1192,83 @@ __device__ __forceinline__ int pass_list(const GmRun &r, const uint4 (&q)[L], in
     }
     if ((lane & 7) == 0) s.sec[4 * w + (lane >> 3)] = m8;
     s.smax[t] = mt;
+    if (t == 0) s.last[1] = 0xFFFFFFFFu;   // kk = 1: the shared minimum below
     __syncthreads();
     uint32_t T = kk <= 8 ? kth_of_64(s.sec[lane], s.sec[lane + 32], kk) : 0u;
     if (T == 0u) T = kth_of_smem(s.smax, kThreads, kk, lane);
-    // 3. the vectors whose maximum reaches T (elements outside the part
-    //    masked) to shared memory, from the warps holding one; then their
-    //    elements >= T, one per thread, to the candidates
-    uint4 *vq = reinterpret_cast<uint4 *>(&s.keys[0][0]);
-    if (__any_sync(kFull, mt != 0 && mt >= T)) {
-        const bool mine = mt != 0 && mt >= T;
+    T_out = T;
+    // the vectors whose maximum reaches T (one or two, mostly)
+    uint32_t um = 0;
 #pragma unroll
-        for (int u = 0; u < L; ++u) {
-            const int g0 = 8 * (u * 512 + t);
-            const bool full = g0 >= lr && g0 + 8 <= hr;
-            const uint4 v = full ? q[u] : mask_vec(q[u], g0, lr, hr);
-            const bool take = mine && (full || (g0 + 8 > lr && g0 < hr)) && key_of(vmax(v)) >= T;
-            const uint32_t bal = __ballot_sync(kFull, take);
-            if (bal) {
-                uint32_t base = 0;
-                if (lane == 0) base = atomicAdd(&s.ngrp, (uint32_t)__popc(bal));
-                base = __shfl_sync(kFull, base, 0);
-                const uint32_t pos = base + (uint32_t)__popc(bal & lanemask_lt());
-                if (take && pos < (uint32_t)kVecCap) {
-                    vq[pos] = v;
-                    s.grp[pos] = (uint32_t)g0;
-                }
+    for (int u = 0; u < L; ++u) {
+        const uint32_t key = (vk[u >> 1] >> (16 * (u & 1))) & 0xFFFFu;
+        um |= (key != 0 && key >= T) ? 1u << u : 0u;
+    }
+    if (kk == 1 && r.id_map == nullptr) {
+        // the maximum T; of the elements at it, the one with the smallest
+        // position (the smallest id: no id map): each thread holding T
+        // offers its first (its vectors are in position order), a shared
+        // minimum picks among them
+        if (um) {
+            const int u = __ffs(um) - 1;
+            const uint4 v = pick(q, u);
+            int e = 7;
+#pragma unroll 1
+            for (int i = 6; i >= 0; --i)
+                if (order_key(half_of(v, i)) == T) e = i;
+            atomicMin(&s.last[1], (uint32_t)(8 * (u * 512 + t) + e));
+        }
+        __syncthreads();
+        const uint32_t p = s.last[1];
+        if (p == 0xFFFFFFFFu) return 0;
+        // the thread holding position p = 8 (u 512 + t) + e writes its entry
+        if ((int)((p >> 3) & 511u) == t) {
+            const uint32_t raw = half_of(pick(q, (int)(p >> 12)), (int)(p & 7u));
+            s.cand[0] = make_entry(T, (uint32_t)((int)p + idb), raw);
+        }
+        __syncthreads();
+        return 1;
+    }
+    // 3. the candidates: the elements >= T of those vectors, each by the
+    //    thread holding it, straight from its registers
+#pragma unroll 1
+    for (; um; um &= um - 1) {
+        const int u = __ffs(um) - 1;
+        const uint4 v = pick(q, u);
+        const int g0 = 8 * (u * 512 + t);
+#pragma unroll 1
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t raw = half_of(v, e);
+            const uint32_t ke = order_key(raw);
+            if (ke != 0 && ke >= T) {
+                uint32_t id = (uint32_t)(g0 + e + idb);
+                if (r.id_map) id = (uint32_t)__ldg(r.id_map + id);
+                const uint32_t pos = atomicAdd(&s.ncand, 1u);
+                if (pos < (uint32_t)kCap) s.cand[pos] = make_entry(ke, id, raw);
             }
         }
     }
     __syncthreads();
-    const int nvec = (int)s.ngrp;
-    if (nvec <= kVecCap)
-        for (int i0 = 0; i0 < 8 * nvec; i0 += kThreads) {
-            const int i = i0 + t;
-            unsigned long long ent = 0ull;
-            if (i < 8 * nvec) {
-                const uint32_t raw = half_of(vq[i >> 3], i & 7);
-                const uint32_t key = order_key(raw);
-                if (key != 0 && key >= T) {   // masked elements: key 0
-                    uint32_t id = (uint32_t)((int)s.grp[i >> 3] + (i & 7) + idb);
-                    if (r.id_map) id = (uint32_t)__ldg(r.id_map + id);
-                    ent = make_entry(key, id, raw);
-                }
-            }
-            const uint32_t bal = __ballot_sync(kFull, ent != 0ull);
-            if (bal) {
-                uint32_t base = 0;
-                if (lane == 0) base = atomicAdd(&s.ncand, (uint32_t)__popc(bal));
-                base = __shfl_sync(kFull, base, 0);
-                const uint32_t pos = base + (uint32_t)__popc(bal & lanemask_lt());
-                if (ent != 0ull && pos < (uint32_t)kCap) s.cand[pos] = ent;
-            }
-        }
-    __syncthreads();
-    // 4. ranked (value desc, id asc); many: sorted lists per warp; more than
-    //    the buffers hold (massive ties): the part scanned exactly
-    const int n = nvec > kVecCap ? kCap + 1 : (int)s.ncand;
+    return (int)s.ncand;
+}
+
+// The part's sorted top-kk from its n candidates (pass_cands; bound T),
+// into s.wl[0]; returns its length, min(n, kk).  Many candidates: sorted
+// lists per warp; more than the buffer holds (massive ties): the part
+// [lo, hi) scanned exactly.  Every thread calls it.
+__device__ __forceinline__ int pass_rank(const GmRun &r, int n, int64_t cb, int64_t lo, int64_t hi, uint32_t T,
+                                         Smem &s)
+{
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int kk = r.kk;
     if (n > kCap) {
         exact_scan<kWarps, 0>(view_of(r), lo, hi, cb, T, s, lane, w);
     } else if (n > kRankMax) {
         select_many<kWarps, 0>(n, kk, s, lane, w);
     } else {
-        for (int i = t; i < n; i += kThreads) {
-            const unsigned long long e = s.cand[i];
-            int rank = 0;
-            for (int j = 0; j < n; ++j) rank += s.cand[j] > e ? 1 : 0;
-            if (rank < kk) s.wl[0][rank] = e;
-        }
+        rank_into_list(s, n, kk, t, kThreads);
     }
     __syncthreads();
-    if (t == 0) {
-        s.ncand = 0u;
-        s.ngrp = 0u;
-    }
     return n < kk ? n : kk;
 }
 
@@ -1258,18 +1295,18 @@ __device__ __forceinline__ void pass_emit(const RoundArgs &a, const GmRun &r, in
 }
 
 // The CTA that came last to column c (its nc CTAs: units u0, u0 + 1, ...):
-// every CTA's published list (kk entries, 0 for none), merged, then
-// emitted; the ticket cleared for the next launch.  At most kCap entries.
-__device__ __forceinline__ void pass_merge(const RoundArgs &a, const GmRun &r, int64_t c, int64_t u0, int nc,
+// every CTA's published entries (per of them each, 0 for none; the part's
+// top-kk or all its candidates), merged, then emitted; the ticket cleared
+// for the next launch.  At most kCap entries in all.
+__device__ __forceinline__ void pass_merge(const RoundArgs &a, const GmRun &r, int64_t c, int64_t u0, int nc, int per,
                                            int32_t draft_tok, Smem &s)
 {
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     const int kk = r.kk;
-    const int n_all = nc * kk;
+    const int n_all = nc * per;
     for (int i0 = 0; i0 < n_all; i0 += kThreads) {
         const int i = i0 + t;
-        const unsigned long long e =
-            i < n_all ? __ldcg(a.partials + (u0 + i / kk) * a.pstride + i % kk) : 0ull;
+        const unsigned long long e = i < n_all ? __ldcg(a.partials + (u0 + i / per) * a.pstride + i % per) : 0ull;
         const uint32_t bal = __ballot_sync(kFull, e != 0ull);
         if (bal) {
             uint32_t base = 0;
@@ -1281,70 +1318,142 @@ __device__ __forceinline__ void pass_merge(const RoundArgs &a, const GmRun &r, i
     }
     __syncthreads();
     const int n = (int)s.ncand < kCap ? (int)s.ncand : kCap;
-    if (n > kRankMax) {
-        select_many<kWarps, 0>(n, kk, s, lane, w);
-    } else {
-        for (int i = t; i < n; i += kThreads) {
-            const unsigned long long e = s.cand[i];
-            int rank = 0;
-            for (int j = 0; j < n; ++j) rank += s.cand[j] > e ? 1 : 0;
-            if (rank < kk) s.wl[0][rank] = e;
-        }
-    }
+    if (n > kRankMax) select_many<kWarps, 0>(n, kk, s, lane, w);
+    else rank_into_list(s, n, kk, t, kThreads);
     __syncthreads();
     if (t == 0) r.ticket[c] = 0u;   // ready for the next launch
     pass_emit(a, r, c, draft_tok, s);
 }
 
-// One-pass mode, all of it, for CTA bi of run r.
+// Greedy verify in one pass: every CTA of a lane's target columns publishes
+// its part's best entry (value desc, id asc; 0 for none) and takes the
+// lane's ticket (the ticket of the lane's first column); the last of them
+// takes each column's best over its CTAs -- the column's argmax -- and
+// verifies the lane: the accept length is the number of leading drafts
+// equal to their column's argmax, the commit ids those argmaxes up to and
+// including position acc, -1 after.  dr: lane j of warp 0 holds draft j
+// (early).  Every thread calls it.
+__device__ __forceinline__ void pass_lane(const RoundArgs &a, const GmRun &r, int bi, int64_t c,
+                                          unsigned long long best, int32_t dr, Smem &s)
+{
+    const int t = threadIdx.x, lane = t & 31;
+    const int gamma = a.gamma, gp1 = gamma + 1;
+    const int64_t cols = r.cols;
+    const int64_t ln = udiv(c, gp1), cf = ln * gp1;
+    const int64_t uf = udiv(cf * r.W + cols - 1, cols);        // the lane's first CTA
+    const int nu = (int)(udiv((cf + gp1) * r.W + cols - 1, cols) - uf);
+    unsigned long long *pl = a.partials + (int64_t)a.d_units * a.pstride;
+    if (t == 0) {
+        __stcg(pl + (int64_t)bi * a.pstride, best);
+        s.last[0] = atom_add_acq_rel(r.ticket + cf, 1u) == (uint32_t)(nu - 1) ? 1u : 0u;
+    }
+    if (t < 16) s.wl[1][t] = 0ull;
+    __syncthreads();
+    if (s.last[0] == 0u) return;
+    for (int i = t; i < nu; i += kThreads) {
+        const int64_t u = uf + i;
+        const unsigned long long e = u == bi ? best : __ldcg(pl + u * a.pstride);
+        atomicMax(&s.wl[1][udiv(u * cols, r.W) - cf], e);   // the CTA's column, within the lane
+    }
+    __syncthreads();
+    if (t < 32) {
+        const int32_t token = lane < gp1 ? (int32_t)entry_id(s.wl[1][lane]) : -1;
+        const uint32_t miss = __ballot_sync(kFull, lane < gamma && dr != token);
+        const int acc = miss ? __ffs(miss) - 1 : gamma;
+        if (lane < gp1) a.out_commit[ln * gp1 + lane] = lane <= acc ? token : -1;
+        count_lane(a.counters, gamma, acc, lane);
+        if (lane == 0) {
+            a.out_accept[ln] = acc;
+            r.ticket[cf] = 0u;   // ready for the next launch
+        }
+    }
+}
+
+// One-pass mode, all of it, for CTA bi of run r.  A CTA whose column has
+// others publishes its candidates unranked when there are at most 2 kk of
+// them (the merging CTA ranks them all), else its ranked top-kk.
 template <int L>
 __device__ __forceinline__ void one_pass(const RoundArgs &a, const GmRun &r, int bi, Smem &s)
 {
     const int t = threadIdx.x;
-    const int64_t cols = r.N / r.V;
-    const int64_t c = (int64_t)bi * cols / r.W;                        // this CTA's column
-    const int64_t f = (c * r.W + cols - 1) / cols;                     // its first CTA
-    const int nc = (int)(((c + 1) * r.W + cols - 1) / cols - f);       // and how many
+    const int64_t cols = r.cols;
+    const int64_t c = udiv((int64_t)bi * cols, r.W);                   // this CTA's column
+    const int64_t f = udiv(c * r.W + cols - 1, cols);                  // its first CTA
+    const int nc = (int)(udiv((c + 1) * r.W + cols - 1, cols) - f);    // and how many
     const int64_t cb = c * r.V, ce = cb + r.V;
     const int64_t jf = (cb + r.mis) >> 3, nvc = ((ce - 1 + r.mis) >> 3) - jf + 1;
-    const int64_t j0 = jf + (bi - f) * nvc / nc, j1 = jf + (bi - f + 1) * nvc / nc;
-    // Plain (L2-cached) loads, not read-only ones: a read-only load may be
-    // issued again at a later use instead of being kept in registers.
+    // the column's vectors split among its CTAs: the first nvc mod nc get
+    // one more
+    const int64_t per_cta = udiv(nvc, nc), extra = nvc - per_cta * nc, sub = bi - f;
+    const int64_t j0 = jf + sub * per_cta + (sub < extra ? sub : extra);
+    const int64_t j1 = j0 + per_cta + (sub < extra ? 1 : 0);
+    // The part: elements [lo, hi).  Its whole vectors [ja, jb) load as
+    // vectors; the (at most two) vectors it shares with the next or previous
+    // column, or with the buffer's edge, element by element, the rest of
+    // them masked.  Plain (L2-cached) loads, not read-only ones: a
+    // read-only load may be issued again at a later use instead of being
+    // kept in registers.
+    const int64_t e0 = 8 * j0 - r.mis, e1 = 8 * j1 - r.mis;
+    const int64_t lo = e0 > cb ? e0 : cb, hi = e1 < ce ? e1 : ce;
+    int64_t ja = (lo + r.mis + 7) >> 3, jb = (hi + r.mis) >> 3;
+    ja = ja > r.jlo ? ja : r.jlo;
+    jb = jb < r.jhi ? jb : r.jhi;
     uint4 q[L];
 #pragma unroll
     for (int u = 0; u < L; ++u) {
         const int64_t j = j0 + u * 512 + t;
-        q[u] = (j < j1 && j >= r.jlo && j < r.jhi) ? __ldcg(r.vb + j) : make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
+        q[u] = (j >= ja && j < jb) ? __ldcg(r.vb + j) : make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
     }
-    if (j0 < r.jlo || j1 > r.jhi) {
-        // the buffer's edge vectors (at most one at each end), element by element
+    {
+        const int64_t jl = (hi - 1 + r.mis) >> 3;   // the part's last vector; j0 its first
+#pragma unroll 1
+        for (int k2 = 0; k2 < 2; ++k2) {
+            const int64_t j = k2 ? jl : j0;
+            if ((k2 && jl == j0) || (j >= ja && j < jb) || (int)((j - j0) & 511) != t) continue;
+            const uint4 v = load_edge(r.buf, j, r.mis, lo, hi);
+            const int u = (int)((j - j0) >> 9);
 #pragma unroll
-        for (int u = 0; u < L; ++u) {
-            const int64_t j = j0 + u * 512 + t;
-            if (j < j1 && (j < r.jlo || j >= r.jhi)) q[u] = load_edge(r.buf, j, r.mis, 0, r.N);
+            for (int i = 0; i < L; ++i)
+                if (i == u) q[i] = v;
         }
     }
-    // a target column's draft token (thread 0), early
+    // a target column's draft token (thread 0); greedy: the lane's drafts
+    // (lane j of warp 0 draft j), early
+    const bool greedy = !r.draft && a.uniforms == nullptr;
     int32_t dtok = -2;
-    if (!r.draft && t == 0) {
+    if (!r.draft && t < 32) {
         const int gp1 = a.gamma + 1;
-        const int64_t ln = c / gp1;
-        const int j = (int)(c - ln * gp1);
-        if (j < a.gamma) dtok = __ldg(a.drafts + ln * a.gamma + j);
+        const int64_t ln = udiv(c, gp1);
+        const int j = greedy ? t : (int)(c - ln * gp1);
+        if (j < a.gamma && (greedy || t == 0)) dtok = __ldg(a.drafts + ln * a.gamma + j);
     }
-    const int64_t e0 = 8 * j0 - r.mis, e1 = 8 * j1 - r.mis;
-    const int len = pass_list<L>(r, q, j0, cb, e0 > cb ? e0 : cb, e1 < ce ? e1 : ce, s);
-    if (nc == 1) {
-        pass_emit(a, r, c, dtok, s);
+    uint32_t T;
+    const int n = pass_cands<L>(r, q, j0, cb, s, T);
+    if (greedy) {
+        // kk = 1, no id map: n <= 1, the best in s.cand[0]
+        pass_lane(a, r, bi, c, n ? s.cand[0] : 0ull, dtok, s);
         return;
     }
-    const int64_t unit0 = r.draft ? 0 : a.d_units;
-    unsigned long long *slot = a.partials + (unit0 + bi) * a.pstride;
-    if (t < r.kk) __stcg(slot + t, t < len ? s.wl[0][t] : 0ull);
-    __syncthreads();   // the list is written
-    if (t == 0) s.last[0] = arrive_at_end(r.ticket + c, (uint32_t)(nc - 1));
+    const int per = 2 * r.kk;   // entries a CTA publishes (the slot holds them)
+    if (nc == 1 || n > per) {
+        const int len = pass_rank(r, n, cb, lo, hi, T, s);
+        if (nc == 1) {
+            pass_emit(a, r, c, dtok, s);
+            return;
+        }
+        unsigned long long *slot = a.partials + ((r.draft ? 0 : a.d_units) + bi) * a.pstride;
+        if (t < per) __stcg(slot + t, t < len ? s.wl[0][t] : 0ull);
+    } else {
+        unsigned long long *slot = a.partials + ((r.draft ? 0 : a.d_units) + bi) * a.pstride;
+        if (t < per) __stcg(slot + t, t < n ? s.cand[t] : 0ull);
+    }
+    __syncthreads();   // the entries are written (and s.cand, s.wl read)
+    if (t == 0) {
+        s.ncand = 0u;
+        s.last[0] = arrive_at_end(r.ticket + c, (uint32_t)(nc - 1));
+    }
     __syncthreads();
-    if (s.last[0] != 0u) pass_merge(a, r, c, unit0 + f, nc, dtok, s);
+    if (s.last[0] != 0u) pass_merge(a, r, c, (r.draft ? 0 : a.d_units) + f, nc, per, dtok, s);
 }
 
 // MODE 0: slice mode; 1: column mode; 2 and 3: column mode with finishing
@@ -1377,8 +1486,8 @@ __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_co
     }
     if constexpr (MODE == 2 || MODE == 3) {
         constexpr int SW = MODE == 2 ? 12 : 8;
-        const int64_t cols = r.N / r.V;
-        const int64_t c0 = bi * cols / r.W, c1 = (bi + 1) * cols / r.W;
+        const int64_t cols = r.cols;
+        const int64_t c0 = udiv(bi * cols, r.W), c1 = udiv((bi + 1) * cols, r.W);
         if (threadIdx.x < Team<SW>::kStreamThreads) team_stream<U, SW>(r, c0, c1, s);
         else team_finish_all<U, SW>(a, r, c0, c1, s);
         return;
@@ -1386,9 +1495,9 @@ __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_co
     if constexpr (MODE == 0) {
         const int64_t g0b = slice_lo(r, bi), g1b = slice_lo(r, bi + 1);
         if (g1b <= g0b) return;
-        int64_t cn = elem_lo<U>(r, g0b) / r.V + 1;   // the column after the one in progress
+        int64_t cn = udiv(elem_lo<U>(r, g0b), r.V) + 1;   // the column after the one in progress
         int64_t cut = cn * r.V;                      // its first element
-        const int64_t cl = (elem_hi<U>(r, g1b - 1) - 1) / r.V;
+        const int64_t cl = udiv(elem_hi<U>(r, g1b - 1) - 1, r.V);
         int64_t cdone = cn - 1;      // the first column not yet handled
         int64_t pend = -1;           // a shared column whose ticket this CTA took inside the stream
         uint32_t pend_old = 0;       // (thread 0) that ticket's count before it

@@ -79,7 +79,7 @@ __device__ __noinline__ void emit_column(const RoundArgs &a, const Run &r, int64
     // the lane's ticket counts its finished columns; the warp that finishes
     // the last one reads the argmaxes back and runs the prefix match
     const int gp1 = a.gamma + 1;
-    const int64_t ln = c / gp1;
+    const int64_t ln = udiv(c, gp1);
     __threadfence();
     __syncwarp();
     unsigned last = 0;
@@ -231,7 +231,7 @@ __device__ __forceinline__ void stream_slice(const RoundArgs &a, const Run &r, i
     if (lane == 0)
         for (int64_t i = 0; i < nst && i < kStages; ++i) issue_stage(r, ws, J0, J1, i);
 
-    int64_t c = first_elem(r, w) / r.V;       // current column
+    int64_t c = udiv(first_elem(r, w), r.V);       // current column
     ColState cs = {0, 0u, 0u, false, 0};
     // a column split across warps has a shared certificate in global memory:
     // every warp raises it with its own certified keys and filters against

@@ -280,21 +280,26 @@ bool plan_gm(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, int
     // One pass: the CTAs of each run dealt out to its columns (every column
     // at least one, every CTA at least one vector), every CTA's slice at
     // most 512 L vectors (L = 8 loads per thread, else 16) so that it holds
-    // the slice in registers, and a column's lists fitting the merge buffer.
+    // the slice in registers, and a column's published entries (2 kk a CTA)
+    // fitting the merge buffer.
+    const int kmax = a.k > a.t_k ? a.k : a.t_k;
     for (int L : {8, 16}) {
+        const int stride = 2 * kmax + 2;
         int32_t wd = 0, wt = 0;
-        split_units(nv_d, nv_t, d.sms, 512, a.pstride, max_partials, &wd, &wt);   // 8 KB a CTA at least
+        split_units(nv_d, nv_t, d.sms, 512, stride, max_partials, &wd, &wt);   // 8 KB a CTA at least
         auto fits = [L](int64_t nv, int64_t cols, int64_t w, int64_t V, int kk) {
             if (nv == 0) return true;
             if (w < cols) return false;
             const int64_t nmin = w / cols, nmax = (w + cols - 1) / cols;
             const int64_t nvc = V / 8 + 2;   // a column's vectors, at most
-            return (nvc + nmin - 1) / nmin <= 512 * (int64_t)L && V / 8 >= nmax && nmax * kk <= (int64_t)gm::kCap;
+            return (nvc + nmin - 1) / nmin <= 512 * (int64_t)L && V / 8 >= nmax &&
+                   nmax * 2 * kk <= (int64_t)gm::kCap;
         };
         const int64_t units = (nv_d > 0 ? wd : 0) + (nv_t > 0 ? wt : 0);
         if (!fits(nv_d, a.d_cols, wd, a.d_V, a.k) || !fits(nv_t, a.t_cols, wt, a.t_V, a.t_k) ||
-            units * a.pstride > max_partials)
+            units * stride > max_partials)
             continue;
+        a.pstride = stride;
         a.d_units = nv_d > 0 ? wd : 0;
         a.t_units = nv_t > 0 ? wt : 0;
         p.gm = true;
@@ -318,7 +323,6 @@ bool plan_gm(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, int
     // outweighs its stream (k above 8 on columns of at most 192 K logits:
     // GB300, C5s at k = 20 / 64: 196 / 288 us with 4, 177 / 197 with 8; C4
     // and C5 at k = 8 faster with 4).  Columns must fit kTeamRows batches.
-    const int kmax = a.k > a.t_k ? a.k : a.t_k;
     const bool eight = kmax > 8 && vmax <= 192 * 1024 &&
                        (vmax / 8 + 2) <= (int64_t)gm::Team<8>::kTeamRows * gm::Team<8>::kStreamThreads * 8;
     const bool four = (vmax / 8 + 2) <= (int64_t)gm::Team<12>::kTeamRows * gm::Team<12>::kStreamThreads * 8;
