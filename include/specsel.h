@@ -282,6 +282,12 @@ spec_status spec_shortlist_topk(const uint16_t *hidden, int64_t cols, int64_t d,
  *                       (a 2-byte key); per column, the k-th largest of
  *                       those maxima bounds the top-k, and only the few
  *                       groups that reach it are read again and ranked.
+ *                       One-pass mode (rounds of at most 4,096 -- or 8,192
+ *                       -- 16-byte vectors a CTA with every column on at
+ *                       least one CTA): each CTA keeps its slice of one
+ *                       column in registers and selects from them; a
+ *                       column's CTAs publish their lists (greedy verify:
+ *                       one argmax each) and the last to arrive merges.
  *                       Column mode (at least 3/4 as many columns as SMs,
  *                       columns of 32,768 to ~393,000 logits): each CTA
  *                       owns whole columns and keeps their keys in shared
@@ -300,9 +306,10 @@ spec_status spec_shortlist_topk(const uint16_t *hidden, int64_t cols, int64_t d,
  *   SPEC_KERNEL_WARP -- every warp streams its own slice with its own ring,
  *                       buffer and threshold; no coordination inside the
  *                       stream.
- *   SPEC_KERNEL_AUTO -- (default) GROUPMAX in column mode at any size; else,
- *                       up to 6 MiB of logits per SM, GROUPMAX in slice mode
- *                       (or CTA where it cannot run); else WARP.
+ *   SPEC_KERNEL_AUTO -- (default) GROUPMAX in one-pass mode where it fits,
+ *                       else in column mode at any size; else, up to 6 MiB
+ *                       of logits per SM, GROUPMAX in slice mode (or CTA
+ *                       where it cannot run); else WARP.
  * The choice is process-wide; SPEC_ERR_ARG for any other value. */
 #define SPEC_KERNEL_AUTO 0
 #define SPEC_KERNEL_WARP 1

@@ -475,6 +475,25 @@ def test_column_over_many_units(k):
     gu.assert_topk_equal(gu.run_topk(x, k, offset=3), oracle.topk(x, k), f"one column V={V} k={k}")
 
 
+@pytest.mark.parametrize("k", [8, 64])
+def test_rounds_of_a_million_vectors(k):
+    """24 draft columns and a lane of 8 target columns at V = 248,046 (about
+    a million 16-byte vectors: more than 4,096 a CTA on a full grid, so the
+    group-maxima kernel's one-pass mode holds 16 vectors a thread), and a
+    sampled verify of 4 such lanes alone."""
+    V = synth.VOCAB
+    x = synth._draft_block(95 + k, 24, V, 3.0)
+    tgt, drafts, _, _ = synth.planted_verify(96 + k, 1, 7, V)
+    v, i, a, c = gu.run_round(x, k, tgt, drafts, offset=k % 8)
+    gu.assert_topk_equal((v, i), oracle.topk(x, k), f"24 columns k={k}")
+    gu.assert_verify_equal((a, c), oracle.verify(tgt, drafts), f"24 columns k={k} verify")
+    t4, d4, _, _ = synth.planted_verify(97 + k, 4, 7, V)
+    u = synth.rng(98 + k, 0).random((4, 8, 2))
+    wa, wc, margin = oracle.sampled_verify(t4, d4, 1.0, 0.95, 20, u)
+    assert margin > 1e-9
+    gu.assert_verify_equal(gu.run_verify_sampled(t4, d4, 1.0, 0.95, 20, u), (wa, wc), "sampled 4 lanes")
+
+
 def test_verify_columns_over_many_units():
     """A lane of four target columns of a million logits each (greedy and
     sampled): every column is shared by dozens of units."""
