@@ -322,6 +322,34 @@ __device__ __forceinline__ uint32_t half_of(const uint4 &q, int e)
     return (e & 1) ? (w >> 16) : (w & 0xFFFFu);
 }
 
+// q (elements [g0, g0 + 8), counted like lo and hi) with its elements
+// outside [lo, hi) masked
+__device__ __forceinline__ uint4 mask_vec(const uint4 &q, int g0, int lo, int hi)
+{
+    const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const int p = g0 + 2 * h;
+        const bool in0 = p >= lo && p < hi, in1 = p + 1 >= lo && p + 1 < hi;
+        o[h] = (in0 ? (wd[h] & 0xFFFFu) : 0x7FFFu) | (in1 ? (wd[h] & 0xFFFF0000u) : 0x7FFF0000u);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Vector u of a thread's registers, u not known at compile time (selects:
+// a short, branch-free sequence instead of a copy of the caller's code per
+// vector).
+template <int L>
+__device__ __forceinline__ uint4 pick(const uint4 (&q)[L], int u)
+{
+    uint4 v = q[0];
+#pragma unroll
+    for (int i = 1; i < L; ++i)
+        if (i == u) v = q[i];
+    return v;
+}
+
 __device__ __forceinline__ unsigned long long make_entry(uint32_t key, uint32_t id, uint32_t raw)
 {
     return ((unsigned long long)key << 48) | ((unsigned long long)(~id) << 16) | raw;
@@ -571,10 +599,44 @@ __device__ __forceinline__ Sel select_candidates(const RoundArgs &a, const GmRun
     }
     if ((lane & 7) == 0) s.sec[4 * w + (lane >> 3)] = m8;
     s.smax[t] = mt;
+    if (t == 0) s.cand[0] = ~0ull;   // kk = 1: the shared minimum below
     __syncthreads();
     // T: the kk-th largest of 64 section maxima (kk <= 8) or of the 512
     // threads' maxima; either is the key of kk distinct groups
     const uint32_t T = kk <= 8 ? kth_of_64(s.sec[lane], s.sec[lane + 32], kk) : kth_of_smem(s.smax, kThreads, kk, lane);
+    if (kk == 1 && r.id_map == nullptr && nb <= kKeyRows) {
+        // the column's maximum T (an argmax: greedy verify, or a top-1):
+        // each thread with a group at T reads its first such group again
+        // (its groups are in position order) and offers the first element
+        // at T in it; a shared minimum of (position, value) picks the
+        // smallest id.  One candidate, no group list, no rank.
+        if (mt != 0 && mt == T) {
+            int i = 0;
+            while (i < nb - 1 && s.keys[i][t] != T) ++i;
+            const int64_t jg = jbase + (int64_t)i * B + t;
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) v[u] = load_col_vec(rv, jg + u * 512, cb, ce);
+            uint32_t um = 0;
+#pragma unroll
+            for (int u = 0; u < U; ++u) um |= key_of(vmax(v[u])) == T ? 1u << u : 0u;
+            const int u = __ffs(um) - 1;
+            const uint4 x = pick(v, u);
+            int e = 7;
+#pragma unroll 1
+            for (int k2 = 6; k2 >= 0; --k2)
+                if (order_key(half_of(x, k2)) == T) e = k2;
+            const int64_t pos = 8 * (jg + u * 512) - r.mis + e - cb;
+            atomicMin(&s.cand[0], ((unsigned long long)pos << 16) | half_of(x, e));
+        }
+        __syncthreads();
+        if (t == 0) {
+            const unsigned long long b = s.cand[0];
+            s.cand[0] = make_entry(T, (uint32_t)(b >> 16), (uint32_t)(b & 0xFFFFu));
+            s.ncand = b != ~0ull ? 1u : 0u;
+        }
+        return Sel{T, 1 << 30, false, draft_tok};
+    }
     // 3. the groups to re-read: every group above T, and of the groups at T
     //    (ties) -- with token ids, which grow batch by batch, and more than a
     //    few of them -- only those of the first batches that hold kk of them
@@ -1124,33 +1186,6 @@ __device__ __forceinline__ void team_finish_all(const RoundArgs &a, const GmRun 
 // otherwise every CTA publishes its sorted list and the one that takes the
 // column's ticket last merges them.
 
-// q (elements [g0, g0 + 8), counted like lo and hi) with its elements
-// outside [lo, hi) masked
-__device__ __forceinline__ uint4 mask_vec(const uint4 &q, int g0, int lo, int hi)
-{
-    const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-        const int p = g0 + 2 * h;
-        const bool in0 = p >= lo && p < hi, in1 = p + 1 >= lo && p + 1 < hi;
-        o[h] = (in0 ? (wd[h] & 0xFFFFu) : 0x7FFFu) | (in1 ? (wd[h] & 0xFFFF0000u) : 0x7FFF0000u);
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-// Vector u of a thread's registers, u not known at compile time (selects:
-// a short, branch-free sequence instead of a copy of the caller's code per
-// vector).
-template <int L>
-__device__ __forceinline__ uint4 pick(const uint4 (&q)[L], int u)
-{
-    uint4 v = q[0];
-#pragma unroll
-    for (int i = 1; i < L; ++i)
-        if (i == u) v = q[i];
-    return v;
-}
 
 // The candidates of the part of a column held by this CTA's slice (vectors
 // j0 + u 512 + t in q[u], every element outside the part already the mask
