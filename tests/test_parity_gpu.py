@@ -239,6 +239,22 @@ def test_ties_everywhere_large():
         assert np.all(i == np.arange(k)[None, :]) and np.all(v == synth.bf16_bits(1.5))
 
 
+def test_argmax_ties_column_mode():
+    """128 columns of 65,536 logits from three levels, the maximum repeated in
+    nearly every group of 64: enough columns for the group-maxima kernel's
+    column mode, whose k = 1 finish must return the first position at the
+    maximum (top-1, and greedy verify of 16 lanes)."""
+    V = 65_536
+    x = synth.levels_block(31, 128, V, [0.0, 1.0, -0.0])
+    gu.assert_topk_equal(gu.run_topk(x, 1), oracle.topk(x, 1), "top-1 ties, 128 columns")
+    lanes, gamma = 16, 7
+    t = synth.levels_block(32, lanes * (gamma + 1), V, [0.0, 2.0, 1.0])
+    d = synth.random_drafts(33, lanes, gamma, V)
+    am = oracle.argmax(t).reshape(lanes, gamma + 1)
+    d[: lanes // 2] = am[: lanes // 2, :gamma]   # half the lanes accept every draft
+    gu.assert_verify_equal(gu.run_verify(t, d), oracle.verify(t, d), "verify ties, 128 columns")
+
+
 def test_signed_zero_and_inf():
     V = 70_001
     x = np.full((4, V), 0xFF80, dtype=np.uint16)                  # all -inf
