@@ -1404,13 +1404,147 @@ __device__ __forceinline__ void pass_lane(const RoundArgs &a, const GmRun &r, in
     }
 }
 
+// ---- one pass in thread-block clusters (MODE 7) -------------------------------
+//
+// The same one pass with each column's CTAs (Q of them, all the column has)
+// launched as one thread-block cluster: instead of publishing to global
+// memory and meeting through a ticket, a column's CTAs store their entries
+// straight into the shared memory of the cluster's first CTA and meet at a
+// cluster barrier -- no L2 round trip for the merge.  The barriers are the
+// hardware's: every CTA of a cluster is resident at once, and every thread
+// of every CTA passes both phases.
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// the address of this CTA's shared variable p in the CTA of the given rank
+__device__ __forceinline__ uint32_t cluster_map(const void *p, uint32_t rank)
+{
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    return a;
+}
+__device__ __forceinline__ void st_cluster_u64(uint32_t addr, unsigned long long v)
+{
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
+// The receive area of the cluster's first CTA: per entries from each of the
+// Q CTAs, in its group-key buffer (which the one-pass mode does not use).
+__device__ __forceinline__ unsigned long long *cluster_inbox(Smem &s)
+{
+    return reinterpret_cast<unsigned long long *>(&s.keys[0][0]);
+}
+static_assert(sizeof(Smem::keys) >= 8 * 2 * SPEC_MAX_K * sizeof(unsigned long long), "inbox of 8 CTAs");
+
+// Greedy verify of a lane from its columns' argmax entries, one per column
+// (value desc, id asc): the first CTA of each column's cluster publishes its
+// column's entry and takes the lane's ticket (the ticket of the lane's first
+// column); the last of them verifies the lane as pass_lane does.  dr: lane
+// j of warp 0 holds draft j.  Every thread of the CTA calls it.
+__device__ __forceinline__ void lane_of_columns(const RoundArgs &a, const GmRun &r, int64_t c, unsigned long long best,
+                                                int32_t dr, Smem &s)
+{
+    const int t = threadIdx.x, lane = t & 31;
+    const int gamma = a.gamma, gp1 = gamma + 1;
+    const int64_t ln = udiv(c, gp1), cf = ln * gp1;
+    unsigned long long *pl = a.partials + (int64_t)a.d_units * a.pstride;   // slot per target column
+    if (t == 0) {
+        __stcg(pl + c * a.pstride, best);
+        s.last[0] = atom_add_acq_rel(r.ticket + cf, 1u) == (uint32_t)gamma ? 1u : 0u;
+    }
+    __syncthreads();
+    if (s.last[0] == 0u || t >= 32) return;
+    const unsigned long long e = lane < gp1 ? (cf + lane == c ? best : __ldcg(pl + (cf + lane) * a.pstride)) : 0ull;
+    const int32_t token = lane < gp1 ? (int32_t)entry_id(e) : -1;
+    const uint32_t miss = __ballot_sync(kFull, lane < gamma && dr != token);
+    const int acc = miss ? __ffs(miss) - 1 : gamma;
+    if (lane < gp1) a.out_commit[ln * gp1 + lane] = lane <= acc ? token : -1;
+    count_lane(a.counters, gamma, acc, lane);
+    if (lane == 0) {
+        a.out_accept[ln] = acc;
+        r.ticket[cf] = 0u;   // ready for the next launch
+    }
+}
+
+// After pass_cands in a cluster of Q CTAs (one column c): the column's
+// entries meet in the first CTA, which merges and emits them (greedy verify:
+// the column's argmax goes on to lane_of_columns).  n, T: pass_cands'
+// results; [lo, hi): this CTA's part.
+__device__ __forceinline__ void cluster_finish(const RoundArgs &a, const GmRun &r, int64_t c, int n, uint32_t T,
+                                               int64_t cb, int64_t lo, int64_t hi, bool greedy, int32_t dtok,
+                                               Smem &s)
+{
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const uint32_t rank = cluster_rank();
+    const int kk = r.kk, per = greedy ? 1 : 2 * kk;
+    unsigned long long *inbox = cluster_inbox(s);
+    // this CTA's entries: its candidates when at most per, else its top-kk
+    const unsigned long long *src = s.cand;
+    int cnt = n;
+    if (!greedy && n > per) {
+        cnt = pass_rank(r, n, cb, lo, hi, T, s);
+        src = s.wl[0];
+    }
+    cluster_wait();   // every CTA of the cluster has started (phase 1, arrived at entry)
+    for (int i = t; i < per; i += kThreads)
+        st_cluster_u64(cluster_map(inbox + rank * per + i, 0), i < cnt ? src[i] : 0ull);
+    cluster_arrive();
+    cluster_wait();   // phase 2: the first CTA holds every entry
+    if (rank != 0) return;
+    uint32_t Q;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(Q));
+    if (greedy) {
+        unsigned long long best = 0ull;
+        if (t < 32) {
+            best = lane < (int)Q ? inbox[lane] : 0ull;
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) {
+                const unsigned long long o = __shfl_xor_sync(kFull, best, d);
+                best = o > best ? o : best;
+            }
+        }
+        lane_of_columns(a, r, c, best, dtok, s);
+        return;
+    }
+    // merge: the nonzero entries into s.cand, ranked into s.wl[0], emitted
+    if (t == 0) s.ncand = 0u;
+    __syncthreads();
+    const int n_all = (int)Q * per;
+    for (int i0 = 0; i0 < n_all; i0 += kThreads) {
+        const int i = i0 + t;
+        const unsigned long long e = i < n_all ? inbox[i] : 0ull;
+        const uint32_t bal = __ballot_sync(kFull, e != 0ull);
+        if (bal) {
+            uint32_t base = 0;
+            if (lane == 0) base = atomicAdd(&s.ncand, (uint32_t)__popc(bal));
+            base = __shfl_sync(kFull, base, 0);
+            const uint32_t pos = base + (uint32_t)__popc(bal & lanemask_lt());
+            if (e != 0ull && pos < (uint32_t)kCap) s.cand[pos] = e;
+        }
+    }
+    __syncthreads();
+    const int m = (int)s.ncand < kCap ? (int)s.ncand : kCap;
+    if (m > kRankMax) select_many<kWarps, 0>(m, kk, s, lane, w);
+    else rank_into_list(s, m, kk, t, kThreads);
+    __syncthreads();
+    pass_emit(a, r, c, dtok, s);
+}
+
 // One-pass mode, all of it, for CTA bi of run r.  A CTA whose column has
 // others publishes its candidates unranked when there are at most 2 kk of
 // them (the merging CTA ranks them all), else its ranked top-kk.
-template <int L>
+template <int L, bool CLUSTER>
 __device__ __forceinline__ void one_pass(const RoundArgs &a, const GmRun &r, int bi, Smem &s)
 {
     const int t = threadIdx.x;
+    if constexpr (CLUSTER) cluster_arrive_relaxed();   // phase 1: this CTA runs
     const int64_t cols = r.cols;
     const int64_t c = udiv((int64_t)bi * cols, r.W);                   // this CTA's column
     const int64_t f = udiv(c * r.W + cols - 1, cols);                  // its first CTA
@@ -1464,6 +1598,10 @@ __device__ __forceinline__ void one_pass(const RoundArgs &a, const GmRun &r, int
     }
     uint32_t T;
     const int n = pass_cands<L>(r, q, j0, cb, s, T);
+    if constexpr (CLUSTER) {
+        cluster_finish(a, r, c, n, T, cb, lo, hi, greedy, dtok, s);
+        return;
+    }
     if (greedy) {
         // kk = 1, no id map: n <= 1, the best in s.cand[0]
         pass_lane(a, r, bi, c, n ? s.cand[0] : 0ull, dtok, s);
@@ -1493,7 +1631,7 @@ __device__ __forceinline__ void one_pass(const RoundArgs &a, const GmRun &r, int
 
 // MODE 0: slice mode; 1: column mode; 2 and 3: column mode with finishing
 // warps, 12 (2) or 8 (3) of the 16 streaming; 4: one pass, U loads per
-// thread.
+// thread; 7: one pass with a cluster of CTAs per column.
 template <int U, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_constant__ RoundArgs a)
 {
@@ -1511,8 +1649,8 @@ __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_co
         s.ncand = 0u;
         s.ngrp = 0u;
     }
-    if constexpr (MODE == 4) {
-        one_pass<U>(a, r, bi, s);
+    if constexpr (MODE == 4 || MODE == 7) {
+        one_pass<U, MODE == 7>(a, r, bi, s);
         return;
     }
     if constexpr (MODE == 1) {

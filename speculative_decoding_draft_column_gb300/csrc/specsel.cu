@@ -55,6 +55,7 @@ struct DeviceState {
     int sms = 0;
     int occ_w[2][2] = {{0, 0}, {0, 0}};   // per-warp kernel: resident CTAs per SM, [slots-1][mapped]
     int occ_c = 0;                        // CTA kernel: resident CTAs per SM
+    int clusters8 = 0;                    // group-maxima one pass in clusters of 8: clusters resident at once
     // Scratch: [col tickets and certificates | lane tickets | partial lists].
     // Each region keeps its place and capacity until the whole area is
     // reallocated (and zeroed), so a ticket is never laid over stale data.
@@ -125,6 +126,31 @@ spec_status device_state(DeviceState **out)
                                                           cta::kSmemBytes);
         if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
         if (d.occ_c < 1) d.occ_c = 1;
+        {
+            // clusters of 8 CTAs of the one-pass kernel that fit on the GPU at once
+            e = cudaFuncSetAttribute(reinterpret_cast<void *>(gm::spec_round_kernel<8, 7>),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gm::kSmemBytes);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+            cudaLaunchConfig_t cfg;
+            memset(&cfg, 0, sizeof cfg);
+            cfg.gridDim = dim3(8 * 19);
+            cfg.blockDim = dim3(gm::kThreads);
+            cfg.dynamicSmemBytes = gm::kSmemBytes;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 8;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<void *>(gm::spec_round_kernel<8, 7>), &cfg) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                n = 0;   // no clusters: the one-pass mode runs without them
+            }
+            d.clusters8 = n;
+        }
         void *kg[9] = {reinterpret_cast<void *>(gm::spec_round_kernel<8, 3>),
                        reinterpret_cast<void *>(gm::spec_round_kernel<8, 4>),
                        reinterpret_cast<void *>(gm::spec_round_kernel<16, 4>),
@@ -258,7 +284,7 @@ struct Plan {
     bool gm;          // the group-maxima kernel
     int gm_u;         // its batch width: 16-byte vectors per thread per batch (1, 2, 4 or 8; one pass: 8 or 16)
     int gm_mode;      // its mode: 0 slices, 1 whole columns per CTA, 2 / 3 whole columns with finishing warps,
-                      // 4 one pass (gm_u: loads per thread)
+                      // 4 one pass (gm_u: loads per thread), 7 one pass in clusters of 8 CTAs a column
     int slots;        // per-warp kernel: 2 for k > 32 (finer seed groups)
     bool mapped;
     int64_t grid;     // CTAs
@@ -283,6 +309,28 @@ bool plan_gm(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, int
     // the slice in registers, and a column's published entries (2 kk a CTA)
     // fitting the merge buffer.
     const int kmax = a.k > a.t_k ? a.k : a.t_k;
+    // One pass in clusters: eight CTAs a column, each column one cluster,
+    // when that keeps at least three quarters of the SMs busy, every
+    // cluster is resident at once, and a column's eighth fits 4,096 vectors.
+    {
+        constexpr int Q = 8;
+        const int64_t cols = (nv_d > 0 ? a.d_cols : 0) + (nv_t > 0 ? a.t_cols : 0);
+        const int64_t units = Q * cols;
+        const int stride = 2 * kmax + 2;
+        auto fits8 = [](int64_t nv, int64_t V) { return nv == 0 || ((V / 8 + 2 + Q - 1) / Q <= 512 * 8 && V / 8 >= Q); };
+        if (cols > 0 && cols <= d.clusters8 && units <= d.sms && 4 * units >= 3 * (int64_t)d.sms &&
+            fits8(nv_d, a.d_V) && fits8(nv_t, a.t_V) && units * stride <= max_partials) {
+            a.pstride = stride;
+            a.d_units = (int32_t)(nv_d > 0 ? Q * a.d_cols : 0);
+            a.t_units = (int32_t)(nv_t > 0 ? Q * a.t_cols : 0);
+            p.gm = true;
+            p.gm_u = 8;
+            p.gm_mode = 7;
+            p.grid = units;
+            p.partials = units * stride;
+            return true;
+        }
+    }
     for (int L : {8, 16}) {
         const int stride = 2 * kmax + 2;
         int32_t wd = 0, wt = 0;
@@ -429,7 +477,7 @@ Plan plan_round(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, 
 // overlaps the current launch's tail.
 template <typename K>
 cudaError_t launch_pdl(K kernel, unsigned grid, unsigned block, size_t smem, cudaStream_t stream, const RoundArgs &a,
-                       bool pdl)
+                       bool pdl, unsigned cluster = 0)
 {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
@@ -437,11 +485,22 @@ cudaError_t launch_pdl(K kernel, unsigned grid, unsigned block, size_t smem, cud
     cfg.blockDim = dim3(block);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (cluster) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = cluster;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
@@ -454,6 +513,7 @@ cudaError_t launch_plan(const Plan &p, const RoundArgs &a, cudaStream_t stream, 
     const unsigned g = (unsigned)p.grid;
     if (p.gm) {
         const size_t m = gm::kSmemBytes;
+        if (p.gm_mode == 7) return launch_pdl(gm::spec_round_kernel<8, 7>, g, gm::kThreads, m, stream, a, pdl, 8);
         if (p.gm_mode == 4 && p.gm_u == 16)
             return launch_pdl(gm::spec_round_kernel<16, 4>, g, gm::kThreads, m, stream, a, pdl);
         if (p.gm_mode == 4) return launch_pdl(gm::spec_round_kernel<8, 4>, g, gm::kThreads, m, stream, a, pdl);
