@@ -287,7 +287,10 @@ spec_status spec_shortlist_topk(const uint16_t *hidden, int64_t cols, int64_t d,
  *                       least one CTA): each CTA keeps its slice of one
  *                       column in registers and selects from them; a
  *                       column's CTAs publish their lists (greedy verify:
- *                       one argmax each) and the last to arrive merges.
+ *                       one argmax each) and the last to arrive merges --
+ *                       through the shared memory of a thread-block
+ *                       cluster of eight CTAs a column where that fills
+ *                       the GPU (about 15 to 19 columns).
  *                       Column mode (at least 3/4 as many columns as SMs,
  *                       columns of 32,768 to ~393,000 logits): each CTA
  *                       owns whole columns and keeps their keys in shared
