@@ -1443,40 +1443,11 @@ __device__ __forceinline__ unsigned long long *cluster_inbox(Smem &s)
 }
 static_assert(sizeof(Smem::keys) >= 8 * 2 * SPEC_MAX_K * sizeof(unsigned long long), "inbox of 8 CTAs");
 
-// Greedy verify of a lane from its columns' argmax entries, one per column
-// (value desc, id asc): the first CTA of each column's cluster publishes its
-// column's entry and takes the lane's ticket (the ticket of the lane's first
-// column); the last of them verifies the lane as pass_lane does.  dr: lane
-// j of warp 0 holds draft j.  Every thread of the CTA calls it.
-__device__ __forceinline__ void lane_of_columns(const RoundArgs &a, const GmRun &r, int64_t c, unsigned long long best,
-                                                int32_t dr, Smem &s)
-{
-    const int t = threadIdx.x, lane = t & 31;
-    const int gamma = a.gamma, gp1 = gamma + 1;
-    const int64_t ln = udiv(c, gp1), cf = ln * gp1;
-    unsigned long long *pl = a.partials + (int64_t)a.d_units * a.pstride;   // slot per target column
-    if (t == 0) {
-        __stcg(pl + c * a.pstride, best);
-        s.last[0] = atom_add_acq_rel(r.ticket + cf, 1u) == (uint32_t)gamma ? 1u : 0u;
-    }
-    __syncthreads();
-    if (s.last[0] == 0u || t >= 32) return;
-    const unsigned long long e = lane < gp1 ? (cf + lane == c ? best : __ldcg(pl + (cf + lane) * a.pstride)) : 0ull;
-    const int32_t token = lane < gp1 ? (int32_t)entry_id(e) : -1;
-    const uint32_t miss = __ballot_sync(kFull, lane < gamma && dr != token);
-    const int acc = miss ? __ffs(miss) - 1 : gamma;
-    if (lane < gp1) a.out_commit[ln * gp1 + lane] = lane <= acc ? token : -1;
-    count_lane(a.counters, gamma, acc, lane);
-    if (lane == 0) {
-        a.out_accept[ln] = acc;
-        r.ticket[cf] = 0u;   // ready for the next launch
-    }
-}
-
 // After pass_cands in a cluster of Q CTAs (one column c): the column's
 // entries meet in the first CTA, which merges and emits them (greedy verify:
-// the column's argmax goes on to lane_of_columns).  n, T: pass_cands'
-// results; [lo, hi): this CTA's part.
+// the column's argmax, with whether it equals the column's draft, goes to
+// the lane's fence-free epilogue, lane_done; dtok: lane j of warp 0 holds
+// draft j).  n, T: pass_cands' results; [lo, hi): this CTA's part.
 __device__ __forceinline__ void cluster_finish(const RoundArgs &a, const GmRun &r, int64_t c, int n, uint32_t T,
                                                int64_t cb, int64_t lo, int64_t hi, bool greedy, int32_t dtok,
                                                Smem &s)
@@ -1510,7 +1481,13 @@ __device__ __forceinline__ void cluster_finish(const RoundArgs &a, const GmRun &
                 best = o > best ? o : best;
             }
         }
-        lane_of_columns(a, r, c, best, dtok, s);
+        if (t < 32) {
+            const int gp1 = a.gamma + 1;
+            const int j = (int)(c - udiv(c, gp1) * gp1);   // the column's position in its lane
+            const int32_t token = (int32_t)entry_id(best);
+            const int32_t dj = __shfl_sync(kFull, dtok, j < 32 ? j : 0);
+            lane_done(a, c, token, j < a.gamma && dj == token, lane);
+        }
         return;
     }
     // merge: the nonzero entries into s.cand, ranked into s.wl[0], emitted
