@@ -27,7 +27,10 @@
 // per warp instead, merged at the end; more than the buffers hold, and the
 // CTA scans the whole column exactly.  A target column then goes to greedy
 // (or sampled) verify.  Every step of phase 2 issues its global loads
-// together: a few round trips to L2 in all.
+// together: a few round trips to L2 in all.  (That is slice mode; the
+// kernel's other modes -- one pass, whole columns, finishing warps -- are
+// described where they are defined, and the kernel's MODE parameter picks
+// one.)
 //
 // The operations are those of the other two kernels ("A drafter inside the
 // artifact", Ignis DFlash2 page, section "How it works"): top-k per draft
@@ -1181,11 +1184,13 @@ __device__ __forceinline__ void team_finish_all(const RoundArgs &a, const GmRun 
 // a column's CTAs split its vectors evenly: CTA b of W works on column
 // floor(b cols / W).  A CTA loads its slice, then selects the top-kk of it
 // by itself: the bound over its own section (or thread) maxima, its
-// elements that reach it, ranked.  No group key goes to global memory and
-// nothing is read twice.  A column with one CTA is finished right there;
-// otherwise every CTA publishes its sorted list and the one that takes the
-// column's ticket last merges them.
-
+// elements that reach it.  No group key goes to global memory and nothing
+// is read twice.  A column with one CTA is finished right there; otherwise
+// every CTA publishes its candidates (at most 2 kk, else its ranked top-kk)
+// and the one that takes the column's ticket last merges them -- or, with
+// a thread-block cluster per column (MODE 7), the first CTA of the cluster
+// merges them from its own shared memory.  Greedy verify publishes one
+// argmax entry per CTA and verifies a lane in one step.
 
 // The candidates of the part of a column held by this CTA's slice (vectors
 // j0 + u 512 + t in q[u], every element outside the part already the mask

@@ -291,12 +291,15 @@ struct Plan {
     int64_t partials; // entries (u64) of the partials area the launch uses
 };
 
-// The group-maxima kernel's plan: the batch width U and the CTAs of each run.
-// Every batch must touch two columns at most (V >= 8 * 512 * U).  Of the
-// widths that allow it, the widest unless a narrower one cuts the vectors
-// of the most loaded CTA by a third: a narrower batch balances small rounds
-// better but gives a column's finishing CTA more group keys to read.  False
-// if no width fits, or the group keys would not fit in max_partials entries.
+// The group-maxima kernel's plan: its mode and the CTAs of each run.  In
+// order: one pass in clusters of 8 CTAs a column; one pass (8 or 16 loads a
+// thread); whole columns per CTA (with finishing warps from 1.5 columns per
+// SM on); and, if slices is set, slice mode.  In slice mode every batch must
+// touch two columns at most (V >= 8 * 512 * U); of the widths that allow it,
+// the widest unless a narrower one cuts the vectors of the most loaded CTA
+// by a third: a narrower batch balances small rounds better but gives a
+// column's finishing CTA more group keys to read.  False if no mode fits, or
+// the scratch it needs would not fit in max_partials entries.
 bool plan_gm(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, int64_t max_partials, bool slices,
              Plan &p)
 {
