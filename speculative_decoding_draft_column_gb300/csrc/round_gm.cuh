@@ -538,7 +538,8 @@ struct Sel {
 // can hold a winner, and their elements >= T in the candidate buffer.  The
 // caller adds the candidates of later batches, if any, and calls rank_emit.
 template <int U, bool COLS>
-__device__ __forceinline__ Sel select_candidates(const RoundArgs &a, const GmRun &r, int64_t c, int rows, Smem &s)
+__device__ __forceinline__ Sel select_candidates(const RoundArgs &a, const GmRun &r, int64_t c, int rows, Smem &s,
+                                                 int first = 0)
 {
     constexpr int64_t B = 512 * U;
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
@@ -548,9 +549,10 @@ __device__ __forceinline__ Sel select_candidates(const RoundArgs &a, const GmRun
     int64_t jbase;
     int nb;
     const uint16_t *k0 = nullptr, *kr = nullptr;   // slice mode: keys of batch 0, and of batch i at kr[512 i]
-    if (COLS) {
+    if (COLS) {   // (from batch `first` of the column on: a part of it, in the cluster modes)
         jbase = (cb + r.mis) >> 3;
-        nb = (int)((((ce - 1 + r.mis) >> 3) - jbase) / B + 1);
+        nb = (int)((((ce - 1 + r.mis) >> 3) - jbase) / B + 1) - first;
+        jbase += (int64_t)first * B;
     } else {
         const int64_t bf = batch_of<U>(r, cb), bl = batch_of<U>(r, ce - 1);
         const bool hin = elem_lo<U>(r, bf) < cb;   // the column starts inside batch bf: its keys there are in H
@@ -1611,9 +1613,121 @@ __device__ __forceinline__ void one_pass(const RoundArgs &a, const GmRun &r, int
     if (s.last[0] != 0u) pass_merge(a, r, c, (r.draft ? 0 : a.d_units) + f, nc, per, dtok, s);
 }
 
+// ---- whole columns in thread-block clusters (MODE 8) --------------------------
+//
+// For rounds with fewer columns than three quarters of the SMs and too many
+// vectors for one pass (C3): each column is one cluster of Q CTAs (Q from 2
+// to 8, the fewest that keep three quarters of the SMs busy).  CTA q of the
+// cluster streams batches [q nb / Q, (q + 1) nb / Q) of the column as
+// column mode does, its group keys in its own shared memory, and selects
+// that part's top-kk with the same finish (bound, groups, ties cut within
+// the part, re-read, rank).  The Q lists then meet in the first CTA's inbox
+// -- past the end of Smem -- across a cluster barrier, and the first CTA
+// merges and emits them.  No tickets, no keys in global memory.
+constexpr size_t kInboxOff = (kSmemBytes + 15) & ~(size_t)15;
+constexpr size_t kSmemInboxBytes = kInboxOff + 8 * SPEC_MAX_K * sizeof(unsigned long long);
+static_assert(kSmemInboxBytes <= 227 * 1024, "one CTA per SM must fit");
+
+template <int U>
+__device__ __forceinline__ void cluster_columns(const RoundArgs &a, const GmRun &r, int bi, Smem &s,
+                                                unsigned char *base)
+{
+    constexpr int64_t B = 512 * U;
+    static_assert(U == 8, "one batch per step");
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    cluster_arrive_relaxed();   // phase 1: this CTA runs
+    uint32_t Q;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(Q));
+    const uint32_t rank = cluster_rank();
+    const int kk = r.kk;
+    const int64_t c = udiv(bi, Q);
+    const int64_t cb = c * r.V, ce = cb + r.V;
+    const int64_t jf = (cb + r.mis) >> 3, jl = (ce - 1 + r.mis) >> 3;
+    const int nb = (int)((jl - jf) / B + 1);
+    const int i_lo = (int)(rank * nb / Q), i_hi = (int)((rank + 1) * nb / Q);
+    if (t < kk) s.wl[0][t] = 0ull;   // the part's list: empty slots stay 0
+    // the part's batches, as stream_columns streams a column
+    for (int i0 = i_lo; i0 < i_hi; ++i0) {
+        uint4 q[kLoads];
+#pragma unroll
+        for (int v = 0; v < kLoads; ++v) {
+            const int64_t j = jf + (int64_t)i0 * B + v * 512 + t;
+            q[v] = (j > jf && j < jl && j >= r.jlo && j < r.jhi) ? __ldg(r.vb + j)
+                                                                  : make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
+        }
+        if (i0 == 0 || i0 + 1 >= nb) {
+            // the column's first and last vectors, element by element
+#pragma unroll
+            for (int v = 0; v < kLoads; ++v) {
+                const int64_t j = jf + (int64_t)i0 * B + v * 512 + t;
+                if (j <= jl && (j == jf || j == jl || j < r.jlo || j >= r.jhi)) q[v] = load_edge(r.buf, j, r.mis, cb, ce);
+            }
+        }
+        uint32_t m = kNaN2;
+#pragma unroll
+        for (int u = 0; u < U; ++u) m = bmax2(m, vmax(q[u]));
+        s.keys[i0 - i_lo][t] = (uint16_t)key_of(m);
+    }
+    const Sel sel = select_candidates<U, true>(a, r, c, i_hi - i_lo, s, i_lo);
+    // the part's top-kk, as rank_emit ranks a column (exactly over the part
+    // when the candidates overflow)
+    __syncthreads();
+    {
+        const int n = (int)s.ncand;
+        if (sel.lost || n > kCap) {
+            const int64_t e0 = 8 * (jf + (int64_t)i_lo * B) - r.mis, e1 = 8 * (jf + (int64_t)i_hi * B) - r.mis;
+            exact_scan<kWarps, 0>(view_of(r), e0 > cb ? e0 : cb, e1 < ce ? e1 : ce, cb, sel.T, s, lane, w);
+        } else if (n > kRankMax) {
+            select_many<kWarps, 0>(n, kk, s, lane, w);
+        } else {
+            rank_into_list(s, n, kk, t, kThreads);
+        }
+    }
+    __syncthreads();
+    unsigned long long *inbox = reinterpret_cast<unsigned long long *>(base + kInboxOff);
+    cluster_wait();   // every CTA of the cluster has started (phase 1, arrived at entry)
+    if (t < kk) st_cluster_u64(cluster_map(inbox + rank * kk + t, 0), s.wl[0][t]);
+    cluster_arrive();
+    cluster_wait();   // phase 2: the first CTA holds every list
+    if (rank != 0) return;
+    // merge: the nonzero entries into s.cand, ranked into s.wl[0]
+    if (t == 0) s.ncand = 0u;
+    __syncthreads();
+    const int n_all = (int)Q * kk;
+    {
+        const unsigned long long e = t < n_all ? inbox[t] : 0ull;   // n_all <= 8 * 64 = kThreads
+        const uint32_t bal = __ballot_sync(kFull, e != 0ull);
+        if (bal) {
+            uint32_t pos = 0;
+            if (lane == 0) pos = atomicAdd(&s.ncand, (uint32_t)__popc(bal));
+            pos = __shfl_sync(kFull, pos, 0) + (uint32_t)__popc(bal & lanemask_lt());
+            if (e != 0ull) s.cand[pos] = e;
+        }
+    }
+    __syncthreads();
+    const int m = (int)s.ncand;
+    if (m > kRankMax) select_many<kWarps, 0>(m, kk, s, lane, w);
+    else rank_into_list(s, m, kk, t, kThreads);
+    __syncthreads();
+    if (r.draft) {
+        for (int i = t; i < kk; i += kThreads) {
+            const unsigned long long e = s.wl[0][i];
+            a.out_vals[c * kk + i] = entry_raw(e);
+            a.out_ids[c * kk + i] = (int32_t)entry_id(e);
+        }
+    } else if (w == 0) {
+        int32_t token = (int32_t)entry_id(s.wl[0][0]);
+        bool accepted;
+        if (a.uniforms) accepted = sampled_decide(a, c, s.wl[0], kk, lane, token);
+        else accepted = __shfl_sync(kFull, sel.draft_tok, 0) == token;
+        lane_done(a, c, token, accepted, lane);
+    }
+}
+
 // MODE 0: slice mode; 1: column mode; 2 and 3: column mode with finishing
 // warps, 12 (2) or 8 (3) of the 16 streaming; 4: one pass, U loads per
-// thread; 7: one pass with a cluster of CTAs per column.
+// thread; 7: one pass with a cluster of CTAs per column; 8: whole columns,
+// a cluster of CTAs per column.
 template <int U, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_constant__ RoundArgs a)
 {
@@ -1633,6 +1747,10 @@ __global__ void __launch_bounds__(kThreads, 1) spec_round_kernel(const __grid_co
     }
     if constexpr (MODE == 4 || MODE == 7) {
         one_pass<U, MODE == 7>(a, r, bi, s);
+        return;
+    }
+    if constexpr (MODE == 8) {
+        cluster_columns<U>(a, r, bi, s, smem);
         return;
     }
     if constexpr (MODE == 1) {

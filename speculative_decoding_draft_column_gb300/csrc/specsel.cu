@@ -56,6 +56,7 @@ struct DeviceState {
     int occ_w[2][2] = {{0, 0}, {0, 0}};   // per-warp kernel: resident CTAs per SM, [slots-1][mapped]
     int occ_c = 0;                        // CTA kernel: resident CTAs per SM
     int clusters8 = 0;                    // group-maxima one pass in clusters of 8: clusters resident at once
+    int col_clusters[9] = {};             // group-maxima whole columns in clusters of Q (2..8): clusters resident at once
     // Scratch: [col tickets and certificates | lane tickets | partial lists].
     // Each region keeps its place and capacity until the whole area is
     // reallocated (and zeroed), so a ticket is never laid over stale data.
@@ -150,6 +151,21 @@ spec_status device_state(DeviceState **out)
                 n = 0;   // no clusters: the one-pass mode runs without them
             }
             d.clusters8 = n;
+            // whole columns in clusters of Q CTAs, Q = 2 .. 8
+            void *k8 = reinterpret_cast<void *>(gm::spec_round_kernel<8, 8>);
+            e = cudaFuncSetAttribute(k8, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gm::kSmemInboxBytes);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+            for (int q = 2; q <= 8; ++q) {
+                cfg.gridDim = dim3((unsigned)(q * (d.sms / q)));
+                cfg.dynamicSmemBytes = gm::kSmemInboxBytes;
+                at[0].val.clusterDim.x = (unsigned)q;
+                int m = 0;
+                if (cudaOccupancyMaxActiveClusters(&m, k8, &cfg) != cudaSuccess) {
+                    cudaGetLastError();
+                    m = 0;
+                }
+                d.col_clusters[q] = m;
+            }
         }
         void *kg[9] = {reinterpret_cast<void *>(gm::spec_round_kernel<8, 3>),
                        reinterpret_cast<void *>(gm::spec_round_kernel<8, 4>),
@@ -284,17 +300,20 @@ struct Plan {
     bool gm;          // the group-maxima kernel
     int gm_u;         // its batch width: 16-byte vectors per thread per batch (1, 2, 4 or 8; one pass: 8 or 16)
     int gm_mode;      // its mode: 0 slices, 1 whole columns per CTA, 2 / 3 whole columns with finishing warps,
-                      // 4 one pass (gm_u: loads per thread), 7 one pass in clusters of 8 CTAs a column
+                      // 4 one pass (gm_u: loads per thread), 7 one pass in clusters of 8 CTAs a column,
+                      // 8 whole columns in clusters of `cluster` CTAs
     int slots;        // per-warp kernel: 2 for k > 32 (finer seed groups)
     bool mapped;
     int64_t grid;     // CTAs
     int64_t partials; // entries (u64) of the partials area the launch uses
+    int cluster = 0;  // CTAs a thread-block cluster (the cluster modes; 0: none)
 };
 
 // The group-maxima kernel's plan: its mode and the CTAs of each run.  In
 // order: one pass in clusters of 8 CTAs a column; one pass (8 or 16 loads a
-// thread); whole columns per CTA (with finishing warps from 1.5 columns per
-// SM on); and, if slices is set, slice mode.  In slice mode every batch must
+// thread); whole columns in clusters of 2 to 8 CTAs; whole columns per CTA
+// (with finishing warps from 1.5 columns per SM on); and, if slices is set,
+// slice mode.  In slice mode every batch must
 // touch two columns at most (V >= 8 * 512 * U); of the widths that allow it,
 // the widest unless a narrower one cuts the vectors of the most loaded CTA
 // by a third: a narrower batch balances small rounds better but gives a
@@ -361,6 +380,34 @@ bool plan_gm(const DeviceState &d, RoundArgs &a, int64_t nv_d, int64_t nv_t, int
         return true;
     }
     if (vmin < gm::kMinV) return false;
+    // Whole columns in clusters: fewer columns than three quarters of the
+    // SMs, each column one cluster of Q CTAs (the fewest that keep three
+    // quarters of the SMs busy, at most 8), every CTA at least one batch of
+    // U = 8 and at most the kKeyRows whose keys it keeps in shared memory,
+    // every cluster resident at once.
+    {
+        int64_t vmax2 = 0;
+        if (nv_d > 0) vmax2 = a.d_V > vmax2 ? a.d_V : vmax2;
+        if (nv_t > 0) vmax2 = a.t_V > vmax2 ? a.t_V : vmax2;
+        const int64_t cols = (nv_d > 0 ? a.d_cols : 0) + (nv_t > 0 ? a.t_cols : 0);
+        const int64_t B = 512 * 8;
+        for (int Q = 2; Q <= 8 && cols > 0 && vmin >= 8 * B; ++Q) {
+            const int64_t units = Q * cols;
+            if (units > d.sms) break;
+            if (4 * units < 3 * (int64_t)d.sms) continue;
+            const int64_t nb_min = (vmin / 8) / B, nb_max = (vmax2 / 8 + 2 + B - 1) / B;
+            if (nb_min < Q || (nb_max + Q - 1) / Q > gm::kKeyRows || cols > d.col_clusters[Q]) break;
+            a.d_units = (int32_t)(nv_d > 0 ? Q * a.d_cols : 0);
+            a.t_units = (int32_t)(nv_t > 0 ? Q * a.t_cols : 0);
+            p.gm = true;
+            p.gm_u = 8;
+            p.gm_mode = 8;
+            p.cluster = Q;
+            p.grid = units;
+            p.partials = 0;
+            return true;
+        }
+    }
     // Column mode: at least three quarters as many columns as SMs, every
     // column at least one batch of U = 8 and at most the kKeyRows batches
     // whose keys a CTA keeps in shared memory.  Each CTA then owns whole
@@ -517,6 +564,9 @@ cudaError_t launch_plan(const Plan &p, const RoundArgs &a, cudaStream_t stream, 
     if (p.gm) {
         const size_t m = gm::kSmemBytes;
         if (p.gm_mode == 7) return launch_pdl(gm::spec_round_kernel<8, 7>, g, gm::kThreads, m, stream, a, pdl, 8);
+        if (p.gm_mode == 8)
+            return launch_pdl(gm::spec_round_kernel<8, 8>, g, gm::kThreads, gm::kSmemInboxBytes, stream, a, pdl,
+                              (unsigned)p.cluster);
         if (p.gm_mode == 4 && p.gm_u == 16)
             return launch_pdl(gm::spec_round_kernel<16, 4>, g, gm::kThreads, m, stream, a, pdl);
         if (p.gm_mode == 4) return launch_pdl(gm::spec_round_kernel<8, 4>, g, gm::kThreads, m, stream, a, pdl);

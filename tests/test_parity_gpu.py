@@ -510,6 +510,31 @@ def test_rounds_of_a_million_vectors(k):
     gu.assert_verify_equal(gu.run_verify_sampled(t4, d4, 1.0, 0.95, 20, u), (wa, wc), "sampled 4 lanes")
 
 
+@pytest.mark.parametrize("cols,k", [(60, 20), (40, 64), (40, 1)])
+def test_columns_in_clusters(cols, k):
+    """Rounds with fewer columns than three quarters of the SMs and too many
+    vectors for one pass, which the group-maxima kernel runs as whole columns
+    in thread-block clusters (2 or 3 CTAs a column): three-level ties and
+    noise columns, the top-k of each."""
+    V = synth.VOCAB
+    x = synth.levels_block(70 + cols + k, cols, V, [0.0, 1.0, -0.0])
+    x[1::2] = synth._draft_block(71 + cols + k, cols // 2, V, 3.0)
+    gu.assert_topk_equal(gu.run_topk(x, k, offset=k % 8), oracle.topk(x, k), f"{cols} columns k={k}")
+
+
+def test_verify_in_clusters():
+    """Greedy and sampled verify of 5 lanes of 8 columns at V = 248,046 (40
+    columns: three CTAs a column in a cluster), half the lanes accepting
+    every draft."""
+    V, lanes, gamma = synth.VOCAB, 5, 7
+    t, d, _, _ = synth.planted_verify(80, lanes, gamma, V)
+    gu.assert_verify_equal(gu.run_verify(t, d), oracle.verify(t, d), "greedy, 40 columns")
+    u = synth.rng(81, 0).random((lanes, gamma + 1, 2))
+    wa, wc, margin = oracle.sampled_verify(t, d, 1.0, 0.95, 20, u)
+    assert margin > 1e-9
+    gu.assert_verify_equal(gu.run_verify_sampled(t, d, 1.0, 0.95, 20, u), (wa, wc), "sampled, 40 columns")
+
+
 def test_verify_columns_over_many_units():
     """A lane of four target columns of a million logits each (greedy and
     sampled): every column is shared by dozens of units."""
