@@ -291,6 +291,11 @@ spec_status spec_shortlist_topk(const uint16_t *hidden, int64_t cols, int64_t d,
  *                       through the shared memory of a thread-block
  *                       cluster of eight CTAs a column where that fills
  *                       the GPU (about 15 to 19 columns).
+ *                       Columns in clusters (fewer columns, too many
+ *                       logits for one pass): each column one cluster of
+ *                       2 to 8 CTAs, each streaming part of it with its
+ *                       keys in shared memory, the parts' lists merged in
+ *                       the cluster's first CTA.
  *                       Column mode (at least 3/4 as many columns as SMs,
  *                       columns of 32,768 to ~393,000 logits): each CTA
  *                       owns whole columns and keeps their keys in shared
