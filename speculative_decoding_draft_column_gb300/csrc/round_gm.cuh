@@ -325,21 +325,6 @@ __device__ __forceinline__ uint32_t half_of(const uint4 &q, int e)
     return (e & 1) ? (w >> 16) : (w & 0xFFFFu);
 }
 
-// q (elements [g0, g0 + 8), counted like lo and hi) with its elements
-// outside [lo, hi) masked
-__device__ __forceinline__ uint4 mask_vec(const uint4 &q, int g0, int lo, int hi)
-{
-    const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-        const int p = g0 + 2 * h;
-        const bool in0 = p >= lo && p < hi, in1 = p + 1 >= lo && p + 1 < hi;
-        o[h] = (in0 ? (wd[h] & 0xFFFFu) : 0x7FFFu) | (in1 ? (wd[h] & 0xFFFF0000u) : 0x7FFF0000u);
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
 // Vector u of a thread's registers, u not known at compile time (selects:
 // a short, branch-free sequence instead of a copy of the caller's code per
 // vector).
